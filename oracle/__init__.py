@@ -1,0 +1,166 @@
+"""fp64 CPU oracle for causal SWA, local+strided and differential attention.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+``cpu_baseline`` / reference leg of ``bench.py`` may import this package.  The
+CUDA product path never imports it and it never imports the product package.
+
+The arithmetic lives in ``swa_oracle.c`` (plain C, fp64, OpenMP over rows);
+this module compiles it with gcc on first use and marshals numpy arrays.
+Inputs may be fp64 arrays or bf16 bit patterns (uint16, widened exactly).
+
+Parity status per function (what pins it is listed in the tests):
+  attn(kind="window")  pinned: worked example of the SWA note §3.2, pair counts
+                       of §4.1, the W=4 window figure of the attention-variants
+                       lesson, W >= N, W = 1, uniform-key mean, brute force.
+  attn(kind="strided") pinned: brute force of the lesson's strided mask,
+                       stride = 1, stride >= N, W >= N special cases, closed-form
+                       pair count.
+  attn(kind="causal")  pinned: worked example (full causal 38/8), brute force.
+  diff                 pinned: lambda = 0, (Q2, K2) = (Q1, K1), affinity in
+                       lambda, brute force of the dense (A1 - lambda A2) V.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "swa_oracle.c")
+_LIB = os.path.join(_HERE, "_liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+KINDS = {"window": 0, "strided": 1, "causal": 2}
+
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+
+
+def build(force: bool = False) -> str:
+    """Compile the C oracle into ``oracle/_liboracle.so`` (gcc, -O2, OpenMP)."""
+    if not force and os.path.exists(_LIB) and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC):
+        return _LIB
+    tmp = _LIB + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-fPIC", "-shared", "-fopenmp", "-std=c99", "-o", tmp, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB)
+            lib.oracle_attn.restype = ctypes.c_int
+            lib.oracle_attn.argtypes = [ctypes.c_int, _P, _P, _P, _P, _I64, _I64, _I64, _I64,
+                                        _I64, _I64, _I64, ctypes.c_double, _P, _I64,
+                                        ctypes.c_int]
+            lib.oracle_diff.restype = ctypes.c_int
+            lib.oracle_diff.argtypes = [_P, _P, _P, _P, _P, ctypes.c_double, _P, _I64, _I64,
+                                        _I64, _I64, _I64, ctypes.c_double, _P, _I64,
+                                        ctypes.c_int]
+            lib.oracle_weights_row.restype = ctypes.c_int
+            lib.oracle_weights_row.argtypes = [ctypes.c_int, _P, _P, _I64, _I64, _I64, _I64,
+                                               _I64, _I64, _I64, ctypes.c_double, _I64, _I64,
+                                               _I64, _P]
+            lib.oracle_pair_count.restype = ctypes.c_int64
+            lib.oracle_pair_count.argtypes = [ctypes.c_int, _I64, _I64, _I64]
+            lib.oracle_mask_row.restype = ctypes.c_int
+            lib.oracle_mask_row.argtypes = [ctypes.c_int, _I64, _I64, _I64, _I64, _P]
+            lib.oracle_max_threads.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def _f64(x: np.ndarray) -> np.ndarray:
+    x = np.asarray(x)
+    if x.dtype == np.uint16:  # bf16 bit patterns: widen exactly
+        x = (x.astype(np.uint32) << 16).view(np.float32)
+    return np.ascontiguousarray(x, dtype=np.float64)
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _rows_arg(rows, N):
+    if rows is None:
+        return None, N
+    r = np.ascontiguousarray(rows, dtype=np.int64)
+    return r, int(r.size)
+
+
+def attn(q, k, v, W: int, scale: float, kind: str = "window", stride: int = 0,
+         rows=None, nthreads: int = 0) -> np.ndarray:
+    """Masked attention in fp64.  q: [B, Hq, N, d]; k, v: [B, Hkv, N, d].
+
+    Returns [B, Hq, nrows, d] (nrows = N when ``rows`` is None)."""
+    lib = _load()
+    q64, k64, v64 = _f64(q), _f64(k), _f64(v)
+    B, Hq, N, d = q64.shape
+    Hkv = k64.shape[1]
+    r, nrows = _rows_arg(rows, N)
+    out = np.empty((B, Hq, nrows, d), dtype=np.float64)
+    rc = lib.oracle_attn(KINDS[kind], _ptr(q64), _ptr(k64), _ptr(v64), _ptr(out), B, Hq, Hkv,
+                         N, d, int(W), int(stride), float(scale),
+                         None if r is None else _ptr(r), nrows, int(nthreads))
+    if rc != 0:
+        raise ValueError(f"oracle_attn rejected its arguments (code {rc})")
+    return out
+
+
+def diff(q1, k1, q2, k2, v, lam: float, scale: float, rows=None, nthreads: int = 0):
+    """Differential causal attention (A1 - lam A2) V in fp64."""
+    lib = _load()
+    a = [_f64(x) for x in (q1, k1, q2, k2, v)]
+    B, Hq, N, d = a[0].shape
+    Hkv = a[1].shape[1]
+    r, nrows = _rows_arg(rows, N)
+    out = np.empty((B, Hq, nrows, d), dtype=np.float64)
+    rc = lib.oracle_diff(*[_ptr(x) for x in a], float(lam), _ptr(out), B, Hq, Hkv, N, d,
+                         float(scale), None if r is None else _ptr(r), nrows, int(nthreads))
+    if rc != 0:
+        raise ValueError(f"oracle_diff rejected its arguments (code {rc})")
+    return out
+
+
+def weights_row(q, k, W: int, scale: float, b: int, h: int, i: int, kind: str = "window",
+                stride: int = 0) -> np.ndarray:
+    """Softmax weights of query row i (length N; keys after i are 0)."""
+    lib = _load()
+    q64, k64 = _f64(q), _f64(k)
+    B, Hq, N, d = q64.shape
+    Hkv = k64.shape[1]
+    w = np.empty(N, dtype=np.float64)
+    rc = lib.oracle_weights_row(KINDS[kind], _ptr(q64), _ptr(k64), B, Hq, Hkv, N, d, int(W),
+                                int(stride), float(scale), b, h, i, _ptr(w))
+    if rc != 0:
+        raise ValueError(f"oracle_weights_row rejected its arguments (code {rc})")
+    return w
+
+
+def pair_count(N: int, W: int, kind: str = "window", stride: int = 0) -> int:
+    """Allowed (i, j) pairs of one head, counted from the mask rows."""
+    n = _load().oracle_pair_count(KINDS[kind], N, W, stride)
+    if n < 0:
+        raise ValueError("bad pair_count arguments")
+    return int(n)
+
+
+def mask_row(N: int, W: int, i: int, kind: str = "window", stride: int = 0) -> np.ndarray:
+    """Row i of the mask as a bool array (True = allowed)."""
+    a = np.zeros(N, dtype=np.uint8)
+    rc = _load().oracle_mask_row(KINDS[kind], N, W, stride, i, _ptr(a))
+    if rc != 0:
+        raise ValueError("bad mask_row arguments")
+    return a.astype(bool)
+
+
+def max_threads() -> int:
+    return int(_load().oracle_max_threads())

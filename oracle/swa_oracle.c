@@ -1,0 +1,245 @@
+/*
+ * swa_oracle.c -- plain fp64 CPU oracle for causal sliding-window attention,
+ * local+strided sparse causal attention and differential causal attention.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the test suite, the smoke check and the
+ * CPU-baseline leg of the benchmark may call this code.  It shares nothing with
+ * the CUDA path (no headers, no helpers, no tables) and the CUDA path never
+ * calls it.
+ *
+ * Sources (web pages, cited by title and section):
+ *   [AV]   "注意力变体——滑动窗口、稀疏、差分" (Attention variants lesson,
+ *          ai-engineering.com.cn, Phase 07 lesson 15), "Build it" steps 1-4.
+ *   [AVpt] "Variantes de Atenção — Janela Deslizante, Esparsa, Diferencial"
+ *          (ai-engineering.academy), "Atenção Diferencial" (the A1, A2,
+ *          DiffAttn formulas) and "Implemente" steps 1-4.
+ *   [SWA]  "SWA：滑动窗口注意力与跨层信息传递" (lizn-zn.github.io),
+ *          §3.1 (window set N_W(i), mask M^SWA, Attention_SWA), §4.1 (pair counts).
+ *
+ * What it computes, for every batch b, query head h (key/value head h / g with
+ * g = Hq / Hkv) and query row i (0-indexed):
+ *   1. the row i of the additive mask, built the way the pages build it:
+ *      every entry -inf, then 0 on the allowed keys
+ *        causal  : j <= i                                   ([AV] step 1)
+ *        window  : max(0, i - W + 1) <= j <= i               ([AV] step 2, [SWA] §3.1)
+ *        strided : window  plus  j = 0, s, 2s, ... <= i       ([AV] step 3)
+ *   2. z_j = scale * (q_i . k_j) + M_ij in fp64 (masked j give -inf and are not
+ *      dotted: -inf + finite = -inf),
+ *   3. a two-pass softmax over the row: m = max_j z_j, p_j = exp(z_j - m),
+ *      a_j = p_j / sum_j p_j  (each row renormalises inside its own mask,
+ *      [SWA] §3.1),
+ *   4. out_i = sum_j a_j v_j.
+ *   Differential ([AVpt] "Atenção Diferencial"): out_i = sum_j (a1_j - lambda a2_j) v_j
+ *   with a1 from (q1, k1) and a2 from (q2, k2), both under the causal mask.
+ *
+ * Inputs are fp64 arrays in layout [B, H, N, d] (q: H = Hq, k and v: H = Hkv).
+ * Output is fp64 [B, Hq, nrows, d] where nrows rows (a list, or all N) are computed.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+enum { MASK_WINDOW = 0, MASK_STRIDED = 1, MASK_CAUSAL = 2 };
+
+/* Row i of the additive mask, for keys 0..i (keys j > i are -inf in every mask
+ * kind, so they are neither stored nor visited). */
+static void mask_row(int kind, int64_t i, int64_t window, int64_t stride, double* M) {
+    for (int64_t j = 0; j <= i; ++j) M[j] = -INFINITY;
+    if (kind == MASK_CAUSAL) {
+        for (int64_t j = 0; j <= i; ++j) M[j] = 0.0;
+        return;
+    }
+    int64_t lo = i - window + 1;
+    if (lo < 0) lo = 0;
+    for (int64_t j = lo; j <= i; ++j) M[j] = 0.0;
+    if (kind == MASK_STRIDED) {
+        for (int64_t j = 0; j <= i; j += stride) M[j] = 0.0;
+    }
+}
+
+/* Softmax weights a_j (j = 0..i) of one row: steps 2-3 above.  z is scratch. */
+static void softmax_row(const double* qi, const double* kh, int64_t d, int64_t i, double scale,
+                        const double* M, double* z, double* a) {
+    double m = -INFINITY;
+    for (int64_t j = 0; j <= i; ++j) {
+        if (M[j] == 0.0) {
+            const double* kj = kh + j * d;
+            double dot = 0.0;
+            for (int64_t t = 0; t < d; ++t) dot += qi[t] * kj[t];
+            z[j] = scale * dot + M[j];
+        } else {
+            z[j] = -INFINITY;
+        }
+        if (z[j] > m) m = z[j];
+    }
+    double l = 0.0;
+    for (int64_t j = 0; j <= i; ++j) {
+        a[j] = (z[j] == -INFINITY) ? 0.0 : exp(z[j] - m);
+        l += a[j];
+    }
+    for (int64_t j = 0; j <= i; ++j) a[j] /= l;
+}
+
+static int check_shape(int64_t B, int64_t Hq, int64_t Hkv, int64_t N, int64_t d) {
+    if (B < 1 || Hq < 1 || Hkv < 1 || N < 1 || d < 1) return 2;
+    if (Hq % Hkv != 0) return 2;
+    return 0;
+}
+
+/*
+ * Masked attention, one of the three mask kinds.  rows == NULL computes all N
+ * rows (nrows must then equal N).  nthreads <= 0 uses the OpenMP default.
+ * Returns 0, or 2 on a bad shape / row index.
+ */
+int oracle_attn(int kind, const double* q, const double* k, const double* v, double* out,
+                int64_t B, int64_t Hq, int64_t Hkv, int64_t N, int64_t d, int64_t W,
+                int64_t stride, double scale, const int64_t* rows, int64_t nrows,
+                int nthreads) {
+    if (check_shape(B, Hq, Hkv, N, d)) return 2;
+    if (kind != MASK_WINDOW && kind != MASK_STRIDED && kind != MASK_CAUSAL) return 2;
+    if (kind != MASK_CAUSAL && W < 1) return 2;
+    if (kind == MASK_STRIDED && stride < 1) return 2;
+    if (rows == NULL && nrows != N) return 2;
+    for (int64_t r = 0; rows && r < nrows; ++r)
+        if (rows[r] < 0 || rows[r] >= N) return 2;
+    const int64_t g = Hq / Hkv;
+    const int64_t total = B * Hq * nrows;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#endif
+#pragma omp parallel
+    {
+        double* M = (double*)malloc(sizeof(double) * (size_t)N);
+        double* z = (double*)malloc(sizeof(double) * (size_t)N);
+        double* a = (double*)malloc(sizeof(double) * (size_t)N);
+#pragma omp for schedule(dynamic, 8)
+        for (int64_t t = 0; t < total; ++t) {
+            const int64_t r = t % nrows;
+            const int64_t h = (t / nrows) % Hq;
+            const int64_t b = t / (nrows * Hq);
+            const int64_t i = rows ? rows[r] : r;
+            const int64_t hk = h / g;
+            const double* qi = q + ((b * Hq + h) * N + i) * d;
+            const double* kh = k + (b * Hkv + hk) * N * d;
+            const double* vh = v + (b * Hkv + hk) * N * d;
+            mask_row(kind, i, W, stride, M);
+            softmax_row(qi, kh, d, i, scale, M, z, a);
+            double* o = out + ((b * Hq + h) * nrows + r) * d;
+            for (int64_t c = 0; c < d; ++c) o[c] = 0.0;
+            for (int64_t j = 0; j <= i; ++j) {
+                if (a[j] == 0.0) continue;
+                const double* vj = vh + j * d;
+                for (int64_t c = 0; c < d; ++c) o[c] += a[j] * vj[c];
+            }
+        }
+        free(M);
+        free(z);
+        free(a);
+    }
+    return 0;
+}
+
+/*
+ * Differential causal attention: out = (A1 - lambda A2) V, A1 = softmax_causal(Q1 K1^T * scale),
+ * A2 = softmax_causal(Q2 K2^T * scale).  Same layouts and row selection as oracle_attn.
+ */
+int oracle_diff(const double* q1, const double* k1, const double* q2, const double* k2,
+                const double* v, double lambda, double* out, int64_t B, int64_t Hq, int64_t Hkv,
+                int64_t N, int64_t d, double scale, const int64_t* rows, int64_t nrows,
+                int nthreads) {
+    if (check_shape(B, Hq, Hkv, N, d)) return 2;
+    if (rows == NULL && nrows != N) return 2;
+    for (int64_t r = 0; rows && r < nrows; ++r)
+        if (rows[r] < 0 || rows[r] >= N) return 2;
+    const int64_t g = Hq / Hkv;
+    const int64_t total = B * Hq * nrows;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#endif
+#pragma omp parallel
+    {
+        double* M = (double*)malloc(sizeof(double) * (size_t)N);
+        double* z = (double*)malloc(sizeof(double) * (size_t)N);
+        double* a1 = (double*)malloc(sizeof(double) * (size_t)N);
+        double* a2 = (double*)malloc(sizeof(double) * (size_t)N);
+#pragma omp for schedule(dynamic, 8)
+        for (int64_t t = 0; t < total; ++t) {
+            const int64_t r = t % nrows;
+            const int64_t h = (t / nrows) % Hq;
+            const int64_t b = t / (nrows * Hq);
+            const int64_t i = rows ? rows[r] : r;
+            const int64_t hk = h / g;
+            const size_t qoff = (size_t)(((b * Hq + h) * N + i) * d);
+            const size_t koff = (size_t)((b * Hkv + hk) * N * d);
+            mask_row(MASK_CAUSAL, i, 0, 0, M);
+            softmax_row(q1 + qoff, k1 + koff, d, i, scale, M, z, a1);
+            softmax_row(q2 + qoff, k2 + koff, d, i, scale, M, z, a2);
+            double* o = out + ((b * Hq + h) * nrows + r) * d;
+            for (int64_t c = 0; c < d; ++c) o[c] = 0.0;
+            for (int64_t j = 0; j <= i; ++j) {
+                const double w = a1[j] - lambda * a2[j];
+                const double* vj = v + koff + (size_t)(j * d);
+                for (int64_t c = 0; c < d; ++c) o[c] += w * vj[c];
+            }
+        }
+        free(M);
+        free(z);
+        free(a1);
+        free(a2);
+    }
+    return 0;
+}
+
+/* The softmax weights of one row (length N; keys after i are 0). */
+int oracle_weights_row(int kind, const double* q, const double* k, int64_t B, int64_t Hq,
+                       int64_t Hkv, int64_t N, int64_t d, int64_t W, int64_t stride,
+                       double scale, int64_t b, int64_t h, int64_t i, double* w) {
+    if (check_shape(B, Hq, Hkv, N, d)) return 2;
+    if (b < 0 || b >= B || h < 0 || h >= Hq || i < 0 || i >= N) return 2;
+    if (kind != MASK_CAUSAL && W < 1) return 2;
+    if (kind == MASK_STRIDED && stride < 1) return 2;
+    const int64_t hk = h / (Hq / Hkv);
+    double* M = (double*)malloc(sizeof(double) * (size_t)N);
+    double* z = (double*)malloc(sizeof(double) * (size_t)N);
+    mask_row(kind, i, W, stride, M);
+    for (int64_t j = 0; j < N; ++j) w[j] = 0.0;
+    softmax_row(q + ((b * Hq + h) * N + i) * d, k + (b * Hkv + hk) * N * d, d, i, scale, M, z, w);
+    free(M);
+    free(z);
+    return 0;
+}
+
+/* Number of allowed (i, j) pairs of one head: the zeros of the mask, counted row by row. */
+int64_t oracle_pair_count(int kind, int64_t N, int64_t W, int64_t stride) {
+    if (N < 1 || (kind != MASK_CAUSAL && W < 1) || (kind == MASK_STRIDED && stride < 1)) return -1;
+    double* M = (double*)malloc(sizeof(double) * (size_t)N);
+    int64_t count = 0;
+    for (int64_t i = 0; i < N; ++i) {
+        mask_row(kind, i, W, stride, M);
+        for (int64_t j = 0; j <= i; ++j) count += (M[j] == 0.0);
+    }
+    free(M);
+    return count;
+}
+
+/* Row i of the mask as 0/1 allowed flags (length N), for pattern checks. */
+int oracle_mask_row(int kind, int64_t N, int64_t W, int64_t stride, int64_t i, uint8_t* allowed) {
+    if (i < 0 || i >= N) return 2;
+    double* M = (double*)malloc(sizeof(double) * (size_t)N);
+    mask_row(kind, i, W, stride, M);
+    for (int64_t j = 0; j < N; ++j) allowed[j] = (j <= i && M[j] == 0.0) ? 1 : 0;
+    free(M);
+    return 0;
+}
+
+int oracle_max_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}

@@ -1,0 +1,59 @@
+"""Closed-form counts of allowed (query, key) pairs and the useful FLOPs built on them.
+
+The pair counts follow the SWA note ("SWA：滑动窗口注意力与跨层信息传递", §4.1):
+a full causal head of length T has T(T+1)/2 allowed pairs and a window of W
+positions (counting the current one) has sum_i min(i, W) = T W - W(W-1)/2 for
+T >= W.  The strided count adds, for every row i, the multiples of the stride
+that lie before the row's window (the local+strided mask of the attention-
+variants lesson, "Build it" step 3).
+
+Useful FLOPs count only the allowed pairs: 2 d for q.k plus 2 d for p.v, i.e.
+4 d per pair per query head; the differential variant has two attention maps
+and counts 8 d per causal pair.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+
+def pairs_window(N: int, W: int) -> int:
+    """Allowed pairs of one head under the causal window of W positions."""
+    if W >= N:
+        return N * (N + 1) // 2
+    return N * W - W * (W - 1) // 2
+
+
+def pairs_causal(N: int) -> int:
+    return N * (N + 1) // 2
+
+
+def pairs_strided(N: int, W: int, stride: int) -> int:
+    """Window pairs plus, per row, the keys 0, s, 2s, ... that precede the window."""
+    i = np.arange(N, dtype=np.int64)
+    lo = np.maximum(0, i - W + 1)
+    win = np.minimum(i + 1, W)
+    extra = np.where(lo > 0, (lo - 1) // stride + 1, 0)
+    return int(win.sum() + extra.sum())
+
+
+def useful_flops(kind: str, B: int, Hq: int, N: int, d: int, W: int, stride: int = 0) -> float:
+    """Band-only useful FLOPs of one forward call."""
+    if kind == "swa":
+        p = pairs_window(N, W)
+        return 4.0 * d * p * B * Hq
+    if kind == "strided":
+        p = pairs_strided(N, W, stride)
+        return 4.0 * d * p * B * Hq
+    if kind == "diff":
+        p = pairs_causal(N)
+        return 8.0 * d * p * B * Hq
+    raise ValueError(kind)
+
+
+def algorithmic_bytes(kind: str, B: int, Hq: int, Hkv: int, N: int, d: int) -> int:
+    """HBM bytes that every correct implementation must move: inputs read once, output written once (bf16)."""
+    q = B * Hq * N * d * 2
+    kv = B * Hkv * N * d * 2
+    if kind == "diff":
+        return 2 * q + 3 * kv + q  # q1, q2, k1, k2, v, out
+    return q + 2 * kv + q  # q, k, v, out

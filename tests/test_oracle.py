@@ -1,0 +1,358 @@
+"""Pins for the fp64 oracle: each test checks it against something other than itself.
+
+Sources: the SWA note ("SWA：滑动窗口注意力与跨层信息传递", §3.1 mask, §3.2 worked
+example, §4.1 pair counts), the attention-variants lesson ("注意力变体——滑动窗口、
+稀疏、差分", concept figure and "Build it" steps 1-4, FlexAttention predicate in
+"Use it") and its Portuguese translation ("Variantes de Atenção", "Atenção
+Diferencial" formulas).
+"""
+import math
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+from conftest import golden_path, read_kv_fixture
+from sparse_causal_attention_swa_b300 import flops
+
+pytestmark = pytest.mark.filterwarnings("ignore::RuntimeWarning")
+
+
+# ---------------------------------------------------------------------------------------------
+# An independent dense brute force: the mask is built as a full N x N matrix the way the lesson
+# describes it (start from -inf, open the allowed keys), and softmax(Q K^T * scale + M) V is
+# evaluated with numpy in fp64.  No code is shared with the C oracle.
+# ---------------------------------------------------------------------------------------------
+def dense_mask(n, kind, window=0, stride=0):
+    M = np.full((n, n), -np.inf)
+    for i in range(n):
+        if kind == "causal":
+            M[i, : i + 1] = 0.0
+            continue
+        M[i, max(0, i - window + 1): i + 1] = 0.0
+        if kind == "strided":
+            M[i, np.arange(0, i + 1, stride)] = 0.0
+    return M
+
+
+def dense_softmax(Q, K, scale, M):
+    S = Q @ K.T * scale + M
+    S = S - S.max(axis=1, keepdims=True)
+    P = np.exp(S)
+    return P / P.sum(axis=1, keepdims=True)
+
+
+def dense_attn(q, k, v, scale, kind, window=0, stride=0):
+    B, Hq, N, d = q.shape
+    g = Hq // k.shape[1]
+    M = dense_mask(N, kind, window, stride)
+    out = np.empty_like(q)
+    for b in range(B):
+        for h in range(Hq):
+            A = dense_softmax(q[b, h], k[b, h // g], scale, M)
+            out[b, h] = A @ v[b, h // g]
+    return out
+
+
+def rand(rng, *shape):
+    return rng.standard_normal(shape)
+
+
+# ---------------------------------------------------------------------------------------------
+# Worked example (SWA note §3.2) and pair counts (§4.1)
+# ---------------------------------------------------------------------------------------------
+def _frac(s):
+    return float(Fraction(s))
+
+
+def _worked_inputs(v_key):
+    fx = read_kv_fixture("swa_note_worked_example.txt")
+    kv = {"0": 0.0, "ln2": math.log(2.0), "ln3": math.log(3.0)}
+    k = np.array([kv[t] for t in fx["k"].split()], dtype=np.float64)
+    v = np.array([float(t) for t in fx[v_key].split()], dtype=np.float64)
+    q = np.zeros(5)
+    q[4] = float(fx["q5"])
+    return fx, q.reshape(1, 1, 5, 1), k.reshape(1, 1, 5, 1), v.reshape(1, 1, 5, 1)
+
+
+@pytest.mark.parametrize("v_key", ["v_split_a", "v_split_b"])
+def test_worked_example_window_and_full(oracle_mod, v_key):
+    fx, q, k, v = _worked_inputs(v_key)
+    W = int(fx["W"])
+    out_w = oracle_mod.attn(q, k, v, W, 1.0, kind="window")[0, 0, 4, 0]
+    assert abs(out_w - _frac(fx["out_window"])) < 1e-14
+    for W_full in (5, 6, 100):
+        out_f = oracle_mod.attn(q, k, v, W_full, 1.0, kind="window")[0, 0, 4, 0]
+        assert abs(out_f - _frac(fx["out_full"])) < 1e-14
+    out_c = oracle_mod.attn(q, k, v, 0, 1.0, kind="causal")[0, 0, 4, 0]
+    assert abs(out_c - _frac(fx["out_full"])) < 1e-14
+
+
+def test_worked_example_weights(oracle_mod):
+    fx, q, k, _ = _worked_inputs("v_split_a")
+    w = oracle_mod.weights_row(q, k, int(fx["W"]), 1.0, 0, 0, 4, kind="window")
+    expect = [0.0, 0.0] + [_frac(t) for t in fx["weights_window"].split()]
+    np.testing.assert_allclose(w, expect, rtol=0, atol=1e-15)
+
+
+def test_pair_counts_worked_example(oracle_mod):
+    fx = read_kv_fixture("swa_note_worked_example.txt")
+    assert oracle_mod.pair_count(5, 3, "window") == int(fx["pairs_window"])
+    assert oracle_mod.pair_count(5, 0, "causal") == int(fx["pairs_full"])
+    assert flops.pairs_window(5, 3) == int(fx["pairs_window"])
+    assert flops.pairs_causal(5) == int(fx["pairs_full"])
+
+
+@pytest.mark.parametrize("N,W", [(1, 1), (7, 1), (64, 63), (64, 64), (64, 65), (100, 7),
+                                 (8192, 1024), (1000, 999), (513, 64)])
+def test_pair_count_closed_form(oracle_mod, N, W):
+    # SWA note §4.1: sum_i min(i, W) = T W - W (W - 1) / 2 for T >= W
+    assert oracle_mod.pair_count(N, W, "window") == flops.pairs_window(N, W)
+
+
+def test_pages_8192_1024_figure(oracle_mod):
+    # The lesson's "about 1024 x 8192 entries" is the rounded form of the exact count.
+    n = oracle_mod.pair_count(8192, 1024, "window")
+    assert n == 8192 * 1024 - 1024 * 1023 // 2 == 7_864_832
+    assert abs(n / (1024 * 8192) - 1) < 0.07
+
+
+# ---------------------------------------------------------------------------------------------
+# Mask convention: the window figure, the FlexAttention predicate, W >= N, W = 1
+# ---------------------------------------------------------------------------------------------
+def _read_figure():
+    sections, cur = {}, None
+    with open(golden_path("av_window_figure.txt"), encoding="utf-8") as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            if line.startswith("["):
+                cur = line.strip("[]").split()[0]
+                sections[cur] = {}
+                continue
+            row, keys = line.split(":")
+            sections[cur][int(row)] = [int(t) for t in keys.split()]
+    return sections
+
+
+def test_window_figure(oracle_mod):
+    fig = _read_figure()
+    for i, keys in fig["sliding_window"].items():
+        assert np.flatnonzero(oracle_mod.mask_row(8, 4, i, "window")).tolist() == keys
+    for i, keys in fig["full_causal"].items():
+        assert np.flatnonzero(oracle_mod.mask_row(8, 0, i, "causal")).tolist() == keys
+
+
+@pytest.mark.parametrize("N,W", [(8, 4), (50, 1), (50, 7), (50, 50), (50, 80)])
+def test_flex_predicate(oracle_mod, N, W):
+    # FlexAttention mask function of the lesson's "Use it": (q - kv < W) & (q >= kv)
+    for i in range(N):
+        pred = np.array([(i - j < W) and (i >= j) for j in range(N)])
+        assert (oracle_mod.mask_row(N, W, i, "window") == pred).all()
+
+
+def test_window_does_not_wrap(oracle_mod):
+    # SWA note §1: at the start of the sequence the window uses the positions that exist
+    for i in range(5):
+        assert np.flatnonzero(oracle_mod.mask_row(10, 5, i, "window")).tolist() == list(range(i + 1))
+
+
+def test_w_ge_n_is_full_causal_bitwise(oracle_mod):
+    rng = np.random.default_rng(1)
+    q, k, v = rand(rng, 1, 2, 37, 8), rand(rng, 1, 2, 37, 8), rand(rng, 1, 2, 37, 8)
+    ref = oracle_mod.attn(q, k, v, 0, 0.3, kind="causal")
+    for W in (37, 38, 74, 1 << 30):
+        out = oracle_mod.attn(q, k, v, W, 0.3, kind="window")
+        assert np.array_equal(out, ref)
+
+
+def test_w1_returns_v(oracle_mod):
+    rng = np.random.default_rng(2)
+    q, k, v = rand(rng, 2, 3, 19, 5), rand(rng, 2, 3, 19, 5), rand(rng, 2, 3, 19, 5)
+    out = oracle_mod.attn(q, k, v, 1, 0.7, kind="window")
+    assert np.array_equal(out, v)
+
+
+def test_rows_sum_to_one(oracle_mod):
+    rng = np.random.default_rng(3)
+    q, k = rand(rng, 1, 1, 64, 16), rand(rng, 1, 1, 64, 16)
+    for kind, W, s in (("window", 9, 0), ("strided", 5, 4), ("causal", 0, 0)):
+        for i in range(64):
+            w = oracle_mod.weights_row(q, k, W, 0.25, 0, 0, i, kind=kind, stride=s)
+            assert abs(w.sum() - 1.0) < 1e-12
+            assert (w[i + 1:] == 0).all() and (w >= 0).all()
+
+
+def test_uniform_keys_give_window_mean(oracle_mod):
+    # Equal scores make the softmax uniform over the allowed keys: out_i = mean of v over the window.
+    rng = np.random.default_rng(4)
+    N, W = 40, 6
+    q, v = rand(rng, 1, 1, N, 4), rand(rng, 1, 1, N, 4)
+    k = np.zeros((1, 1, N, 4))
+    out = oracle_mod.attn(q, k, v, W, 1.0, kind="window")[0, 0]
+    for i in range(N):
+        lo = max(0, i - W + 1)
+        np.testing.assert_allclose(out[i], v[0, 0, lo: i + 1].mean(axis=0), rtol=0, atol=1e-14)
+
+
+def test_large_scores_pick_argmax(oracle_mod):
+    # Scores far apart make the softmax one-hot at the row maximum; an exp without the max
+    # subtraction would overflow to inf/nan here.
+    N, d = 12, 1
+    q = np.ones((1, 1, N, d))
+    k = np.arange(N, dtype=np.float64).reshape(1, 1, N, d) * 1000.0
+    v = np.arange(N, dtype=np.float64).reshape(1, 1, N, d) + 0.5
+    out = oracle_mod.attn(q, k, v, 4, 1.0, kind="window")[0, 0, :, 0]
+    np.testing.assert_array_equal(out, np.arange(N) + 0.5)  # the newest key always wins
+
+
+# ---------------------------------------------------------------------------------------------
+# Brute force against the dense masked softmax on tiny inputs
+# ---------------------------------------------------------------------------------------------
+@pytest.mark.parametrize("seed", [10, 11])
+@pytest.mark.parametrize("N", [1, 5, 33, 64])
+def test_window_brute_force(oracle_mod, seed, N):
+    rng = np.random.default_rng(seed)
+    B, Hq, Hkv, d = 2, 4, 2, 8
+    q, k, v = rand(rng, B, Hq, N, d), rand(rng, B, Hkv, N, d), rand(rng, B, Hkv, N, d)
+    for W in range(1, N + 3):
+        ref = dense_attn(q, k, v, 0.4, "window", W)
+        out = oracle_mod.attn(q, k, v, W, 0.4, kind="window")
+        assert np.max(np.abs(out - ref)) < 1e-12, W
+
+
+@pytest.mark.parametrize("N", [1, 17, 48, 64])
+def test_strided_brute_force(oracle_mod, N):
+    rng = np.random.default_rng(N)
+    q, k, v = rand(rng, 1, 2, N, 8), rand(rng, 1, 2, N, 8), rand(rng, 1, 2, N, 8)
+    for W in (1, 2, 5, 16, N, N + 2):
+        for s in (1, 2, 3, 7, 16, N, N + 1):
+            ref = dense_attn(q, k, v, 0.5, "strided", W, s)
+            out = oracle_mod.attn(q, k, v, W, 0.5, kind="strided", stride=s)
+            assert np.max(np.abs(out - ref)) < 1e-12, (W, s)
+
+
+def test_causal_brute_force(oracle_mod):
+    rng = np.random.default_rng(5)
+    q, k, v = rand(rng, 1, 3, 45, 16), rand(rng, 1, 3, 45, 16), rand(rng, 1, 3, 45, 16)
+    assert np.max(np.abs(oracle_mod.attn(q, k, v, 0, 0.25, kind="causal")
+                         - dense_attn(q, k, v, 0.25, "causal"))) < 1e-12
+
+
+def test_strided_special_cases(oracle_mod):
+    N = 40
+    rng = np.random.default_rng(6)
+    q, k, v = rand(rng, 1, 1, N, 4), rand(rng, 1, 1, N, 4), rand(rng, 1, 1, N, 4)
+    causal = oracle_mod.attn(q, k, v, 0, 0.5, kind="causal")
+    # stride 1 opens every earlier key; a window covering everything does the same
+    assert np.array_equal(oracle_mod.attn(q, k, v, 3, 0.5, kind="strided", stride=1), causal)
+    assert np.array_equal(oracle_mod.attn(q, k, v, N, 0.5, kind="strided", stride=7), causal)
+    # a stride past the end adds only key 0 to the window
+    for i in range(N):
+        m = oracle_mod.mask_row(N, 3, i, "strided", N)
+        expect = oracle_mod.mask_row(N, 3, i, "window")
+        expect[0] = True
+        assert (m == expect).all()
+
+
+@pytest.mark.parametrize("N,W,s", [(64, 8, 4), (100, 10, 7), (16384, 256, 128), (300, 300, 5),
+                                   (50, 1, 1)])
+def test_strided_pair_count_closed_form(oracle_mod, N, W, s):
+    assert oracle_mod.pair_count(N, W, "strided", s) == flops.pairs_strided(N, W, s)
+
+
+def test_strided_headline_pair_count():
+    assert flops.pairs_strided(16384, 256, 128) == 5_185_792
+
+
+# ---------------------------------------------------------------------------------------------
+# Differential attention (A1 - lambda A2) V
+# ---------------------------------------------------------------------------------------------
+def _diff_inputs(seed, B=1, Hq=2, Hkv=2, N=30, d=8):
+    rng = np.random.default_rng(seed)
+    return (rand(rng, B, Hq, N, d), rand(rng, B, Hkv, N, d), rand(rng, B, Hq, N, d),
+            rand(rng, B, Hkv, N, d), rand(rng, B, Hkv, N, d))
+
+
+def test_diff_lambda_zero_is_causal(oracle_mod):
+    q1, k1, q2, k2, v = _diff_inputs(7)
+    ref = oracle_mod.attn(q1, k1, v, 0, 0.35, kind="causal")
+    np.testing.assert_allclose(oracle_mod.diff(q1, k1, q2, k2, v, 0.0, 0.35), ref, rtol=0, atol=1e-14)
+
+
+def test_diff_same_maps(oracle_mod):
+    q1, k1, _, _, v = _diff_inputs(8)
+    ref = oracle_mod.attn(q1, k1, v, 0, 0.35, kind="causal")
+    out = oracle_mod.diff(q1, k1, q1, k1, v, 0.8, 0.35)
+    np.testing.assert_allclose(out, 0.2 * ref, rtol=0, atol=1e-13)
+
+
+def test_diff_affine_in_lambda(oracle_mod):
+    args = _diff_inputs(9)
+    o0 = oracle_mod.diff(*args, 0.0, 0.35)
+    o1 = oracle_mod.diff(*args, 1.0, 0.35)
+    o8 = oracle_mod.diff(*args, 0.8, 0.35)
+    np.testing.assert_allclose(o8, o0 + 0.8 * (o1 - o0), rtol=0, atol=1e-13)
+
+
+def test_diff_brute_force(oracle_mod):
+    q1, k1, q2, k2, v = _diff_inputs(10, B=2, Hq=4, Hkv=2, N=41, d=8)
+    N = q1.shape[2]
+    M = dense_mask(N, "causal")
+    ref = np.empty_like(q1)
+    for b in range(2):
+        for h in range(4):
+            A1 = dense_softmax(q1[b, h], k1[b, h // 2], 0.3, M)
+            A2 = dense_softmax(q2[b, h], k2[b, h // 2], 0.3, M)
+            ref[b, h] = (A1 - 0.8 * A2) @ v[b, h // 2]
+    out = oracle_mod.diff(q1, k1, q2, k2, v, 0.8, 0.3)
+    assert np.max(np.abs(out - ref)) < 1e-12
+
+
+# ---------------------------------------------------------------------------------------------
+# GQA mapping, row subsets, bf16 inputs
+# ---------------------------------------------------------------------------------------------
+def test_gqa_equals_repeated_kv(oracle_mod):
+    rng = np.random.default_rng(12)
+    B, Hq, Hkv, N, d = 2, 6, 2, 23, 4
+    q, k, v = rand(rng, B, Hq, N, d), rand(rng, B, Hkv, N, d), rand(rng, B, Hkv, N, d)
+    g = Hq // Hkv
+    k_rep, v_rep = np.repeat(k, g, axis=1), np.repeat(v, g, axis=1)  # head h -> kv head h // g
+    for kind, W, s in (("window", 5, 0), ("strided", 4, 3), ("causal", 0, 0)):
+        a = oracle_mod.attn(q, k, v, W, 0.5, kind=kind, stride=s)
+        b = oracle_mod.attn(q, k_rep, v_rep, W, 0.5, kind=kind, stride=s)
+        assert np.array_equal(a, b)
+
+
+def test_row_subset_matches_full(oracle_mod):
+    rng = np.random.default_rng(13)
+    q, k, v = rand(rng, 1, 2, 50, 4), rand(rng, 1, 2, 50, 4), rand(rng, 1, 2, 50, 4)
+    full = oracle_mod.attn(q, k, v, 7, 0.5)
+    rows = np.array([0, 3, 49, 17])
+    assert np.array_equal(oracle_mod.attn(q, k, v, 7, 0.5, rows=rows), full[:, :, rows])
+    d_full = oracle_mod.diff(q, k, k, q, v, 0.5, 0.5)
+    assert np.array_equal(oracle_mod.diff(q, k, k, q, v, 0.5, 0.5, rows=rows), d_full[:, :, rows])
+
+
+def test_bad_arguments_rejected(oracle_mod):
+    q = np.zeros((1, 3, 4, 2))
+    k = np.zeros((1, 2, 4, 2))
+    with pytest.raises(ValueError):
+        oracle_mod.attn(q, k, k, 2, 1.0)  # Hq not a multiple of Hkv
+    q = np.zeros((1, 2, 4, 2))
+    with pytest.raises(ValueError):
+        oracle_mod.attn(q, k, k, 0, 1.0)  # W < 1
+    with pytest.raises(ValueError):
+        oracle_mod.attn(q, k, k, 2, 1.0, rows=[4])
+
+
+def test_bf16_inputs_widen_exactly(oracle_mod):
+    import swa_inputs
+
+    rng = np.random.default_rng(14)
+    x = rng.standard_normal((1, 1, 16, 8)).astype(np.float32)
+    h = swa_inputs.f32_to_bf16_bits(x)
+    ref = oracle_mod.attn(swa_inputs.bf16_bits_to_f64(h), swa_inputs.bf16_bits_to_f64(h),
+                          swa_inputs.bf16_bits_to_f64(h), 3, 0.5)
+    assert np.array_equal(oracle_mod.attn(h, h, h, 3, 0.5), ref)
