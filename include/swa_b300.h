@@ -1,0 +1,105 @@
+/*
+ * swa_b300.h -- C ABI of the B300 (sm_103a) sliding-window / sparse / differential
+ * causal attention forward library (libswa_b300.so).
+ *
+ * Sources, cited by page title and section:
+ *   [SWA]  "SWA：滑动窗口注意力与跨层信息传递" (lizn-zn.github.io): §1 (the window W
+ *          counts the current position; FlashAttention window_size = (W-1, 0)),
+ *          §3.1 (window set N_W(i) = {j : max(1, i-W+1) <= j <= i}, mask M^SWA and
+ *          Attention_SWA = softmax(Q K^T / sqrt(d_k) + M^SWA) V, row-wise softmax),
+ *          §4.1 (skip the work outside the window).
+ *   [AV]   "注意力变体——滑动窗口、稀疏、差分" (ai-engineering.com.cn), "Build it"
+ *          step 2 (sliding-window causal mask), step 3 (local + strided mask),
+ *          step 4 (differential attention).
+ *   [AVpt] "Variantes de Atenção — Janela Deslizante, Esparsa, Diferencial"
+ *          (ai-engineering.academy), "Atenção Diferencial": A1 = softmax(Q1 K1^T / sqrt d),
+ *          A2 = softmax(Q2 K2^T / sqrt d), DiffAttn = (A1 - lambda A2) V.
+ *
+ * Common conventions for the three compute calls:
+ *   - Tensors are bf16, contiguous, layout [B, H, N, d]: q, q1, q2 and out have
+ *     H = Hq heads; k, k1, k2 and v have H = Hkv heads.  Query head h reads
+ *     key/value head h / (Hq / Hkv) (grouped-query attention).
+ *   - Rows are 0-indexed: query i may read key j iff max(0, i - W + 1) <= j <= i.
+ *     W >= N gives full causal attention; W = 1 lets each row read only itself.
+ *   - scale multiplies q . k before the softmax (the pages use 1 / sqrt(d)).
+ *   - All pointers are DEVICE pointers owned by the caller; out must not overlap an
+ *     input.  Every pointer must be 16-byte aligned.  The call is asynchronous on
+ *     `stream` (a cudaStream_t passed as void*; NULL = the legacy default stream) and
+ *     does not synchronise.  Accumulation is fp32; out is rounded to bf16 (RNE).
+ *   - d must be 64 or 128; N * d * 2 bytes per head must fit the TMA limits
+ *     (N < 2^31).  The device must be sm_103 (B300).
+ *   - The library keeps process-lifetime state per device (kernel attributes, a
+ *     cached strided tile list); it performs no per-call allocation except the
+ *     first strided call for a new (N, W, stride) shape, which builds and caches
+ *     that shape's tile list.
+ *   - Errors are returned as swa_status codes; nothing is thrown across the ABI.
+ *     Argument errors are detected on the host before anything is launched.
+ */
+#ifndef SWA_B300_H
+#define SWA_B300_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum swa_status {
+    SWA_OK = 0,
+    SWA_ERR_NULL = 1,        /* a required pointer is NULL */
+    SWA_ERR_SHAPE = 2,       /* B, Hq, Hkv, N < 1; W < 1; stride < 1; Hq % Hkv != 0; N too large */
+    SWA_ERR_ALIGN = 3,       /* a pointer is not 16-byte aligned */
+    SWA_ERR_UNSUPPORTED = 4, /* d not in {64, 128}, or the current device is not sm_103 */
+    SWA_ERR_CUDA = 5,        /* a CUDA runtime / driver call failed (launch, attribute, map) */
+    SWA_ERR_TIMEOUT = 6,     /* a kernel-side bounded wait ran out (read by swa_device_status) */
+    SWA_ERR_VALUE = 7        /* scale not finite and > 0, or lambda not finite */
+} swa_status;
+
+/*
+ * Causal sliding-window attention forward ([SWA] §3.1; [AV] step 2):
+ *   out[b, h, i, :] = sum_{j = max(0, i-W+1)}^{i} softmax_j(scale * q_i . k_j) v_j
+ * with each row's softmax normalised over its own window.  W >= N is full causal.
+ */
+int swa_attn_fwd(const void* q, const void* k, const void* v, void* out, int B, int Hq,
+                 int Hkv, int N, int d, int W, float scale, void* stream);
+
+/*
+ * Local + strided sparse causal attention forward ([AV] step 3): row i reads the
+ * window keys max(0, i-W+1) <= j <= i and every key j = 0, stride, 2*stride, ... <= i
+ * (absolute multiples of stride; a key in both sets counts once).
+ * The first call for a new (N, W, stride) builds and caches a device tile list.
+ */
+int strided_attn_fwd(const void* q, const void* k, const void* v, void* out, int B, int Hq,
+                     int Hkv, int N, int d, int W, int stride, float scale, void* stream);
+
+/*
+ * Differential causal attention forward ([AVpt] "Atenção Diferencial"; [AV] step 4):
+ *   out = (softmax_causal(scale Q1 K1^T) - lambda softmax_causal(scale Q2 K2^T)) V.
+ * q1, q2, out: Hq heads; k1, k2, v: Hkv heads.  Both maps are full causal.
+ */
+int diff_attn_fwd(const void* q1, const void* k1, const void* q2, const void* k2,
+                  const void* v, float lambda, void* out, int B, int Hq, int Hkv, int N, int d,
+                  float scale, void* stream);
+
+/* Human-readable name of a status code (static storage; never NULL). */
+const char* swa_status_string(int status);
+
+/*
+ * Synchronise `stream`, then read and clear the library's device status word on the
+ * current device.  Returns SWA_OK, SWA_ERR_TIMEOUT if a kernel's bounded wait ran out
+ * since the last call (that kernel wrote no output rows it could not finish), or
+ * SWA_ERR_CUDA if the synchronisation itself failed.
+ */
+int swa_device_status(void* stream);
+
+/*
+ * Self-test of the kernel watchdog: launches one CTA that waits on a barrier nobody
+ * arrives at, with a wait limit of `limit_us` microseconds (1..1000000).  The wait runs
+ * out, the kernel records SWA_ERR_TIMEOUT in the device status word and returns.
+ * Asynchronous; read the outcome with swa_device_status.
+ */
+int swa_watchdog_selftest(int limit_us, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SWA_B300_H */

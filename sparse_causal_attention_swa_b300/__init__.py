@@ -1,0 +1,168 @@
+"""B300 (sm_103a) causal sliding-window, local+strided and differential attention forward.
+
+The compute lives in ``libswa_b300.so`` (hand-written CUDA for sm_103a: TMA-fed shared
+memory rings, tcgen05 MMAs accumulating in tensor memory, an exp2 online softmax).  This
+module is a thin ctypes binding with the same names as the C ABI declared in
+``include/swa_b300.h``; it only marshals arguments.  PyTorch is used for device memory
+and streams.  There is no CPU fallback: if the library is missing, every call raises.
+
+Low-level calls (pointers or tensors, explicit sizes, asynchronous on ``stream``):
+    swa_attn_fwd, strided_attn_fwd, diff_attn_fwd, swa_status_string,
+    swa_device_status, swa_watchdog_selftest
+Convenience wrappers on [B, H, N, d] bf16 tensors (allocate ``out``; CPU inputs are
+copied to the current CUDA device and the result copied back):
+    swa_attention, strided_attention, diff_attention
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIBRARY_PATH = os.path.join(_PKG, "libswa_b300.so")
+
+SWA_OK = 0
+_lib = None
+
+
+class SwaError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {swa_status_string(code)} (status {code})")
+
+
+def load():
+    """Load the compiled library; raise if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIBRARY_PATH):
+            raise RuntimeError(
+                f"{LIBRARY_PATH} is missing: the CUDA extension is not built "
+                "(run `python -m sparse_causal_attention_swa_b300._build`)")
+        lib = ctypes.CDLL(LIBRARY_PATH)
+        P, I, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+        lib.swa_attn_fwd.argtypes = [P, P, P, P, I, I, I, I, I, I, F, P]
+        lib.swa_attn_fwd.restype = I
+        lib.strided_attn_fwd.argtypes = [P, P, P, P, I, I, I, I, I, I, I, F, P]
+        lib.strided_attn_fwd.restype = I
+        lib.diff_attn_fwd.argtypes = [P, P, P, P, P, F, P, I, I, I, I, I, F, P]
+        lib.diff_attn_fwd.restype = I
+        lib.swa_status_string.argtypes = [I]
+        lib.swa_status_string.restype = ctypes.c_char_p
+        lib.swa_device_status.argtypes = [P]
+        lib.swa_device_status.restype = I
+        lib.swa_watchdog_selftest.argtypes = [I, P]
+        lib.swa_watchdog_selftest.restype = I
+        _lib = lib
+    return _lib
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(code: int, where: str):
+    if code != SWA_OK:
+        raise SwaError(code, where)
+
+
+def swa_status_string(status: int) -> str:
+    return load().swa_status_string(int(status)).decode()
+
+
+# ---------------------------------------------------------------- C-ABI mirrors
+def swa_attn_fwd(q, k, v, out, B, Hq, Hkv, N, d, W, scale, stream=None):
+    _check(load().swa_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, Hq, Hkv, N, d, W,
+                               float(scale), _stream(stream)), "swa_attn_fwd")
+
+
+def strided_attn_fwd(q, k, v, out, B, Hq, Hkv, N, d, W, stride, scale, stream=None):
+    _check(load().strided_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, Hq, Hkv, N, d, W,
+                                   stride, float(scale), _stream(stream)), "strided_attn_fwd")
+
+
+def diff_attn_fwd(q1, k1, q2, k2, v, lam, out, B, Hq, Hkv, N, d, scale, stream=None):
+    _check(load().diff_attn_fwd(_ptr(q1), _ptr(k1), _ptr(q2), _ptr(k2), _ptr(v), float(lam),
+                                _ptr(out), B, Hq, Hkv, N, d, float(scale), _stream(stream)),
+           "diff_attn_fwd")
+
+
+def swa_device_status(stream=None) -> int:
+    return int(load().swa_device_status(_stream(stream)))
+
+
+def swa_watchdog_selftest(limit_us: int, stream=None):
+    _check(load().swa_watchdog_selftest(int(limit_us), _stream(stream)), "swa_watchdog_selftest")
+
+
+# ---------------------------------------------------------------- tensor wrappers
+def _prepare(*ts):
+    import torch
+
+    dev = None
+    for t in ts:
+        if t.is_cuda:
+            dev = t.device
+    if dev is None:
+        dev = torch.device("cuda", torch.cuda.current_device())
+    out = []
+    for t in ts:
+        if t.dtype != torch.bfloat16 or t.dim() != 4:
+            raise ValueError("expected bf16 tensors of shape [B, H, N, d]")
+        out.append(t.to(dev, non_blocking=True).contiguous())
+    return out, dev
+
+
+def _finish(out, like):
+    return out if like.is_cuda else out.to("cpu", non_blocking=False)
+
+
+def swa_attention(q, k, v, window: int, scale: float | None = None, out=None):
+    """Causal sliding-window attention, window counting the current position."""
+    import torch
+
+    (qd, kd, vd), dev = _prepare(q, k, v)
+    B, Hq, N, d = qd.shape
+    o = out if out is not None else torch.empty_like(qd)
+    swa_attn_fwd(qd, kd, vd, o, B, Hq, kd.shape[1], N, d, int(window),
+                 scale if scale is not None else 1.0 / math.sqrt(d))
+    return _finish(o, q)
+
+
+def strided_attention(q, k, v, window: int, stride: int, scale: float | None = None, out=None):
+    """Local window plus every stride-th key (absolute multiples of stride), causal."""
+    import torch
+
+    (qd, kd, vd), dev = _prepare(q, k, v)
+    B, Hq, N, d = qd.shape
+    o = out if out is not None else torch.empty_like(qd)
+    strided_attn_fwd(qd, kd, vd, o, B, Hq, kd.shape[1], N, d, int(window), int(stride),
+                     scale if scale is not None else 1.0 / math.sqrt(d))
+    return _finish(o, q)
+
+
+def diff_attention(q1, k1, q2, k2, v, lam: float, scale: float | None = None, out=None):
+    """(softmax_causal(Q1 K1^T s) - lam softmax_causal(Q2 K2^T s)) V."""
+    import torch
+
+    (a, b_, c, e, f), dev = _prepare(q1, k1, q2, k2, v)
+    B, Hq, N, d = a.shape
+    o = out if out is not None else torch.empty_like(a)
+    diff_attn_fwd(a, b_, c, e, f, lam, o, B, Hq, b_.shape[1], N, d,
+                  scale if scale is not None else 1.0 / math.sqrt(d))
+    return _finish(o, q1)

@@ -1,0 +1,546 @@
+// attn_fwd.cuh -- sm_103a forward kernel for causal sliding-window attention and its two
+// variants (local + strided sparse, differential), one CTA per work item.
+//
+// What it computes (sources cited by page title and section):
+//   * "SWA：滑动窗口注意力与跨层信息传递" §3.1: out_i = softmax_j(scale q_i.k_j + M_ij) v_j
+//     with M_ij = 0 iff max(0, i-W+1) <= j <= i (0-indexed; W counts the current row),
+//     each row normalised inside its own window; §4.1: work outside the window is skipped.
+//   * "注意力变体——滑动窗口、稀疏、差分", "Build it" step 3: the local + strided mask adds
+//     keys j = 0, s, 2s, ... <= i to the window.
+//   * "Variantes de Atenção", "Atenção Diferencial": out = (A1 - lambda A2) V with two
+//     causal softmax maps from (Q1, K1) and (Q2, K2).
+//
+// CTA organisation (384 threads, one CTA per SM because of TMEM and shared memory):
+//   warps 0-3  softmax warpgroup of slot 0   (thread t owns query row t of the slot)
+//   warps 4-7  softmax warpgroup of slot 1
+//   warp 8     TMA producer (lane 0): Q tiles once, then K / V tiles into an smem ring
+//   warp 9     TMEM owner + MMA issuer (lane 0): S = Q K^T and O += P V on tcgen05
+//   warps 10-11 idle
+// A "slot" is 128 query rows.  The two slots of a work item are either two query heads of
+// one GQA group on the same rows, the two score streams of the differential variant, or
+// two consecutive 128-row tiles of one head; they walk the same KV tile sequence in lock
+// step so that every K / V tile is loaded once for both.
+//
+// Tensor memory (512 columns x 128 lanes, fp32):
+//   [  0,128) S of slot 0   (P of slot 0, bf16 packed in pairs, overwrites columns [0,64))
+//   [128,256) S of slot 1   (P of slot 1 in [128,192))
+//   [256,256+D) O of slot 0,  [384,384+D) O of slot 1
+//
+// Per KV tile and slot, the MMA thread issues, in order, PV_s(j) then S_s(j+1); tcgen05
+// MMAs of one thread execute in issue order, so S_s(j+1) cannot overwrite P_s(j) before
+// PV_s(j) has read it, and the commit after S_s(j+1) also covers PV_s(j).
+//
+// Online softmax in base 2: x = s * scale * log2(e).  The running row maximum m is only
+// moved (and O, l rescaled) when the new tile's maximum exceeds it by more than 8 in the
+// log2 domain; otherwise exponents stay <= 8 and p <= 256, exact in bf16 and safe in fp32.
+// The final out = O / l is exact whichever maximum was used.
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include "ptx.cuh"
+
+namespace swa {
+
+constexpr int BM = 128;  // query rows per slot
+constexpr int BN = 128;  // keys per KV tile
+constexpr int NUM_THREADS = 384;
+constexpr int PRODUCER_WARP = 8;
+constexpr int MMA_WARP = 9;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr float RESCALE_THRESHOLD = 8.0f;  // log2 units
+
+enum Mode : int { MODE_WINDOW = 0, MODE_STRIDED = 1, MODE_DIFF = 2 };
+
+// Tile-list entry encoding (strided mode): kind in bits 24.., tile index below.
+constexpr int TILE_KIND_SHIFT = 24;
+constexpr int TILE_KIND_WINDOW = 0;
+constexpr int TILE_KIND_STRIDED = 1;
+
+struct KParams {
+    CUtensorMap tm_q;   // queries (slot 0; both slots unless diff), view [B*Hq][N][d]
+    CUtensorMap tm_k;   // keys (slot 0 / both), view [B*Hkv][N][d]
+    CUtensorMap tm_v;   // values
+    CUtensorMap tm_q2;  // diff: Q2
+    CUtensorMap tm_k2;  // diff: K2 ; strided: compact keys, rows 0, s, 2s, ...
+    CUtensorMap tm_v2;  // strided: compact values
+    __nv_bfloat16* out;
+    const int* tiles;   // strided: [n_blocks + 1] offsets, then encoded entries
+    int* status;        // device status word (SWA_ERR_TIMEOUT on a watchdog abort)
+    unsigned long long wait_limit_ns;
+    int B, Hq, Hkv, N, W, stride;
+    int n_qtiles;       // ceil(N / BM)
+    int pair_mode;      // 1: both slots on the same rows; 0: consecutive row tiles of a head
+    float scale_log2;   // scale * log2(e)
+    float lambda;       // diff only
+};
+
+template <int D, int MODE>
+struct SmemLayout {
+    static constexpr int QBYTES = BM * D * 2;
+    static constexpr int EBYTES = BN * D * 2;  // one ring entry: a K or V tile
+    static constexpr int STAGES = (D == 128) ? 4 : 8;
+    static constexpr int OFF_Q = 0;
+    static constexpr int OFF_RING = 2 * QBYTES;
+    static constexpr int OFF_BAR = OFF_RING + STAGES * EBYTES;
+    // barriers: q_full, ring_full[S], ring_empty[S], s_full[2], p_full[2], o_final[2],
+    //           lsm_ready, drain
+    static constexpr int BAR_Q = 0;
+    static constexpr int BAR_FULL = 1;
+    static constexpr int BAR_EMPTY = 1 + STAGES;
+    static constexpr int BAR_S = 1 + 2 * STAGES;
+    static constexpr int BAR_P = BAR_S + 2;
+    static constexpr int BAR_O = BAR_P + 2;
+    static constexpr int BAR_L = BAR_O + 2;
+    static constexpr int BAR_DRAIN = BAR_L + 1;
+    static constexpr int NBARS = BAR_DRAIN + 1;
+    static constexpr int OFF_TMEM = OFF_BAR + NBARS * 8;
+    static constexpr int OFF_ABORT = OFF_TMEM + 4;
+    static constexpr int OFF_LSM = (OFF_ABORT + 4 + 15) / 16 * 16;
+    static constexpr int END = OFF_LSM + BM * 4;
+    static constexpr int BYTES = END + 1024;  // slack for aligning the base to 1024
+    static_assert(BYTES <= 232448, "shared memory budget");
+    static_assert(EBYTES % 1024 == 0 && QBYTES % 1024 == 0, "1024-byte tile alignment");
+};
+
+struct WorkItem {
+    int b, hk;
+    int h[2];    // query head of each slot
+    int r0[2];   // first row of each slot
+    int block;   // row-block index (tile-list row)
+    int R0, R1;  // union of valid rows
+};
+
+template <int MODE>
+__device__ __forceinline__ WorkItem decode_item(const KParams& p, int item) {
+    WorkItem w;
+    const int g = p.Hq / p.Hkv;
+    if (p.pair_mode) {
+        // heaviest row tiles first: the last row tile has the longest (or an equal) KV range
+        const int per = (MODE == MODE_DIFF) ? p.B * p.Hq : p.B * p.Hkv * (g / 2);
+        const int qt = p.n_qtiles - 1 - item / per;
+        const int rem = item % per;
+        if (MODE == MODE_DIFF) {
+            w.b = rem / p.Hq;
+            w.h[0] = w.h[1] = rem % p.Hq;
+            w.hk = w.h[0] / g;
+        } else {
+            const int pair = rem % (g / 2);  // adjacent items share K / V tiles in L2
+            const int bhk = rem / (g / 2);
+            w.b = bhk / p.Hkv;
+            w.hk = bhk % p.Hkv;
+            w.h[0] = w.hk * g + 2 * pair;
+            w.h[1] = w.h[0] + 1;
+        }
+        w.r0[0] = w.r0[1] = qt * BM;
+        w.block = qt;
+    } else {
+        const int nqp = (p.n_qtiles + 1) / 2;
+        const int per = p.B * p.Hq;
+        const int qp = nqp - 1 - item / per;
+        const int bh = item % per;
+        w.b = bh / p.Hq;
+        w.h[0] = w.h[1] = bh % p.Hq;
+        w.hk = w.h[0] / g;
+        w.r0[0] = 2 * qp * BM;
+        w.r0[1] = w.r0[0] + BM;
+        w.block = qp;
+    }
+    w.R0 = w.r0[0];
+    w.R1 = min(w.r0[1] + BM - 1, p.N - 1);
+    return w;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+template <int D, int MODE>
+__global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd_kernel(const __grid_constant__ KParams p) {
+    using L = SmemLayout<D, MODE>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t bars = sbase + L::OFF_BAR;
+    auto bar = [&](int i) -> uint32_t { return bars + 8u * (uint32_t)i; };
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_ABORT);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_TMEM);
+    float* lsm = reinterpret_cast<float*>(smem + L::OFF_LSM);
+
+    const uint32_t warp = warp_id();
+    const uint32_t lane = lane_id();
+    const WorkItem wi = decode_item<MODE>(p, blockIdx.x);
+
+    // ---- tile sequence of this item
+    int n_tiles, kv_lo = 0, list_off = 0;
+    if (MODE == MODE_STRIDED) {
+        const int nblk = p.pair_mode ? p.n_qtiles : (p.n_qtiles + 1) / 2;
+        list_off = nblk + 1 + p.tiles[wi.block];
+        n_tiles = p.tiles[wi.block + 1] - p.tiles[wi.block];
+    } else {
+        kv_lo = (MODE == MODE_DIFF) ? 0 : max(0, wi.R0 - p.W + 1) / BN;
+        n_tiles = wi.R1 / BN - kv_lo + 1;
+    }
+    auto tile_at = [&](int jj, int& kind, int& idx) {
+        if (MODE == MODE_STRIDED) {
+            const int e = p.tiles[list_off + jj];
+            kind = e >> TILE_KIND_SHIFT;
+            idx = e & ((1 << TILE_KIND_SHIFT) - 1);
+        } else {
+            kind = TILE_KIND_WINDOW;
+            idx = kv_lo + jj;
+        }
+    };
+
+    // ---- setup: barriers, TMEM
+    if (warp == MMA_WARP) {
+        tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+        tmem_relinquish();
+    }
+    if (threadIdx.x == 0) {
+        mbar_init(bar(L::BAR_Q), 1);
+        for (int s = 0; s < L::STAGES; ++s) {
+            mbar_init(bar(L::BAR_FULL + s), 1);
+            mbar_init(bar(L::BAR_EMPTY + s), 1);
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(bar(L::BAR_S + s), 1);
+            mbar_init(bar(L::BAR_P + s), 128);
+            mbar_init(bar(L::BAR_O + s), 1);
+        }
+        mbar_init(bar(L::BAR_L), 128);
+        mbar_init(bar(L::BAR_DRAIN), 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == PRODUCER_WARP && lane == 0) {
+        tma_prefetch_desc(&p.tm_q);
+        tma_prefetch_desc(&p.tm_k);
+        tma_prefetch_desc(&p.tm_v);
+        if (MODE != MODE_WINDOW) tma_prefetch_desc(&p.tm_k2);
+        if (MODE == MODE_DIFF) tma_prefetch_desc(&p.tm_q2);
+        if (MODE == MODE_STRIDED) tma_prefetch_desc(&p.tm_v2);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const uint64_t lim = p.wait_limit_ns;
+
+    if (warp == PRODUCER_WARP) {
+        // ===================================== TMA producer
+        if (lane == 0) {
+            constexpr int NCH = D / 64;  // 64-column (128-byte) chunks per row
+            uint32_t last_par[L::STAGES];
+            bool used[L::STAGES];
+            for (int s = 0; s < L::STAGES; ++s) used[s] = false;
+            // Q tiles of both slots
+            mbar_arrive_expect_tx(bar(L::BAR_Q), 2 * L::QBYTES);
+            for (int s = 0; s < 2; ++s) {
+                const CUtensorMap* mq = (MODE == MODE_DIFF && s == 1) ? &p.tm_q2 : &p.tm_q;
+                const int mat = wi.b * p.Hq + wi.h[s];
+                for (int c = 0; c < NCH; ++c)
+                    tma_load_3d(sbase + L::OFF_Q + s * L::QBYTES + c * (BM * 128), mq, bar(L::BAR_Q),
+                                c * 64, wi.r0[s], mat);
+            }
+            uint32_t st = 0, ph = 0;
+            const int kmat = wi.b * p.Hkv + wi.hk;
+            bool ok = true;
+            auto push = [&](const CUtensorMap* m, int row) -> bool {
+                if (!mbar_wait_bounded(bar(L::BAR_EMPTY + st), ph ^ 1u, abort_flag, lim)) return false;
+                mbar_arrive_expect_tx(bar(L::BAR_FULL + st), L::EBYTES);
+                const uint32_t dst = sbase + L::OFF_RING + st * L::EBYTES;
+                for (int c = 0; c < NCH; ++c)
+                    tma_load_3d(dst + c * (BN * 128), m, bar(L::BAR_FULL + st), c * 64, row, kmat);
+                used[st] = true;
+                last_par[st] = ph;
+                if (++st == (uint32_t)L::STAGES) {
+                    st = 0;
+                    ph ^= 1u;
+                }
+                return true;
+            };
+            for (int jj = 0; jj < n_tiles && ok; ++jj) {
+                int kind, idx;
+                tile_at(jj, kind, idx);
+                const bool compact = (MODE == MODE_STRIDED && kind == TILE_KIND_STRIDED);
+                const CUtensorMap* mk = compact ? &p.tm_k2 : &p.tm_k;
+                const CUtensorMap* mv = compact ? &p.tm_v2 : &p.tm_v;
+                const int row = idx * BN;
+                ok = push(mk, row);
+                if (ok && MODE == MODE_DIFF) ok = push(&p.tm_k2, row);
+                if (ok) ok = push(mv, row);
+            }
+            // drain: every issued copy must have landed before the CTA may exit
+            {
+                volatile int never = 0;
+                (void)mbar_wait_bounded(bar(L::BAR_Q), 0, &never, lim);
+                for (int s = 0; s < L::STAGES; ++s)
+                    if (used[s]) (void)mbar_wait_bounded(bar(L::BAR_FULL + s), last_par[s], &never, lim);
+            }
+        }
+        __syncwarp();
+    } else if (warp == MMA_WARP) {
+        // ===================================== MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t ID_S = idesc_bf16_f32(BM, BN, 0);
+            constexpr uint32_t ID_O = idesc_bf16_f32(BM, D, 1);
+            const uint32_t ring0 = sbase + L::OFF_RING;
+            const uint32_t tS[2] = {tmem_base + 0u, tmem_base + 128u};
+            const uint32_t tO[2] = {tmem_base + 256u, tmem_base + 384u};
+            auto issue_S = [&](int s, int entry) {
+                const uint32_t qa = sbase + L::OFF_Q + s * L::QBYTES;
+                const uint32_t ka = ring0 + entry * L::EBYTES;
+#pragma unroll
+                for (int k = 0; k < D / 16; ++k) {
+                    const uint32_t off = (k >> 2) * (BM * 128) + (k & 3) * 32;
+                    const uint32_t koff = (k >> 2) * (BN * 128) + (k & 3) * 32;
+                    mma_ss(tS[s], smem_desc_sw128(qa + off, 16, 1024),
+                           smem_desc_sw128(ka + koff, 16, 1024), ID_S, k > 0 ? 1u : 0u);
+                }
+            };
+            auto issue_PV = [&](int s, int entry, bool acc) {
+                const uint32_t va = ring0 + entry * L::EBYTES;
+#pragma unroll
+                for (int k = 0; k < BN / 16; ++k) {
+                    mma_ts(tO[s], tS[s] + k * 8, smem_desc_sw128(va + k * 2048, BN * 128, 1024),
+                           ID_O, (acc || k > 0) ? 1u : 0u);
+                }
+            };
+            uint32_t st = 0, ph = 0;
+            bool ok = true;
+            auto pop = [&](int& e) -> bool {
+                if (!mbar_wait_bounded(bar(L::BAR_FULL + st), ph, abort_flag, lim)) return false;
+                e = (int)st;
+                if (++st == (uint32_t)L::STAGES) {
+                    st = 0;
+                    ph ^= 1u;
+                }
+                return true;
+            };
+            int kA = 0, kB = 0;
+            ok = mbar_wait_bounded(bar(L::BAR_Q), 0, abort_flag, lim);
+            if (ok) ok = pop(kA);
+            if (ok && MODE == MODE_DIFF) ok = pop(kB);
+            if (ok) {
+                if (MODE != MODE_DIFF) kB = kA;
+                tc_fence_after();
+                issue_S(0, kA);
+                mma_commit(bar(L::BAR_S + 0));
+                issue_S(1, kB);
+                mma_commit(bar(L::BAR_S + 1));
+                mma_commit(bar(L::BAR_EMPTY + kA));
+                if (MODE == MODE_DIFF) mma_commit(bar(L::BAR_EMPTY + kB));
+            }
+            for (int jj = 0; jj < n_tiles && ok; ++jj) {
+                int ve = 0, nA = 0, nB = 0;
+                const bool more = jj + 1 < n_tiles;
+                ok = pop(ve);
+                if (ok && more) {
+                    ok = pop(nA);
+                    if (ok && MODE == MODE_DIFF) ok = pop(nB);
+                    if (MODE != MODE_DIFF) nB = nA;
+                }
+                for (int s = 0; s < 2 && ok; ++s) {
+                    ok = mbar_wait_bounded(bar(L::BAR_P + s), (uint32_t)jj & 1u, abort_flag, lim);
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_PV(s, ve, jj > 0);
+                    if (more) {
+                        issue_S(s, s == 0 ? nA : nB);
+                        mma_commit(bar(L::BAR_S + s));
+                    } else {
+                        mma_commit(bar(L::BAR_O + s));
+                    }
+                }
+                if (!ok) break;
+                mma_commit(bar(L::BAR_EMPTY + ve));
+                if (more) {
+                    mma_commit(bar(L::BAR_EMPTY + nA));
+                    if (MODE == MODE_DIFF) mma_commit(bar(L::BAR_EMPTY + nB));
+                }
+            }
+            // drain: all issued MMAs must complete before TMEM is released
+            mma_commit(bar(L::BAR_DRAIN));
+            volatile int never = 0;
+            (void)mbar_wait_bounded(bar(L::BAR_DRAIN), 0, &never, lim);
+        }
+        __syncwarp();
+    } else if (warp < 8) {
+        // ===================================== softmax warpgroups
+        const int s = (int)(warp >> 2);
+        const int wq = (int)(warp & 3);
+        const int trow = wq * 32 + (int)lane;
+        const int row = wi.r0[s] + trow;
+        const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
+        const uint32_t tS = tmem_base + lane_off + (uint32_t)(s * 128);
+        const uint32_t tO = tmem_base + lane_off + 256u + (uint32_t)(s * 128);
+        const float sl2 = p.scale_log2;
+        const int lo_i = (MODE == MODE_DIFF) ? 0 : max(0, row - p.W + 1);
+        const int lo_strided = (MODE == MODE_STRIDED) ? (lo_i + p.stride - 1) / p.stride : 0;
+        float m = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int jj = 0; jj < n_tiles; ++jj) {
+            ok = mbar_wait_bounded(bar(L::BAR_S + s), (uint32_t)jj & 1u, abort_flag, lim);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            tc_fence_after();
+            float x[BN];
+            {
+                uint32_t r[32];
+#pragma unroll
+                for (int c = 0; c < BN / 32; ++c) {
+                    tmem_ld32(tS + c * 32, r);
+#pragma unroll
+                    for (int t = 0; t < 32; ++t) x[c * 32 + t] = __uint_as_float(r[t]);
+                }
+            }
+            // allowed columns of this row in this tile: [a, bnd]
+            int kind, idx;
+            tile_at(jj, kind, idx);
+            int a, bnd;
+            if (MODE == MODE_STRIDED && kind == TILE_KIND_STRIDED) {
+                a = 0;
+                bnd = lo_strided - idx * BN - 1;
+            } else {
+                const int c0 = idx * BN;
+                a = lo_i - c0;
+                bnd = row - c0;
+            }
+            if (a > 0 || bnd < BN - 1) {
+#pragma unroll
+                for (int t = 0; t < BN; ++t) x[t] = (t >= a && t <= bnd) ? x[t] : -INFINITY;
+            }
+            float mt = x[0];
+#pragma unroll
+            for (int t = 1; t < BN; ++t) mt = fmaxf(mt, x[t]);
+            const float m_new = fmaxf(m, mt);
+            const bool need = (m_new - m) * sl2 > RESCALE_THRESHOLD;
+            const bool rescale = __any_sync(0xffffffffu, need);
+            float alpha = 1.f;
+            if (rescale) {
+                alpha = (m_new == -INFINITY) ? 1.f : fast_exp2((m - m_new) * sl2);
+                l *= alpha;
+                m = m_new;
+            }
+            const float ms = (m == -INFINITY) ? 0.f : m * sl2;
+            // P = exp2(x * scale * log2 e - m * scale * log2 e), packed bf16 pairs into TMEM
+            float rs = 0.f;
+#pragma unroll
+            for (int c = 0; c < BN / 64; ++c) {
+                uint32_t pk[32];
+#pragma unroll
+                for (int t = 0; t < 32; ++t) {
+                    const float p0 = fast_exp2(fmaf(x[c * 64 + 2 * t], sl2, -ms));
+                    const float p1 = fast_exp2(fmaf(x[c * 64 + 2 * t + 1], sl2, -ms));
+                    rs += p0 + p1;
+                    pk[t] = pack_bf16x2(p0, p1);
+                }
+                tmem_st32(tS + c * 32, pk);
+            }
+            l += rs;
+            // O is complete up to tile jj-1 here (its PV was issued before this tile's S)
+            if (rescale && jj > 0) {
+                uint32_t r[32];
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    tmem_ld32(tO + c * 32, r);
+#pragma unroll
+                    for (int t = 0; t < 32; ++t)
+                        r[t] = __float_as_uint(__uint_as_float(r[t]) * alpha);
+                    tmem_st32(tO + c * 32, r);
+                }
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(bar(L::BAR_P + s));
+        }
+        // ---- epilogue
+        if (ok) {
+            ok = mbar_wait_bounded(bar(L::BAR_O + s), 0, abort_flag, lim);
+            ok = __all_sync(0xffffffffu, ok);
+        }
+        if (ok) {
+            tc_fence_after();
+            const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+            if (MODE == MODE_DIFF && s == 1) {
+                lsm[trow] = inv_l;
+                mbar_arrive(bar(L::BAR_L));
+            } else {
+                float inv_l2 = 0.f;
+                if (MODE == MODE_DIFF) {
+                    ok = mbar_wait_bounded(bar(L::BAR_L), 0, abort_flag, lim);
+                    if (ok) ok = mbar_wait_bounded(bar(L::BAR_O + 1), 0, abort_flag, lim);
+                    ok = __all_sync(0xffffffffu, ok);
+                    tc_fence_after();
+                    inv_l2 = lsm[trow] * p.lambda;
+                }
+                if (ok) {
+                    __nv_bfloat16* orow =
+                        p.out + ((size_t)(wi.b * p.Hq + wi.h[s]) * p.N + (size_t)row) * D;
+                    const uint32_t tO2 = tmem_base + lane_off + 384u;
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t r[32];
+                        tmem_ld32(tO + c * 32, r);
+                        float y[32];
+#pragma unroll
+                        for (int t = 0; t < 32; ++t) y[t] = __uint_as_float(r[t]) * inv_l;
+                        if (MODE == MODE_DIFF) {
+                            tmem_ld32(tO2 + c * 32, r);
+#pragma unroll
+                            for (int t = 0; t < 32; ++t) y[t] -= __uint_as_float(r[t]) * inv_l2;
+                        }
+                        if (row < p.N) {
+                            uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+                            for (int v4 = 0; v4 < 4; ++v4) {
+                                uint4 u;
+                                u.x = pack_bf16x2(y[v4 * 8 + 0], y[v4 * 8 + 1]);
+                                u.y = pack_bf16x2(y[v4 * 8 + 2], y[v4 * 8 + 3]);
+                                u.z = pack_bf16x2(y[v4 * 8 + 4], y[v4 * 8 + 5]);
+                                u.w = pack_bf16x2(y[v4 * 8 + 6], y[v4 * 8 + 7]);
+                                dst[v4] = u;
+                            }
+                        }
+                    }
+                }
+            }
+        }
+    }
+
+    // ---- teardown
+    tc_fence_before();
+    __syncthreads();
+    if (warp == MMA_WARP) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+    if (threadIdx.x == 0 && *abort_flag) atomicExch(p.status, 6 /* SWA_ERR_TIMEOUT */);
+}
+
+// One CTA waits on a barrier nobody arrives at; the bounded wait must run out and report.
+__global__ void watchdog_selftest_kernel(int* status, unsigned long long limit_ns) {
+    __shared__ __align__(8) uint64_t b;
+    __shared__ int abort_word;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&b), 1);
+        abort_word = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const bool ok = mbar_wait_bounded(smem_u32(&b), 0, &abort_word, limit_ns);
+        if (!ok) atomicExch(status, 6 /* SWA_ERR_TIMEOUT */);
+    }
+}
+
+}  // namespace swa

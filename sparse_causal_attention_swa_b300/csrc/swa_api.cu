@@ -1,0 +1,323 @@
+// swa_api.cu -- the C ABI of libswa_b300.so: argument validation, TMA tensor maps, the
+// strided tile list, and kernel launches.  Declarations and the contract of every entry
+// point are in include/swa_b300.h.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <tuple>
+#include <vector>
+
+#include "attn_fwd.cuh"
+#include "swa_b300.h"
+
+namespace {
+
+using swa::BM;
+using swa::BN;
+using swa::KParams;
+
+constexpr int kMaxDevices = 64;
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s per bounded wait
+
+// Device status word: kernels record SWA_ERR_TIMEOUT here when a bounded wait runs out.
+__device__ int g_status_word;
+
+struct DeviceState {
+    bool probed = false;
+    bool supported = false;
+    int* status = nullptr;  // device address of g_status_word
+    bool attr_set[2][3] = {};
+    // strided tile lists, keyed by (N, W, stride, rows per block)
+    std::map<std::tuple<int, int, int, int>, int*> tile_lists;
+};
+
+std::mutex g_mutex;
+DeviceState g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+int current_device_state(DeviceState** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SWA_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return SWA_ERR_UNSUPPORTED;
+    DeviceState& st = g_dev[dev];
+    if (!st.probed) {
+        int major = 0, minor = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+            return SWA_ERR_CUDA;
+        st.supported = (major == 10 && minor == 3);
+        if (st.supported) {
+            void* p = nullptr;
+            if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return SWA_ERR_CUDA;
+            st.status = static_cast<int*>(p);
+        }
+        st.probed = true;
+    }
+    if (!st.supported) return SWA_ERR_UNSUPPORTED;
+    if (!g_encode) {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                             cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || fn == nullptr)
+            return SWA_ERR_CUDA;
+        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    *out = &st;
+    return SWA_OK;
+}
+
+// 3-D view [nmat][rows][d] of a bf16 tensor; consecutive rows are `row_stride` elements
+// apart and consecutive matrices (heads) `mat_stride` elements apart.  The box is
+// 64 columns (128 bytes, one swizzle span) x 128 rows x 1 matrix, 128-byte swizzled.
+int make_map(CUtensorMap* m, const void* base, int d, long long rows, long long row_stride,
+             long long nmat, long long mat_stride) {
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)rows, (cuuint64_t)nmat};
+    cuuint64_t strides[2] = {(cuuint64_t)row_stride * 2, (cuuint64_t)mat_stride * 2};
+    cuuint32_t box[3] = {64, 128, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? SWA_OK : SWA_ERR_CUDA;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_common(int B, int Hq, int Hkv, int N, int d, float scale) {
+    if (B < 1 || Hq < 1 || Hkv < 1 || N < 1) return SWA_ERR_SHAPE;
+    if (Hq % Hkv != 0) return SWA_ERR_SHAPE;
+    // grid and TMA coordinate limits: rows and heads are 32-bit coordinates
+    if ((long long)B * Hq > (1ll << 24) || (long long)N > (1ll << 30)) return SWA_ERR_SHAPE;
+    if (d != 64 && d != 128) return SWA_ERR_UNSUPPORTED;
+    if (!std::isfinite(scale) || !(scale > 0.f)) return SWA_ERR_VALUE;
+    return SWA_OK;
+}
+
+template <int D, int MODE>
+int launch(const KParams& kp, int n_items, cudaStream_t stream, DeviceState& st) {
+    using L = swa::SmemLayout<D, MODE>;
+    auto kern = swa::attn_fwd_kernel<D, MODE>;
+    bool& set = st.attr_set[D == 128 ? 1 : 0][MODE];
+    if (!set) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::BYTES) !=
+            cudaSuccess)
+            return SWA_ERR_CUDA;
+        set = true;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)n_items, 1, 1);
+    cfg.blockDim = dim3(swa::NUM_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = L::BYTES;
+    cfg.stream = stream;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, kp);
+    return e == cudaSuccess ? SWA_OK : SWA_ERR_CUDA;
+}
+
+template <int MODE>
+int dispatch(int d, const KParams& kp, int n_items, cudaStream_t stream, DeviceState& st) {
+    if (d == 128) return launch<128, MODE>(kp, n_items, stream, st);
+    return launch<64, MODE>(kp, n_items, stream, st);
+}
+
+void fill_common(KParams& kp, int B, int Hq, int Hkv, int N, int W, int stride, float scale,
+                 void* out, DeviceState& st) {
+    kp.out = static_cast<__nv_bfloat16*>(out);
+    kp.tiles = nullptr;
+    kp.status = st.status;
+    kp.wait_limit_ns = kWaitLimitNs;
+    kp.B = B;
+    kp.Hq = Hq;
+    kp.Hkv = Hkv;
+    kp.N = N;
+    kp.W = W;
+    kp.stride = stride;
+    kp.n_qtiles = (N + BM - 1) / BM;
+    kp.scale_log2 = scale * 1.4426950408889634f;
+    kp.lambda = 0.f;
+}
+
+// Work items: two slots per CTA.  Query heads of one GQA group are paired when the group
+// size is even; otherwise the slots are two consecutive row tiles of one head.
+int n_items_for(const KParams& kp) {
+    if (kp.pair_mode) return kp.B * kp.Hkv * ((kp.Hq / kp.Hkv) / 2) * kp.n_qtiles;
+    return kp.B * kp.Hq * ((kp.n_qtiles + 1) / 2);
+}
+
+// The strided tile list: for every row block (the union of an item's rows), the compact
+// strided-key tiles that hold keys 0, s, 2s, ... before the block's last window start,
+// then the window tiles from the first row's window start to the block's last row.
+int get_tile_list(DeviceState& st, int N, int W, int stride, int rows_per_block,
+                  cudaStream_t stream, const int** out) {
+    auto key = std::make_tuple(N, W, stride, rows_per_block);
+    auto it = st.tile_lists.find(key);
+    if (it != st.tile_lists.end()) {
+        *out = it->second;
+        return SWA_OK;
+    }
+    const int nblk = (N + rows_per_block - 1) / rows_per_block;
+    std::vector<int> offs(nblk + 1, 0), ents;
+    for (int blk = 0; blk < nblk; ++blk) {
+        const long long R0 = (long long)blk * rows_per_block;
+        const long long R1 = std::min<long long>(R0 + rows_per_block, N) - 1;
+        const long long lo0 = std::max<long long>(0, R0 - W + 1);
+        const long long lo1 = std::max<long long>(0, R1 - W + 1);
+        const long long nkeys = (lo1 + stride - 1) / stride;  // multiples of s below lo1
+        const long long ncompact = (nkeys + BN - 1) / BN;
+        for (long long c = 0; c < ncompact; ++c)
+            ents.push_back((swa::TILE_KIND_STRIDED << swa::TILE_KIND_SHIFT) | (int)c);
+        for (long long t = lo0 / BN; t <= R1 / BN; ++t)
+            ents.push_back((swa::TILE_KIND_WINDOW << swa::TILE_KIND_SHIFT) | (int)t);
+        offs[blk + 1] = (int)ents.size();
+    }
+    std::vector<int> host(offs);
+    host.insert(host.end(), ents.begin(), ents.end());
+    int* dptr = nullptr;
+    if (cudaMalloc(&dptr, host.size() * sizeof(int)) != cudaSuccess) return SWA_ERR_CUDA;
+    if (cudaMemcpyAsync(dptr, host.data(), host.size() * sizeof(int), cudaMemcpyHostToDevice,
+                        stream) != cudaSuccess ||
+        cudaStreamSynchronize(stream) != cudaSuccess) {
+        cudaFree(dptr);
+        return SWA_ERR_CUDA;
+    }
+    st.tile_lists[key] = dptr;
+    *out = dptr;
+    return SWA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* swa_status_string(int status) {
+    switch (status) {
+        case SWA_OK: return "ok";
+        case SWA_ERR_NULL: return "null pointer argument";
+        case SWA_ERR_SHAPE: return "invalid shape argument";
+        case SWA_ERR_ALIGN: return "pointer not 16-byte aligned";
+        case SWA_ERR_UNSUPPORTED: return "unsupported head dimension or device (needs d in {64,128} on sm_103)";
+        case SWA_ERR_CUDA: return "CUDA runtime or driver error";
+        case SWA_ERR_TIMEOUT: return "kernel watchdog: a bounded wait ran out";
+        case SWA_ERR_VALUE: return "invalid scalar argument (scale must be finite and > 0; lambda finite)";
+        default: return "unknown status";
+    }
+}
+
+int swa_attn_fwd(const void* q, const void* k, const void* v, void* out, int B, int Hq, int Hkv,
+                 int N, int d, int W, float scale, void* stream) {
+    if (!q || !k || !v || !out) return SWA_ERR_NULL;
+    if (W < 1) return SWA_ERR_SHAPE;
+    int rc = check_common(B, Hq, Hkv, N, d, scale);
+    if (rc) return rc;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return SWA_ERR_ALIGN;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceState* st = nullptr;
+    if ((rc = current_device_state(&st))) return rc;
+    KParams kp;
+    std::memset(&kp, 0, sizeof(kp));
+    fill_common(kp, B, Hq, Hkv, N, std::min(W, N), 1, scale, out, *st);
+    kp.pair_mode = ((Hq / Hkv) % 2 == 0) ? 1 : 0;
+    if ((rc = make_map(&kp.tm_q, q, d, N, d, (long long)B * Hq, (long long)N * d))) return rc;
+    if ((rc = make_map(&kp.tm_k, k, d, N, d, (long long)B * Hkv, (long long)N * d))) return rc;
+    if ((rc = make_map(&kp.tm_v, v, d, N, d, (long long)B * Hkv, (long long)N * d))) return rc;
+    return dispatch<swa::MODE_WINDOW>(d, kp, n_items_for(kp), static_cast<cudaStream_t>(stream),
+                                      *st);
+}
+
+int strided_attn_fwd(const void* q, const void* k, const void* v, void* out, int B, int Hq,
+                     int Hkv, int N, int d, int W, int stride, float scale, void* stream) {
+    if (!q || !k || !v || !out) return SWA_ERR_NULL;
+    if (W < 1 || stride < 1) return SWA_ERR_SHAPE;
+    int rc = check_common(B, Hq, Hkv, N, d, scale);
+    if (rc) return rc;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return SWA_ERR_ALIGN;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceState* st = nullptr;
+    if ((rc = current_device_state(&st))) return rc;
+    KParams kp;
+    std::memset(&kp, 0, sizeof(kp));
+    const int Wc = std::min(W, N);
+    const int sc = std::min(stride, N);  // a stride >= N opens key 0 only, as stride N does
+    fill_common(kp, B, Hq, Hkv, N, Wc, sc, scale, out, *st);
+    kp.pair_mode = ((Hq / Hkv) % 2 == 0) ? 1 : 0;
+    const int* list = nullptr;
+    if ((rc = get_tile_list(*st, N, Wc, sc, kp.pair_mode ? BM : 2 * BM,
+                            static_cast<cudaStream_t>(stream), &list)))
+        return rc;
+    kp.tiles = list;
+    const long long ns = (N - 1) / sc + 1;  // keys 0, s, 2s, ... < N
+    if ((rc = make_map(&kp.tm_q, q, d, N, d, (long long)B * Hq, (long long)N * d))) return rc;
+    if ((rc = make_map(&kp.tm_k, k, d, N, d, (long long)B * Hkv, (long long)N * d))) return rc;
+    if ((rc = make_map(&kp.tm_v, v, d, N, d, (long long)B * Hkv, (long long)N * d))) return rc;
+    if ((rc = make_map(&kp.tm_k2, k, d, ns, (long long)sc * d, (long long)B * Hkv,
+                       (long long)N * d)))
+        return rc;
+    if ((rc = make_map(&kp.tm_v2, v, d, ns, (long long)sc * d, (long long)B * Hkv,
+                       (long long)N * d)))
+        return rc;
+    return dispatch<swa::MODE_STRIDED>(d, kp, n_items_for(kp), static_cast<cudaStream_t>(stream),
+                                       *st);
+}
+
+int diff_attn_fwd(const void* q1, const void* k1, const void* q2, const void* k2, const void* v,
+                  float lambda, void* out, int B, int Hq, int Hkv, int N, int d, float scale,
+                  void* stream) {
+    if (!q1 || !k1 || !q2 || !k2 || !v || !out) return SWA_ERR_NULL;
+    int rc = check_common(B, Hq, Hkv, N, d, scale);
+    if (rc) return rc;
+    if (!std::isfinite(lambda)) return SWA_ERR_VALUE;
+    if (!aligned16(q1) || !aligned16(k1) || !aligned16(q2) || !aligned16(k2) || !aligned16(v) ||
+        !aligned16(out))
+        return SWA_ERR_ALIGN;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceState* st = nullptr;
+    if ((rc = current_device_state(&st))) return rc;
+    KParams kp;
+    std::memset(&kp, 0, sizeof(kp));
+    fill_common(kp, B, Hq, Hkv, N, N, 1, scale, out, *st);
+    kp.lambda = lambda;
+    kp.pair_mode = 1;  // the two slots are the two score streams of the same rows
+    if ((rc = make_map(&kp.tm_q, q1, d, N, d, (long long)B * Hq, (long long)N * d))) return rc;
+    if ((rc = make_map(&kp.tm_k, k1, d, N, d, (long long)B * Hkv, (long long)N * d))) return rc;
+    if ((rc = make_map(&kp.tm_q2, q2, d, N, d, (long long)B * Hq, (long long)N * d))) return rc;
+    if ((rc = make_map(&kp.tm_k2, k2, d, N, d, (long long)B * Hkv, (long long)N * d))) return rc;
+    if ((rc = make_map(&kp.tm_v, v, d, N, d, (long long)B * Hkv, (long long)N * d))) return rc;
+    const int n_items = B * Hq * kp.n_qtiles;
+    return dispatch<swa::MODE_DIFF>(d, kp, n_items, static_cast<cudaStream_t>(stream), *st);
+}
+
+int swa_device_status(void* stream) {
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return SWA_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceState* st = nullptr;
+    int rc = current_device_state(&st);
+    if (rc) return rc;
+    int word = 0;
+    if (cudaMemcpy(&word, st->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return SWA_ERR_CUDA;
+    const int zero = 0;
+    if (cudaMemcpy(st->status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+        return SWA_ERR_CUDA;
+    return word == 0 ? SWA_OK : word;
+}
+
+int swa_watchdog_selftest(int limit_us, void* stream) {
+    if (limit_us < 1 || limit_us > 1000000) return SWA_ERR_VALUE;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceState* st = nullptr;
+    int rc = current_device_state(&st);
+    if (rc) return rc;
+    swa::watchdog_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+        st->status, (unsigned long long)limit_us * 1000ull);
+    return cudaPeekAtLastError() == cudaSuccess ? SWA_OK : SWA_ERR_CUDA;
+}
+
+}  // extern "C"

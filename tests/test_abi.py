@@ -1,0 +1,96 @@
+"""The C-ABI library: it loads, exports every symbol the header declares, and rejects bad
+arguments on the host before touching a GPU (so these run without one)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+import sparse_causal_attention_swa_b300 as pkg
+
+HEADER = os.path.join(ROOT, "include", "swa_b300.h")
+
+
+def declared_functions():
+    src = open(HEADER, encoding="utf-8").read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?(?:int|char\s*\*|const char\s*\*|void)\s*\*?\s*"
+                                 r"([a-z_][a-z0-9_]*)\s*\(", src, flags=re.M)))
+
+
+def test_header_declares_the_three_calls():
+    names = declared_functions()
+    for n in ("swa_attn_fwd", "strided_attn_fwd", "diff_attn_fwd", "swa_status_string",
+              "swa_device_status", "swa_watchdog_selftest"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol():
+    lib = ctypes.CDLL(pkg.LIBRARY_PATH)
+    for n in declared_functions():
+        assert hasattr(lib, n), n
+
+
+def test_status_strings():
+    for code in range(0, 8):
+        s = pkg.swa_status_string(code)
+        assert s and s != "unknown status"
+    assert pkg.swa_status_string(99) == "unknown status"
+
+
+P = 0x10000  # a 16-byte aligned, never dereferenced pointer value
+lib = None
+
+
+@pytest.fixture(scope="module")
+def L():
+    return pkg.load()
+
+
+def call_swa(L, q=P, k=P, v=P, out=P, B=1, Hq=2, Hkv=2, N=128, d=64, W=16, scale=0.125):
+    return L.swa_attn_fwd(q, k, v, out, B, Hq, Hkv, N, d, W, scale, None)
+
+
+def test_swa_validation(L):
+    assert call_swa(L, q=None) == 1
+    assert call_swa(L, out=None) == 1
+    assert call_swa(L, B=0) == 2
+    assert call_swa(L, N=0) == 2
+    assert call_swa(L, W=0) == 2
+    assert call_swa(L, Hq=3, Hkv=2) == 2
+    assert call_swa(L, d=96) == 4
+    assert call_swa(L, d=256) == 4
+    assert call_swa(L, scale=0.0) == 7
+    assert call_swa(L, scale=float("nan")) == 7
+    assert call_swa(L, scale=-1.0) == 7
+    assert call_swa(L, k=P + 8) == 3
+    assert call_swa(L, out=P + 2) == 3
+
+
+def test_strided_validation(L):
+    f = L.strided_attn_fwd
+    assert f(None, P, P, P, 1, 2, 2, 128, 64, 16, 4, 0.125, None) == 1
+    assert f(P, P, P, P, 1, 2, 2, 128, 64, 16, 0, 0.125, None) == 2
+    assert f(P, P, P, P, 1, 2, 2, 128, 64, 0, 4, 0.125, None) == 2
+    assert f(P, P, P, P, 1, 2, 2, 128, 80, 16, 4, 0.125, None) == 4
+    assert f(P, P, P, P + 4, 1, 2, 2, 128, 64, 16, 4, 0.125, None) == 3
+
+
+def test_diff_validation(L):
+    f = L.diff_attn_fwd
+    assert f(P, P, None, P, P, 0.8, P, 1, 2, 2, 128, 64, 0.125, None) == 1
+    assert f(P, P, P, P, P, float("inf"), P, 1, 2, 2, 128, 64, 0.125, None) == 7
+    assert f(P, P, P, P, P, 0.8, P, 1, 2, 4, 128, 64, 0.125, None) == 2
+    assert f(P, P, P, P, P + 8, 0.8, P, 1, 2, 2, 128, 64, 0.125, None) == 3
+
+
+def test_watchdog_selftest_validation(L):
+    assert L.swa_watchdog_selftest(0, None) == 7
+    assert L.swa_watchdog_selftest(2_000_000, None) == 7
+
+
+def test_binding_raises_with_status():
+    with pytest.raises(pkg.SwaError) as e:
+        pkg.swa_attn_fwd(P, P, P, P, 1, 2, 2, 128, 64, 0, 0.125, stream=0)
+    assert e.value.code == 2

@@ -1,0 +1,159 @@
+"""GPU parity: the sm_103a kernels, called through the C ABI, against the fp64 oracle on
+the same seeded bf16 inputs.  Tolerances: |gpu - oracle| <= 1.5e-2 + 1e-2 |oracle| for
+causal SWA and local+strided, |gpu - oracle| <= 3e-2 for differential attention."""
+import numpy as np
+import pytest
+import torch
+
+import swa_inputs
+from swa_inputs import Workload
+import sparse_causal_attention_swa_b300 as pkg
+from gpu_util import assert_close, run_gpu, run_oracle, to_dev, to_f64, out_like
+
+pytestmark = pytest.mark.gpu
+
+HEADS = [(1, 1), (2, 1), (3, 3), (4, 2), (6, 2), (8, 2)]
+
+
+def _w(kind, B, Hq, Hkv, N, d, W, stride=0, lam=0.0, seed=0):
+    return Workload(f"t_{kind}", kind, B, Hq, Hkv, N, d, W, stride=stride, lam=lam,
+                    seed_index=1000 + seed)
+
+
+def check(w, rows=None, label=""):
+    inp = swa_inputs.make_inputs(w)
+    got = run_gpu(w, inp)
+    ref = run_oracle(w, inp, rows=rows)
+    if rows is not None:
+        got = got[:, :, rows]
+    return assert_close(w, got, ref, label or f"{w}")
+
+
+# ------------------------------------------------------------------------- causal SWA
+def test_small_config_full():
+    w = swa_inputs.WORKLOADS["swa_small"]
+    err = check(w, label="swa_small")
+    print(f"swa_small max err {err:.3e}")
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("heads", HEADS)
+def test_window_sweep(d, heads):
+    Hq, Hkv = heads
+    for N in (1, 17, 128, 129, 255, 300, 513):
+        for W in sorted({1, 2, 63, 64, 65, 127, 128, 129, max(1, N - 1), N, 2 * N}):
+            check(_w("swa", 1, Hq, Hkv, N, d, W, seed=N * 7 + W), label=f"N={N} W={W} d={d} {heads}")
+
+
+def test_batch_and_many_heads():
+    check(_w("swa", 3, 8, 4, 700, 128, 200, seed=5))
+    check(_w("swa", 2, 9, 3, 640, 64, 77, seed=6))
+
+
+def test_w1_returns_v_bit_exact():
+    for Hq, Hkv, d in ((2, 2, 64), (8, 2, 128), (3, 1, 128)):
+        w = _w("swa", 2, Hq, Hkv, 389, d, 1, seed=11)
+        inp = swa_inputs.make_inputs(w)
+        got = run_gpu(w, inp)
+        v = swa_inputs.bf16_bits_to_f64(inp["v"])
+        expect = np.repeat(v, Hq // Hkv, axis=1)
+        assert np.array_equal(got, expect)
+
+
+def test_w_ge_n_bitwise_identical():
+    w = _w("swa", 1, 4, 2, 777, 128, 777, seed=12)
+    inp = swa_inputs.make_inputs(w)
+    a = run_gpu(w, inp)
+    for W in (778, 2 * 777, 1 << 30):
+        assert np.array_equal(run_gpu(w.replace(W=W), inp), a)
+
+
+def test_deterministic_and_stream():
+    w = _w("swa", 1, 4, 2, 1000, 128, 300, seed=13)
+    inp = swa_inputs.make_inputs(w)
+    d = {n: to_dev(a) for n, a in inp.items()}
+    outs = []
+    s = torch.cuda.Stream()
+    for _ in range(2):
+        out, _ = out_like(d["q"])
+        with torch.cuda.stream(s):
+            pkg.swa_attn_fwd(d["q"], d["k"], d["v"], out, 1, 4, 2, 1000, 128, 300, w.scale,
+                             stream=s)
+        s.synchronize()
+        outs.append(to_f64(out))
+    assert np.array_equal(outs[0], outs[1])
+
+
+def test_tensor_wrapper_host_roundtrip():
+    w = _w("swa", 1, 2, 1, 300, 64, 50, seed=14)
+    inp = swa_inputs.make_inputs(w)
+    q = torch.from_numpy(inp["q"].view(np.int16)).view(torch.bfloat16)
+    k = torch.from_numpy(inp["k"].view(np.int16)).view(torch.bfloat16)
+    v = torch.from_numpy(inp["v"].view(np.int16)).view(torch.bfloat16)
+    out = pkg.swa_attention(q, k, v, 50)
+    assert out.device.type == "cpu"
+    assert_close(w, out.float().numpy().astype(np.float64), run_oracle(w, inp), "wrapper")
+
+
+def _full_size(name, n_random=200, boundary_step=1):
+    w = swa_inputs.WORKLOADS[name]
+    rows = swa_inputs.sample_rows(w.N, n_random, seed=w.seed, tile=128)
+    if boundary_step > 1:
+        keep = set(range(256)) | set(range(w.N - 128, w.N))
+        keep |= {r for r in rows if (r // 128) % boundary_step == 0 or r % 128 not in (0, 127)}
+        rows = np.array(sorted(keep), dtype=np.int64)
+    err = check(w, rows=rows, label=name)
+    print(f"{name}: {rows.size} rows x {w.B * w.Hq} heads checked, max err {err:.3e}")
+
+
+def test_mistral_full_size_sampled():
+    _full_size("mistral_swa")
+
+
+def test_gemma_swa_full_size_sampled():
+    _full_size("gemma_swa", n_random=100)
+
+
+def test_gemma_global_full_size_sampled():
+    _full_size("gemma_global", n_random=40, boundary_step=16)
+
+
+# ------------------------------------------------------------------------- local + strided
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("heads", [(1, 1), (4, 2), (3, 1)])
+def test_strided_sweep(d, heads):
+    Hq, Hkv = heads
+    for N in (1, 100, 129, 300, 700):
+        for W, s in ((1, 1), (2, 3), (16, 4), (64, 7), (128, 128), (129, 64), (200, 1000),
+                     (N, 5), (3, 128), (300, 13)):
+            check(_w("strided", 1, Hq, Hkv, N, d, W, stride=s, seed=N + 3 * W + s),
+                  label=f"strided N={N} W={W} s={s} d={d} {heads}")
+
+
+def test_strided_full_size_sampled():
+    _full_size("strided")
+
+
+# ------------------------------------------------------------------------- differential
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("heads", [(1, 1), (2, 2), (4, 2)])
+def test_diff_sweep(d, heads):
+    Hq, Hkv = heads
+    for N in (1, 60, 128, 200, 513):
+        for lam in (0.0, 0.8, 1.0):
+            check(_w("diff", 1, Hq, Hkv, N, d, N, lam=lam, seed=N + int(10 * lam)),
+                  label=f"diff N={N} lam={lam} d={d} {heads}")
+
+
+def test_diff_full_size_sampled():
+    _full_size("diff")
+
+
+# ------------------------------------------------------------------------- watchdog
+def test_watchdog_reports_timeout_and_clears():
+    assert pkg.swa_device_status() == 0
+    pkg.swa_watchdog_selftest(20_000)  # 20 ms bounded wait on a barrier nobody arrives at
+    assert pkg.swa_device_status() == 6
+    assert pkg.swa_device_status() == 0
+    # the context is still usable afterwards
+    check(_w("swa", 1, 2, 2, 200, 64, 30, seed=99))
