@@ -1,0 +1,469 @@
+#!/usr/bin/env python3
+"""Benchmark: causal SWA forward band-only useful TFLOP/s at the Mistral-7B shape on B300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--all] [--no-cpu-baseline] [--no-e2e]
+
+One step = one forward call of the hot path over one batch of synthetic, seeded bf16
+input (i.i.d. N(0,1), layout [B, H, N, d]) that is already resident in HBM.  The default
+workload is the Mistral-7B-shaped causal SWA layer (B=1, Hq=32, Hkv=8, N=16384, d=128,
+W=4096).  Its inputs plus output (320 MiB) exceed the 126 MB L2, so no flush is needed
+between steps.  Useful FLOPs count only allowed (query, key) pairs: 4 d per pair per
+query head.
+
+Rank 0 prints one JSON line.  Under torchrun (N > 1) every rank runs its own replica of
+the workload (weak scaling, no data-path collective); the timed region is bracketed by a
+barrier and device synchronisation, and the time is the maximum over ranks.
+
+``--impl reference`` times the fp64 CPU oracle (the only reference this method has) on
+the host cores over bounded row samples of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import swa_inputs  # noqa: E402
+from sparse_causal_attention_swa_b300 import flops as flopcount  # noqa: E402
+
+METRIC = "causal SWA fwd band-only TFLOP/s (Mistral shape, 1 B300) and % of BF16 peak"
+DEFAULT_WORKLOAD = "mistral_swa"
+KERNEL_SOURCES = ["sparse_causal_attention_swa_b300/csrc/attn_fwd.cuh",
+                  "sparse_causal_attention_swa_b300/csrc/ptx.cuh",
+                  "sparse_causal_attention_swa_b300/csrc/swa_api.cu"]
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+# DRAM traffic per launch of the dominant kernel, from one ncu capture (dram__bytes_read.sum
+# + dram__bytes_write.sum), keyed by workload, with the hash of the kernel sources it was
+# taken on.  A changed kernel invalidates the figure (reported as null).
+TRAFFIC = {
+    "mistral_swa": (331.8e6, "6c8ff68bf935c986"),
+}
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return pk, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def workload_units(w: swa_inputs.Workload):
+    fl = flopcount.useful_flops(w.kind, w.B, w.Hq, w.N, w.d, w.W, w.stride)
+    by = flopcount.algorithmic_bytes(w.kind, w.B, w.Hq, w.Hkv, w.N, w.d)
+    return fl, by
+
+
+# ------------------------------------------------------------------------------ distributed
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def max_over_ranks(value: float, ws: int, device=None) -> float:
+    """Maximum of a per-rank float over the process group (identity when ws == 1)."""
+    if ws == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(ws: int, device=None):
+    if ws > 1:
+        import torch.distributed as dist
+
+        if device is not None and device.type == "cuda":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+# ------------------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid: str | None, period_ms: int = 50):
+        self.proc = None
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               f"-lms={period_ms}"]
+        if uuid:
+            cmd.insert(1, f"--id={uuid}")
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=10)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+                power.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(smax)),
+                "power_w_max": float(max(power)), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------------------ CPU oracle
+def oracle_sample_rows(w: swa_inputs.Workload, n_rows: int, seed: int) -> np.ndarray:
+    """A bounded, seeded sample of query rows spread over the sequence."""
+    rng = np.random.default_rng(seed)
+    return np.sort(rng.choice(w.N, size=min(n_rows, w.N), replace=False)).astype(np.int64)
+
+
+def sample_flops(w: swa_inputs.Workload, rows: np.ndarray) -> float:
+    i = rows.astype(np.int64)
+    if w.kind == "swa":
+        per = np.minimum(i + 1, w.W)
+        return 4.0 * w.d * float(per.sum()) * w.B * w.Hq
+    if w.kind == "strided":
+        lo = np.maximum(0, i - w.W + 1)
+        per = np.minimum(i + 1, w.W) + np.where(lo > 0, (lo - 1) // w.stride + 1, 0)
+        return 4.0 * w.d * float(per.sum()) * w.B * w.Hq
+    return 8.0 * w.d * float((i + 1).sum()) * w.B * w.Hq
+
+
+def run_oracle_rows(w, inp, rows):
+    import oracle
+
+    if w.kind == "diff":
+        return oracle.diff(inp["q1"], inp["k1"], inp["q2"], inp["k2"], inp["v"], w.lam, w.scale,
+                           rows=rows)
+    kind = "window" if w.kind == "swa" else "strided"
+    return oracle.attn(inp["q"], inp["k"], inp["v"], w.W, w.scale, kind=kind, stride=w.stride,
+                       rows=rows)
+
+
+def oracle_inputs_f64(inp):
+    """Widen the bf16 inputs once, so the timed oracle calls measure its arithmetic."""
+    return {n: swa_inputs.bf16_bits_to_f64(a) for n, a in inp.items()}
+
+
+def cpu_baseline(w, inp, budget_s: float = 15.0):
+    """Time the oracle as it stands on the host cores over a bounded row sample."""
+    import oracle
+
+    oracle.build()
+    inp = oracle_inputs_f64(inp)
+    probe = oracle_sample_rows(w, 4, seed=w.seed)
+    t0 = time.perf_counter()
+    run_oracle_rows(w, inp, probe)
+    dt = max(time.perf_counter() - t0, 1e-3)
+    n = int(max(4, min(w.N, 4 * budget_s / dt)))
+    rows = oracle_sample_rows(w, n, seed=w.seed + 1)
+    t0 = time.perf_counter()
+    run_oracle_rows(w, inp, rows)
+    dt = time.perf_counter() - t0
+    fl = sample_flops(w, rows)
+    return {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.max_threads(),
+            "kind": "oracle",
+            "sample": f"{rows.size} seeded random query rows x all {w.B * w.Hq} heads of "
+                      f"{w.name} ({fl:.3e} useful FLOPs, {dt:.1f} s, fp64)"}
+
+
+def reference_arm(args, w, ws, rank):
+    """--impl reference: the fp64 oracle on host cores, same metric and workload."""
+    if rank != 0:
+        return
+    import oracle
+
+    oracle.build()
+    inp = oracle_inputs_f64(swa_inputs.make_inputs(w))
+    fl_full, _ = workload_units(w)
+    # size every step so warmup + steps stay within about two minutes
+    probe = oracle_sample_rows(w, 4, seed=w.seed)
+    t0 = time.perf_counter()
+    run_oracle_rows(w, inp, probe)
+    dt = max(time.perf_counter() - t0, 1e-3)
+    per_step_budget = 120.0 / max(1, args.steps + args.warmup)
+    n = int(max(1, min(w.N, 4 * per_step_budget / dt)))
+    samples = [oracle_sample_rows(w, n, seed=w.seed + 10 + s)
+               for s in range(args.steps + args.warmup)]
+    for s in range(args.warmup):
+        run_oracle_rows(w, inp, samples[s])
+    fl = 0.0
+    t0 = time.perf_counter()
+    for s in range(args.warmup, args.warmup + args.steps):
+        run_oracle_rows(w, inp, samples[s])
+        fl += sample_flops(w, samples[s])
+    dt = time.perf_counter() - t0
+    value = fl / dt / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(w, fl_full),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.max_threads(),
+                         "kind": "oracle",
+                         "sample": f"{n} seeded random query rows x {w.B * w.Hq} heads per "
+                                   f"step"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(w, fl):
+    cfg = {"workload": w.name, "kind": w.kind, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "N": w.N,
+           "d": w.d, "W": w.W, "scale": w.scale, "useful_flops_per_step": fl,
+           "l2": "inputs+output larger than the 126 MB L2; no flush between steps"}
+    if w.kind == "strided":
+        cfg["stride"] = w.stride
+    if w.kind == "diff":
+        cfg["lambda"] = w.lam
+        cfg["flop_convention"] = "8 d per causal pair (two attention maps)"
+    return cfg
+
+
+# ------------------------------------------------------------------------------ GPU arm
+def to_device(inp, dev):
+    import torch
+
+    return {n: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+            for n, a in inp.items()}
+
+
+def launch(pkg, w, t, out, stream):
+    if w.kind == "swa":
+        pkg.swa_attn_fwd(t["q"], t["k"], t["v"], out, w.B, w.Hq, w.Hkv, w.N, w.d, w.W, w.scale,
+                         stream)
+    elif w.kind == "strided":
+        pkg.strided_attn_fwd(t["q"], t["k"], t["v"], out, w.B, w.Hq, w.Hkv, w.N, w.d, w.W,
+                             w.stride, w.scale, stream)
+    else:
+        pkg.diff_attn_fwd(t["q1"], t["k1"], t["q2"], t["k2"], t["v"], w.lam, out, w.B, w.Hq,
+                          w.Hkv, w.N, w.d, w.scale, stream)
+
+
+def bench_workload(args, w, ws, rank, dev, want_cpu, want_e2e):
+    import torch
+
+    import sparse_causal_attention_swa_b300 as pkg
+
+    pkg.load()
+    inp = swa_inputs.make_inputs(w)
+    t = to_device(inp, dev)
+    first = t["q1"] if w.kind == "diff" else t["q"]
+    out = torch.empty_like(first)
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+    fl, algo_bytes = workload_units(w)
+
+    for _ in range(args.warmup):
+        launch(pkg, w, t, out, sh)
+    torch.cuda.synchronize(dev)
+    if pkg.swa_device_status(sh) != 0:
+        raise RuntimeError("kernel watchdog fired during warm-up")
+
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+        if uuid and not uuid.startswith("GPU-"):
+            uuid = "GPU-" + uuid
+    except Exception:
+        uuid = None
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    t_begin = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(uuid)
+    time.sleep(0.3)  # let the sampler start
+    barrier(ws, dev)
+    torch.cuda.synchronize(dev)
+    t_begin.record(stream)
+    for s in range(args.steps):
+        starts[s].record(stream)
+        launch(pkg, w, t, out, sh)
+        ends[s].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(ws, dev)
+    clk = clocks.stop()
+    if pkg.swa_device_status(sh) != 0:
+        raise RuntimeError("kernel watchdog fired during the timed region")
+    total_ms = t_begin.elapsed_time(t_end)
+    launch_ms = float(np.mean([a.elapsed_time(b) for a, b in zip(starts, ends)]))
+    total_ms = max_over_ranks(total_ms, ws, dev)
+    launch_ms = max_over_ranks(launch_ms, ws, dev)
+    ms_per_step = total_ms / args.steps
+    value = fl * ws / (ms_per_step * 1e-3) / 1e12
+
+    peaks, peak_src = load_peaks()
+    bf16_peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    achieved_tf = fl / (launch_ms * 1e-3) / 1e12
+    tkey = TRAFFIC.get(w.name)
+    traffic = tkey[0] if (tkey and tkey[1] == kernel_hash()) else None
+    tensor_bound = w.name not in ("swa_small",)
+    if tensor_bound:
+        roofline = {"bound": "tensor", "achieved": achieved_tf, "peak": bf16_peak,
+                    "unit": "TFLOP/s", "frac": achieved_tf / bf16_peak, "traffic": traffic,
+                    "peak_source": f"{peak_src} bf16_tflops (burst, kernel timed alone)",
+                    "kernel": f"attn_fwd_kernel<{w.d},{ {'swa': 0, 'strided': 1, 'diff': 2}[w.kind]}>",
+                    "algorithmic_flops_per_launch": fl,
+                    "hbm_gbs_algorithmic": algo_bytes / (launch_ms * 1e-3) / 1e9}
+    else:
+        gbs = algo_bytes / (launch_ms * 1e-3) / 1e9
+        roofline = {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
+                    "frac": gbs / hbm_peak, "traffic": traffic,
+                    "peak_source": f"{peak_src} hbm_gbs",
+                    "algorithmic_bytes_per_launch": algo_bytes}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic", "config": workload_config(w, fl),
+        "pct_of_bf16_peak": 100.0 * achieved_tf / bf16_peak,
+        "roofline": roofline, "gpu_launches": args.steps, "clocks": clk,
+    }
+    if ws > 1:
+        line["config"]["parallelism"] = f"replicas x{ws} (independent problems per rank)"
+
+    if want_e2e:
+        line["e2e"] = e2e_measure(args, w, inp, pkg, dev, ws)
+    if want_cpu and rank == 0 and ws == 1:
+        line["cpu_baseline"] = cpu_baseline(w, inp)
+    return line
+
+
+def e2e_measure(args, w, inp, pkg, dev, ws):
+    """Same metric through the public API with host buffers: pinned H2D of the inputs, the
+    C-ABI call, D2H of the output, every step inside the timed region."""
+    import torch
+
+    host = {n: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).pin_memory()
+            for n, a in inp.items()}
+    dev_t = {n: torch.empty_like(h, device=dev) for n, h in host.items()}
+    first = dev_t["q1"] if w.kind == "diff" else dev_t["q"]
+    out = torch.empty_like(first)
+    out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+    h2d = sum(h.numel() * 2 for h in host.values())
+    d2h = out.numel() * 2
+    steps = max(3, min(args.steps, 20))
+
+    def step():
+        for n in host:
+            dev_t[n].copy_(host[n], non_blocking=True)
+        launch(pkg, w, dev_t, out, sh)
+        out_host.copy_(out, non_blocking=True)
+
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize(dev)
+    barrier(ws, dev)
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = max_over_ranks(a.elapsed_time(b) / steps, ws, dev)
+    fl, _ = workload_units(w)
+    return {"value": fl * ws / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms,
+            "steps": steps}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(swa_inputs.WORKLOADS))
+    ap.add_argument("--all", action="store_true",
+                    help="one line per workload (measurement sweep, not the headline)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    ws, rank, local = dist_env()
+    w = swa_inputs.WORKLOADS[args.workload]
+
+    if args.impl == "reference":
+        reference_arm(args, w, ws, rank)
+        return 0
+
+    import torch
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if ws > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+    names = sorted(swa_inputs.WORKLOADS) if args.all else [args.workload]
+    for name in names:
+        line = bench_workload(args, swa_inputs.WORKLOADS[name], ws, rank, dev,
+                              want_cpu=not args.no_cpu_baseline and not args.all,
+                              want_e2e=not args.no_e2e)
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())
