@@ -50,8 +50,13 @@ typedef enum swa_status {
     SWA_ERR_UNSUPPORTED = 4, /* d not in {64, 128}, or the current device is not sm_103 */
     SWA_ERR_CUDA = 5,        /* a CUDA runtime / driver call failed (launch, attribute, map) */
     SWA_ERR_TIMEOUT = 6,     /* a kernel-side bounded wait ran out (read by swa_device_status) */
-    SWA_ERR_VALUE = 7        /* scale not finite and > 0, or lambda not finite */
+    SWA_ERR_VALUE = 7,       /* scale not finite and > 0, or lambda not finite */
+    SWA_ERR_TOO_LARGE = 8    /* the problem's tile list exceeds SWA_NOALLOC_TILE_CAPACITY */
 } swa_status;
+
+/* Capacity, in int entries (256 KiB), of the fixed device array that
+ * strided_attn_fwd_noalloc keeps its tile list in. */
+#define SWA_NOALLOC_TILE_CAPACITY 65536
 
 /*
  * Causal sliding-window attention forward ([SWA] §3.1; [AV] step 2):
@@ -78,6 +83,31 @@ int strided_attn_fwd(const void* q, const void* k, const void* v, void* out, int
 int diff_attn_fwd(const void* q1, const void* k1, const void* q2, const void* k2,
                   const void* v, float lambda, void* out, int B, int Hq, int Hkv, int N, int d,
                   float scale, void* stream);
+
+/*
+ * strided_attn_fwd without any device allocation.  The pages have no counterpart to
+ * this call; it exists for callers that cannot call cudaMalloc, for example code that
+ * runs under an external memory manager or an allocator that forbids foreign device
+ * allocations, or a process that must not grow its device footprint after start-up.
+ * Same arguments, semantics and result as strided_attn_fwd.  Instead of the cached,
+ * cudaMalloc'ed tile list, the call rebuilds the list on `stream` with a small device
+ * kernel inside one fixed file-scope device array of SWA_NOALLOC_TILE_CAPACITY ints
+ * (256 KiB, held by every GPU that loads the library until the process exits).
+ *   - The first call on a device looks up that array's device address (once per
+ *     device); make that first call before any stream capture.
+ *   - A problem whose tile list needs more than SWA_NOALLOC_TILE_CAPACITY entries is
+ *     rejected with SWA_ERR_TOO_LARGE before anything is launched.  The list holds
+ *     ceil(N / R) + 1 offsets plus, per block of R rows (R = 128 when Hq / Hkv is even,
+ *     else 256), the strided tiles before the block's windows and its window tiles.
+ *   - Every call shares the one array: calls whose kernels may overlap on the GPU
+ *     (different streams without ordering between them) race on it and must not be
+ *     issued; calls on one stream are ordered and safe.
+ *   - The call itself allocates nothing: no cudaMalloc, no cudaFree, no allocating
+ *     library routine.
+ */
+int strided_attn_fwd_noalloc(const void* q, const void* k, const void* v, void* out, int B,
+                             int Hq, int Hkv, int N, int d, int W, int stride, float scale,
+                             void* stream);
 
 /* Human-readable name of a status code (static storage; never NULL). */
 const char* swa_status_string(int status);

@@ -7,8 +7,8 @@ module is a thin ctypes binding with the same names as the C ABI declared in
 and streams.  There is no CPU fallback: if the library is missing, every call raises.
 
 Low-level calls (pointers or tensors, explicit sizes, asynchronous on ``stream``):
-    swa_attn_fwd, strided_attn_fwd, diff_attn_fwd, swa_status_string,
-    swa_device_status, swa_watchdog_selftest
+    swa_attn_fwd, strided_attn_fwd, diff_attn_fwd, strided_attn_fwd_noalloc,
+    swa_status_string, swa_device_status, swa_watchdog_selftest
 Convenience wrappers on [B, H, N, d] bf16 tensors (allocate ``out``; CPU inputs are
 copied to the current CUDA device and the result copied back):
     swa_attention, strided_attention, diff_attention
@@ -46,6 +46,8 @@ def load():
         lib.swa_attn_fwd.restype = I
         lib.strided_attn_fwd.argtypes = [P, P, P, P, I, I, I, I, I, I, I, F, P]
         lib.strided_attn_fwd.restype = I
+        lib.strided_attn_fwd_noalloc.argtypes = [P, P, P, P, I, I, I, I, I, I, I, F, P]
+        lib.strided_attn_fwd_noalloc.restype = I
         lib.diff_attn_fwd.argtypes = [P, P, P, P, P, F, P, I, I, I, I, I, F, P]
         lib.diff_attn_fwd.restype = I
         lib.swa_status_string.argtypes = [I]
@@ -94,6 +96,14 @@ def swa_attn_fwd(q, k, v, out, B, Hq, Hkv, N, d, W, scale, stream=None):
 def strided_attn_fwd(q, k, v, out, B, Hq, Hkv, N, d, W, stride, scale, stream=None):
     _check(load().strided_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, Hq, Hkv, N, d, W,
                                    stride, float(scale), _stream(stream)), "strided_attn_fwd")
+
+
+def strided_attn_fwd_noalloc(q, k, v, out, B, Hq, Hkv, N, d, W, stride, scale, stream=None):
+    """strided_attn_fwd for callers that cannot allocate device memory: the tile list is
+    rebuilt on the stream inside a fixed device array owned by the library."""
+    _check(load().strided_attn_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, Hq, Hkv, N,
+                                           d, W, stride, float(scale), _stream(stream)),
+           "strided_attn_fwd_noalloc")
 
 
 def diff_attn_fwd(q1, k1, q2, k2, v, lam, out, B, Hq, Hkv, N, d, scale, stream=None):

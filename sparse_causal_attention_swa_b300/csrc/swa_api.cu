@@ -192,6 +192,67 @@ int get_tile_list(DeviceState& st, int N, int W, int stride, int rows_per_block,
     return SWA_OK;
 }
 
+// ---------------------------------------------------------------------------------------
+// Allocation-free strided call: the tile list lives in one fixed device array.
+// ---------------------------------------------------------------------------------------
+static __device__ __align__(256) int g_noalloc_tiles[SWA_NOALLOC_TILE_CAPACITY];
+
+struct NoAllocState {
+    bool ready = false;
+    int* tiles = nullptr;  // device address of g_noalloc_tiles on that device
+};
+NoAllocState g_noalloc[kMaxDevices];
+
+__host__ __device__ inline void noalloc_block_counts(long long blk, int N, int W, int stride,
+                                                     int rpb, long long* ncompact,
+                                                     long long* wfirst, long long* wlast) {
+    const long long R0 = blk * rpb;
+    const long long R1 = (R0 + rpb < N ? R0 + rpb : N) - 1;
+    const long long lo0 = R0 - W + 1 > 0 ? R0 - W + 1 : 0;
+    const long long lo1 = R1 - W + 1 > 0 ? R1 - W + 1 : 0;
+    const long long nkeys = (lo1 + stride - 1) / stride;
+    *ncompact = (nkeys + BN - 1) / BN;
+    *wfirst = lo0 / BN;
+    *wlast = R1 / BN;
+}
+
+long long noalloc_list_length(int N, int W, int stride, int rpb) {
+    const long long nblk = (N + rpb - 1) / rpb;
+    long long len = nblk + 1;
+    for (long long blk = 0; blk < nblk; ++blk) {
+        long long nc, wf, wl;
+        noalloc_block_counts(blk, N, W, stride, rpb, &nc, &wf, &wl);
+        len += nc + (wl - wf + 1);
+        if (len > SWA_NOALLOC_TILE_CAPACITY) break;
+    }
+    return len;
+}
+
+// Thread 0 writes the offsets; then every thread fills the entries of its blocks.
+__global__ void noalloc_build_tiles_kernel(int* list, int N, int W, int stride, int rpb) {
+    const int nblk = (N + rpb - 1) / rpb;
+    if (threadIdx.x == 0) {
+        int pos = 0;
+        list[0] = 0;
+        for (int blk = 0; blk < nblk; ++blk) {
+            long long nc, wf, wl;
+            noalloc_block_counts(blk, N, W, stride, rpb, &nc, &wf, &wl);
+            pos += (int)(nc + (wl - wf + 1));
+            list[blk + 1] = pos;
+        }
+    }
+    __syncthreads();
+    for (int blk = threadIdx.x; blk < nblk; blk += blockDim.x) {
+        long long nc, wf, wl;
+        noalloc_block_counts(blk, N, W, stride, rpb, &nc, &wf, &wl);
+        int* e = list + nblk + 1 + list[blk];
+        for (long long c = 0; c < nc; ++c)
+            *e++ = (swa::TILE_KIND_STRIDED << swa::TILE_KIND_SHIFT) | (int)c;
+        for (long long t = wf; t <= wl; ++t)
+            *e++ = (swa::TILE_KIND_WINDOW << swa::TILE_KIND_SHIFT) | (int)t;
+    }
+}
+
 }  // namespace
 
 extern "C" {
@@ -206,6 +267,7 @@ const char* swa_status_string(int status) {
         case SWA_ERR_CUDA: return "CUDA runtime or driver error";
         case SWA_ERR_TIMEOUT: return "kernel watchdog: a bounded wait ran out";
         case SWA_ERR_VALUE: return "invalid scalar argument (scale must be finite and > 0; lambda finite)";
+        case SWA_ERR_TOO_LARGE: return "problem too large for the fixed tile-list capacity of the allocation-free call";
         default: return "unknown status";
     }
 }
@@ -264,6 +326,60 @@ int strided_attn_fwd(const void* q, const void* k, const void* v, void* out, int
         return rc;
     return dispatch<swa::MODE_STRIDED>(d, kp, n_items_for(kp), static_cast<cudaStream_t>(stream),
                                        *st);
+}
+
+int strided_attn_fwd_noalloc(const void* q, const void* k, const void* v, void* out, int B,
+                             int Hq, int Hkv, int N, int d, int W, int stride, float scale,
+                             void* stream) {
+    if (!q || !k || !v || !out) return SWA_ERR_NULL;
+    if (W < 1 || stride < 1) return SWA_ERR_SHAPE;
+    int rc = check_common(B, Hq, Hkv, N, d, scale);
+    if (rc) return rc;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return SWA_ERR_ALIGN;
+    const int Wc = std::min(W, N);
+    const int sc = std::min(stride, N);
+    const int pair_mode = ((Hq / Hkv) % 2 == 0) ? 1 : 0;
+    const int rpb = pair_mode ? BM : 2 * BM;
+    if (noalloc_list_length(N, Wc, sc, rpb) > SWA_NOALLOC_TILE_CAPACITY) return SWA_ERR_TOO_LARGE;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceState* st = nullptr;
+    if ((rc = current_device_state(&st))) return rc;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SWA_ERR_CUDA;
+    NoAllocState& na = g_noalloc[dev];
+    if (!na.ready) {  // once per device, with that device current
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_noalloc_tiles) != cudaSuccess || ptr == nullptr)
+            return SWA_ERR_CUDA;
+        na.tiles = static_cast<int*>(ptr);
+        na.ready = true;
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(1, 1, 1);
+        cfg.blockDim = dim3(256, 1, 1);
+        cfg.stream = s;
+        if (cudaLaunchKernelEx(&cfg, noalloc_build_tiles_kernel, na.tiles, N, Wc, sc, rpb) !=
+            cudaSuccess)
+            return SWA_ERR_CUDA;
+    }
+    KParams kp;
+    std::memset(&kp, 0, sizeof(kp));
+    fill_common(kp, B, Hq, Hkv, N, Wc, sc, scale, out, *st);
+    kp.pair_mode = pair_mode;
+    kp.tiles = na.tiles;
+    const long long ns = (N - 1) / sc + 1;
+    if ((rc = make_map(&kp.tm_q, q, d, N, d, (long long)B * Hq, (long long)N * d))) return rc;
+    if ((rc = make_map(&kp.tm_k, k, d, N, d, (long long)B * Hkv, (long long)N * d))) return rc;
+    if ((rc = make_map(&kp.tm_v, v, d, N, d, (long long)B * Hkv, (long long)N * d))) return rc;
+    if ((rc = make_map(&kp.tm_k2, k, d, ns, (long long)sc * d, (long long)B * Hkv,
+                       (long long)N * d)))
+        return rc;
+    if ((rc = make_map(&kp.tm_v2, v, d, ns, (long long)sc * d, (long long)B * Hkv,
+                       (long long)N * d)))
+        return rc;
+    return dispatch<swa::MODE_STRIDED>(d, kp, n_items_for(kp), s, *st);
 }
 
 int diff_attn_fwd(const void* q1, const void* k1, const void* q2, const void* k2, const void* v,

@@ -33,7 +33,7 @@ def test_library_exports_every_declared_symbol():
 
 
 def test_status_strings():
-    for code in range(0, 8):
+    for code in range(0, 9):
         s = pkg.swa_status_string(code)
         assert s and s != "unknown status"
     assert pkg.swa_status_string(99) == "unknown status"
@@ -83,6 +83,15 @@ def test_diff_validation(L):
     assert f(P, P, P, P, P, float("inf"), P, 1, 2, 2, 128, 64, 0.125, None) == 7
     assert f(P, P, P, P, P, 0.8, P, 1, 2, 4, 128, 64, 0.125, None) == 2
     assert f(P, P, P, P, P + 8, 0.8, P, 1, 2, 2, 128, 64, 0.125, None) == 3
+
+
+def test_noalloc_validation(L):
+    f = L.strided_attn_fwd_noalloc
+    assert f(None, P, P, P, 1, 2, 2, 128, 64, 16, 4, 0.125, None) == 1
+    assert f(P, P, P, P, 1, 2, 2, 128, 64, 16, 0, 0.125, None) == 2
+    assert f(P, P, P, P + 4, 1, 2, 2, 128, 64, 16, 4, 0.125, None) == 3
+    # a list longer than the fixed capacity is refused on the host, before any launch
+    assert f(P, P, P, P, 1, 1, 1, 1 << 22, 64, 256, 1, 0.125, None) == 8
 
 
 def test_watchdog_selftest_validation(L):
