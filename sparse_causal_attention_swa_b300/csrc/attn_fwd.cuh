@@ -239,9 +239,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd_kernel(const __grid_c
         // ===================================== TMA producer
         if (lane == 0) {
             constexpr int NCH = D / 64;  // 64-column (128-byte) chunks per row
-            uint32_t last_par[L::STAGES];
-            bool used[L::STAGES];
-            for (int s = 0; s < L::STAGES; ++s) used[s] = false;
+            uint32_t used_mask = 0, par_mask = 0;  // per stage: filled at least once / parity
             // Q tiles of both slots
             mbar_arrive_expect_tx(bar(L::BAR_Q), 2 * L::QBYTES);
             for (int s = 0; s < 2; ++s) {
@@ -260,8 +258,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd_kernel(const __grid_c
                 const uint32_t dst = sbase + L::OFF_RING + st * L::EBYTES;
                 for (int c = 0; c < NCH; ++c)
                     tma_load_3d(dst + c * (BN * 128), m, bar(L::BAR_FULL + st), c * 64, row, kmat);
-                used[st] = true;
-                last_par[st] = ph;
+                used_mask |= 1u << st;
+                par_mask = (par_mask & ~(1u << st)) | (ph << st);
                 if (++st == (uint32_t)L::STAGES) {
                     st = 0;
                     ph ^= 1u;
@@ -284,7 +282,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd_kernel(const __grid_c
                 volatile int never = 0;
                 (void)mbar_wait_bounded(bar(L::BAR_Q), 0, &never, lim);
                 for (int s = 0; s < L::STAGES; ++s)
-                    if (used[s]) (void)mbar_wait_bounded(bar(L::BAR_FULL + s), last_par[s], &never, lim);
+                    if (used_mask & (1u << s))
+                        (void)mbar_wait_bounded(bar(L::BAR_FULL + s), (par_mask >> s) & 1u, &never,
+                                                lim);
             }
         }
         __syncwarp();
@@ -393,16 +393,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd_kernel(const __grid_c
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             tc_fence_after();
-            float x[BN];
-            {
-                uint32_t r[32];
-#pragma unroll
-                for (int c = 0; c < BN / 32; ++c) {
-                    tmem_ld32(tS + c * 32, r);
-#pragma unroll
-                    for (int t = 0; t < 32; ++t) x[c * 32 + t] = __uint_as_float(r[t]);
-                }
-            }
+            // the whole 128-key score row of this thread, one TMEM load
+            uint32_t xr[BN];
+            tmem_ld128(tS, xr);
             // allowed columns of this row in this tile: [a, bnd]
             int kind, idx;
             tile_at(jj, kind, idx);
@@ -417,11 +410,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd_kernel(const __grid_c
             }
             if (a > 0 || bnd < BN - 1) {
 #pragma unroll
-                for (int t = 0; t < BN; ++t) x[t] = (t >= a && t <= bnd) ? x[t] : -INFINITY;
+                for (int t = 0; t < BN; ++t)
+                    xr[t] = (t >= a && t <= bnd) ? xr[t] : __float_as_uint(-INFINITY);
             }
-            float mt = x[0];
+            // row maximum: eight independent 3-input max chains, then a short tree
+            float mc[8];
 #pragma unroll
-            for (int t = 1; t < BN; ++t) mt = fmaxf(mt, x[t]);
+            for (int c = 0; c < 8; ++c) {
+                float v = __uint_as_float(xr[c * 16]);
+#pragma unroll
+                for (int u = 1; u < 15; u += 2)
+                    v = fmax3(v, __uint_as_float(xr[c * 16 + u]), __uint_as_float(xr[c * 16 + u + 1]));
+                mc[c] = fmaxf(v, __uint_as_float(xr[c * 16 + 15]));
+            }
+            const float mt = fmax3(fmax3(mc[0], mc[1], mc[2]), fmax3(mc[3], mc[4], mc[5]),
+                                   fmaxf(mc[6], mc[7]));
             const float m_new = fmaxf(m, mt);
             const bool need = (m_new - m) * sl2 > RESCALE_THRESHOLD;
             const bool rescale = __any_sync(0xffffffffu, need);
@@ -432,21 +435,37 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd_kernel(const __grid_c
                 m = m_new;
             }
             const float ms = (m == -INFINITY) ? 0.f : m * sl2;
-            // P = exp2(x * scale * log2 e - m * scale * log2 e), packed bf16 pairs into TMEM
-            float rs = 0.f;
+            // P = exp2(x * scale * log2 e - m * scale * log2 e): the argument two lanes at a
+            // time (packed fma), four packed partial row sums, bf16 pairs stored to TMEM in
+            // 32-column chunks as soon as they are ready
+            const uint64_t sl2x2 = f32x2_pack(sl2, sl2);
+            const uint64_t nmsx2 = f32x2_pack(-ms, -ms);
+            uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
 #pragma unroll
             for (int c = 0; c < BN / 64; ++c) {
                 uint32_t pk[32];
 #pragma unroll
                 for (int t = 0; t < 32; ++t) {
-                    const float p0 = fast_exp2(fmaf(x[c * 64 + 2 * t], sl2, -ms));
-                    const float p1 = fast_exp2(fmaf(x[c * 64 + 2 * t + 1], sl2, -ms));
-                    rs += p0 + p1;
+                    const int e = c * 64 + 2 * t;
+                    const uint64_t z = f32x2_fma(
+                        f32x2_pack(__uint_as_float(xr[e]), __uint_as_float(xr[e + 1])), sl2x2,
+                        nmsx2);
+                    float z0, z1;
+                    f32x2_unpack(z, z0, z1);
+                    const float p0 = fast_exp2(z0);
+                    const float p1 = fast_exp2(z1);
+                    acc[t & 3] = f32x2_add(acc[t & 3], f32x2_pack(p0, p1));
                     pk[t] = pack_bf16x2(p0, p1);
                 }
                 tmem_st32(tS + c * 32, pk);
             }
-            l += rs;
+            {
+                const uint64_t s01 = f32x2_add(acc[0], acc[1]);
+                const uint64_t s23 = f32x2_add(acc[2], acc[3]);
+                float u0, u1;
+                f32x2_unpack(f32x2_add(s01, s23), u0, u1);
+                l += u0 + u1;
+            }
             // O is complete up to tile jj-1 here (its PV was issued before this tile's S)
             if (rescale && jj > 0) {
                 uint32_t r[32];
