@@ -14,8 +14,15 @@
 //   warps 0-3  softmax warpgroup of slot 0   (thread t owns query row t of the slot)
 //   warps 4-7  softmax warpgroup of slot 1
 //   warp 8     TMA producer (lane 0): Q tiles once, then K / V tiles into an smem ring
-//   warp 9     TMEM owner + MMA issuer (lane 0): S = Q K^T and O += P V on tcgen05
-//   warps 10-11 idle
+//   warp 9     TMEM owner; lane 0 issues slot 0's MMAs: S = Q K^T and O += P V on tcgen05
+//   warp 10    lane 0 issues slot 1's MMAs
+//   warp 11    idle
+// Each slot has its own issuing thread: tcgen05.mma issue blocks on a shallow queue, so a
+// single issuer cannot run ahead, and its barrier bookkeeping would idle the tensor core;
+// with two issuers one thread's bookkeeping overlaps the other's MMA stream.  The two
+// issuers still take turns (slot 0's batch of tile j, then slot 1's, then slot 0's of j+1,
+// through the two "turn" barriers), so the tensor core alternates between the slots and
+// each slot's softmax overlaps the other slot's MMAs.
 // A "slot" is 128 query rows.  The two slots of a work item are either two query heads of
 // one GQA group on the same rows, the two score streams of the differential variant, or
 // two consecutive 128-row tiles of one head; they walk the same KV tile sequence in lock
@@ -26,9 +33,9 @@
 //   [128,256) S of slot 1   (P of slot 1 in [128,192))
 //   [256,256+D) O of slot 0,  [384,384+D) O of slot 1
 //
-// Per KV tile and slot, the MMA thread issues, in order, PV_s(j) then S_s(j+1); tcgen05
-// MMAs of one thread execute in issue order, so S_s(j+1) cannot overwrite P_s(j) before
-// PV_s(j) has read it, and the commit after S_s(j+1) also covers PV_s(j).
+// Per KV tile, slot s's MMA thread issues, in order, PV_s(j) then S_s(j+1); tcgen05 MMAs of
+// one thread execute in issue order, so S_s(j+1) cannot overwrite P_s(j) before PV_s(j) has
+// read it, and the commit after S_s(j+1) also covers PV_s(j).
 //
 // Online softmax in base 2: x = s * scale * log2(e).  The running row maximum m is only
 // moved (and O, l rescaled) when the new tile's maximum exceeds it by more than 8 in the
@@ -46,7 +53,8 @@ constexpr int BM = 128;  // query rows per slot
 constexpr int BN = 128;  // keys per KV tile
 constexpr int NUM_THREADS = 384;
 constexpr int PRODUCER_WARP = 8;
-constexpr int MMA_WARP = 9;
+constexpr int MMA_WARP = 9;       // TMEM owner; issues the MMAs of slot 0
+constexpr int MMA_WARP_1 = 10;    // issues the MMAs of slot 1
 constexpr uint32_t TMEM_COLS = 512;
 constexpr float RESCALE_THRESHOLD = 8.0f;  // log2 units
 
@@ -92,8 +100,9 @@ struct SmemLayout {
     static constexpr int BAR_P = BAR_S + 2;
     static constexpr int BAR_O = BAR_P + 2;
     static constexpr int BAR_L = BAR_O + 2;
-    static constexpr int BAR_DRAIN = BAR_L + 1;
-    static constexpr int NBARS = BAR_DRAIN + 1;
+    static constexpr int BAR_DRAIN = BAR_L + 1;  // two: one per MMA issuer
+    static constexpr int BAR_TURN = BAR_DRAIN + 2;  // two: "slot s may issue its next batch"
+    static constexpr int NBARS = BAR_TURN + 2;
     static constexpr int OFF_TMEM = OFF_BAR + NBARS * 8;
     static constexpr int OFF_ABORT = OFF_TMEM + 4;
     static constexpr int OFF_LSM = (OFF_ABORT + 4 + 15) / 16 * 16;
@@ -209,7 +218,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd_kernel(const __grid_c
         mbar_init(bar(L::BAR_Q), 1);
         for (int s = 0; s < L::STAGES; ++s) {
             mbar_init(bar(L::BAR_FULL + s), 1);
-            mbar_init(bar(L::BAR_EMPTY + s), 1);
+            mbar_init(bar(L::BAR_EMPTY + s), 2);  // released by both MMA issuers
         }
         for (int s = 0; s < 2; ++s) {
             mbar_init(bar(L::BAR_S + s), 1);
@@ -218,6 +227,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd_kernel(const __grid_c
         }
         mbar_init(bar(L::BAR_L), 128);
         mbar_init(bar(L::BAR_DRAIN), 1);
+        mbar_init(bar(L::BAR_DRAIN + 1), 1);
+        mbar_init(bar(L::BAR_TURN), 1);
+        mbar_init(bar(L::BAR_TURN + 1), 1);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -288,32 +300,36 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd_kernel(const __grid_c
             }
         }
         __syncwarp();
-    } else if (warp == MMA_WARP) {
-        // ===================================== MMA issuer
+    } else if (warp == MMA_WARP || warp == MMA_WARP_1) {
+        // ===================================== MMA issuers (one thread per slot)
         if (lane == 0) {
+            const int s = (warp == MMA_WARP) ? 0 : 1;
             constexpr uint32_t ID_S = idesc_bf16_f32(BM, BN, 0);
             constexpr uint32_t ID_O = idesc_bf16_f32(BM, D, 1);
             const uint32_t ring0 = sbase + L::OFF_RING;
-            const uint32_t tS[2] = {tmem_base + 0u, tmem_base + 128u};
-            const uint32_t tO[2] = {tmem_base + 256u, tmem_base + 384u};
-            auto issue_S = [&](int s, int entry) {
-                const uint32_t qa = sbase + L::OFF_Q + s * L::QBYTES;
-                const uint32_t ka = ring0 + entry * L::EBYTES;
+            // Descriptors are built once; the 14-bit start-address field holds address >> 4
+            // in the low bits, so moving to another K step, chunk or ring entry is an add of
+            // (byte offset >> 4) that cannot carry (shared memory addresses are < 2^18).
+            const uint64_t aq = smem_desc_sw128(sbase + L::OFF_Q + s * L::QBYTES, 16, 1024);
+            const uint64_t dk0 = smem_desc_sw128(ring0, 16, 1024);
+            const uint64_t dv0 = smem_desc_sw128(ring0, BN * 128, 1024);
+            const uint32_t tS = tmem_base + 128u * (uint32_t)s;
+            const uint32_t tO = tmem_base + 256u + 128u * (uint32_t)s;
+            auto issue_S = [&](int entry) {
+                const uint64_t bk = dk0 + (uint64_t)(entry * (L::EBYTES >> 4));
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k) {
-                    const uint32_t off = (k >> 2) * (BM * 128) + (k & 3) * 32;
-                    const uint32_t koff = (k >> 2) * (BN * 128) + (k & 3) * 32;
-                    mma_ss(tS[s], smem_desc_sw128(qa + off, 16, 1024),
-                           smem_desc_sw128(ka + koff, 16, 1024), ID_S, k > 0 ? 1u : 0u);
+                    const uint32_t offq = ((k >> 2) * (BM * 128) + (k & 3) * 32) >> 4;
+                    const uint32_t offk = ((k >> 2) * (BN * 128) + (k & 3) * 32) >> 4;
+                    mma_ss(tS, aq + offq, bk + offk, ID_S, k > 0 ? 1u : 0u);
                 }
             };
-            auto issue_PV = [&](int s, int entry, bool acc) {
-                const uint32_t va = ring0 + entry * L::EBYTES;
+            auto issue_PV = [&](int entry, bool acc) {
+                const uint64_t bv = dv0 + (uint64_t)(entry * (L::EBYTES >> 4));
 #pragma unroll
-                for (int k = 0; k < BN / 16; ++k) {
-                    mma_ts(tO[s], tS[s] + k * 8, smem_desc_sw128(va + k * 2048, BN * 128, 1024),
-                           ID_O, (acc || k > 0) ? 1u : 0u);
-                }
+                for (int k = 0; k < BN / 16; ++k)
+                    mma_ts(tO, tS + (uint32_t)(k * 8), bv + (uint64_t)((k * 2048) >> 4), ID_O,
+                           (acc || k > 0) ? 1u : 0u);
             };
             uint32_t st = 0, ph = 0;
             bool ok = true;
@@ -326,19 +342,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd_kernel(const __grid_c
                 }
                 return true;
             };
+            // Both issuers pop every ring entry (in the producer's order) and release every
+            // entry they popped, so each empty barrier gets its two arrivals; an entry this
+            // slot does not read (the other stream's K in the differential call) is released
+            // after this thread's earlier MMAs, which is merely conservative.
             int kA = 0, kB = 0;
             ok = mbar_wait_bounded(bar(L::BAR_Q), 0, abort_flag, lim);
             if (ok) ok = pop(kA);
             if (ok && MODE == MODE_DIFF) ok = pop(kB);
+            // turn order: slot 1 issues a batch only after slot 0 has issued its batch of the
+            // same step, and slot 0 only after slot 1 has issued its previous one.  Slot 0
+            // can therefore never be two batches ahead, so the turn phases cannot alias.
+            // Turn barrier t[1] completes once per slot-0 batch, t[0] once per slot-1 batch.
+            if (ok && s == 1) ok = mbar_wait_bounded(bar(L::BAR_TURN + 1), 0u, abort_flag, lim);
             if (ok) {
-                if (MODE != MODE_DIFF) kB = kA;
                 tc_fence_after();
-                issue_S(0, kA);
-                mma_commit(bar(L::BAR_S + 0));
-                issue_S(1, kB);
-                mma_commit(bar(L::BAR_S + 1));
+                issue_S((MODE == MODE_DIFF && s == 1) ? kB : kA);
+                mma_commit(bar(L::BAR_S + s));
                 mma_commit(bar(L::BAR_EMPTY + kA));
                 if (MODE == MODE_DIFF) mma_commit(bar(L::BAR_EMPTY + kB));
+                mbar_arrive(bar(L::BAR_TURN + (s ^ 1)));
             }
             for (int jj = 0; jj < n_tiles && ok; ++jj) {
                 int ve = 0, nA = 0, nB = 0;
@@ -347,31 +370,32 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd_kernel(const __grid_c
                 if (ok && more) {
                     ok = pop(nA);
                     if (ok && MODE == MODE_DIFF) ok = pop(nB);
-                    if (MODE != MODE_DIFF) nB = nA;
                 }
-                for (int s = 0; s < 2 && ok; ++s) {
-                    ok = mbar_wait_bounded(bar(L::BAR_P + s), (uint32_t)jj & 1u, abort_flag, lim);
-                    if (!ok) break;
-                    tc_fence_after();
-                    issue_PV(s, ve, jj > 0);
-                    if (more) {
-                        issue_S(s, s == 0 ? nA : nB);
-                        mma_commit(bar(L::BAR_S + s));
-                    } else {
-                        mma_commit(bar(L::BAR_O + s));
-                    }
-                }
+                if (ok) ok = mbar_wait_bounded(bar(L::BAR_P + s), (uint32_t)jj & 1u, abort_flag, lim);
+                // slot 0's batch jj follows slot 1's batch jj-1 (phase jj of t[0]); slot 1's
+                // batch jj follows slot 0's batch jj (phase jj+1 of t[1])
+                if (ok) ok = mbar_wait_bounded(bar(L::BAR_TURN + s), (uint32_t)(jj + s) & 1u,
+                                               abort_flag, lim);
                 if (!ok) break;
+                tc_fence_after();
+                issue_PV(ve, jj > 0);
+                if (more) {
+                    issue_S((MODE == MODE_DIFF && s == 1) ? nB : nA);
+                    mma_commit(bar(L::BAR_S + s));
+                } else {
+                    mma_commit(bar(L::BAR_O + s));
+                }
+                mbar_arrive(bar(L::BAR_TURN + (s ^ 1)));
                 mma_commit(bar(L::BAR_EMPTY + ve));
                 if (more) {
                     mma_commit(bar(L::BAR_EMPTY + nA));
                     if (MODE == MODE_DIFF) mma_commit(bar(L::BAR_EMPTY + nB));
                 }
             }
-            // drain: all issued MMAs must complete before TMEM is released
-            mma_commit(bar(L::BAR_DRAIN));
+            // drain: all MMAs this thread issued must complete before TMEM is released
+            mma_commit(bar(L::BAR_DRAIN + s));
             volatile int never = 0;
-            (void)mbar_wait_bounded(bar(L::BAR_DRAIN), 0, &never, lim);
+            (void)mbar_wait_bounded(bar(L::BAR_DRAIN + s), 0, &never, lim);
         }
         __syncwarp();
     } else if (warp < 8) {
