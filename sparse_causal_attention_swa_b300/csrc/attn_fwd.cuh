@@ -14,15 +14,20 @@
 //   warps 0-3  softmax warpgroup of slot 0   (thread t owns query row t of the slot)
 //   warps 4-7  softmax warpgroup of slot 1
 //   warp 8     TMA producer (lane 0): Q tiles once, then K / V tiles into an smem ring
-//   warp 9     TMEM owner; lane 0 issues slot 0's MMAs: S = Q K^T and O += P V on tcgen05
-//   warp 10    lane 0 issues slot 1's MMAs
+//   warp 9     TMEM owner; issues slot 0's MMAs: S = Q K^T and O += P V on tcgen05
+//   warp 10    issues slot 1's MMAs
 //   warp 11    idle
-// Each slot has its own issuing thread: tcgen05.mma issue blocks on a shallow queue, so a
+// Each slot has its own issuing warp: tcgen05.mma issue blocks on a shallow queue, so a
 // single issuer cannot run ahead, and its barrier bookkeeping would idle the tensor core;
-// with two issuers one thread's bookkeeping overlaps the other's MMA stream.  The two
-// issuers still take turns (slot 0's batch of tile j, then slot 1's, then slot 0's of j+1,
-// through the two "turn" barriers), so the tensor core alternates between the slots and
-// each slot's softmax overlaps the other slot's MMAs.
+// with two issuers one warp's bookkeeping overlaps the other's MMA stream.  The issuing
+// warps stay converged and one elected lane performs each tcgen05 operation, which keeps
+// the operands warp-uniform and makes each MMA issue about as fast as the tensor core
+// executes a 128x128x16 step.  The two issuers still take turns (slot 0's batch of tile j,
+// then slot 1's, then slot 0's of j+1, through the two "turn" barriers), so the tensor
+// core alternates between the slots and each slot's softmax overlaps the other slot's
+// MMAs; letting the issuers overlap instead drives the slots into lock step.
+// setmaxnreg moves registers from the TMA / MMA warpgroup (56 per thread) to the softmax
+// warpgroups (224), which hold a whole 128-key score row per thread.
 // A "slot" is 128 query rows.  The two slots of a work item are either two query heads of
 // one GQA group on the same rows, the two score streams of the differential variant, or
 // two consecutive 128-row tiles of one head; they walk the same KV tile sequence in lock
@@ -247,8 +252,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd_kernel(const __grid_c
     const uint32_t tmem_base = *tmem_slot;
     const uint64_t lim = p.wait_limit_ns;
 
+    // Registers: the softmax warpgroups hold a 128-key score row per thread; the TMA / MMA
+    // warpgroup needs few.  Launch budget 384 x 168 = 256 x 224 + 128 x 56.
     if (warp == PRODUCER_WARP) {
         // ===================================== TMA producer
+        setmaxnreg_dec<56>();
         if (lane == 0) {
             constexpr int NCH = D / 64;  // 64-column (128-byte) chunks per row
             uint32_t used_mask = 0, par_mask = 0;  // per stage: filled at least once / parity
@@ -301,105 +309,112 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd_kernel(const __grid_c
         }
         __syncwarp();
     } else if (warp == MMA_WARP || warp == MMA_WARP_1) {
-        // ===================================== MMA issuers (one thread per slot)
-        if (lane == 0) {
-            const int s = (warp == MMA_WARP) ? 0 : 1;
-            constexpr uint32_t ID_S = idesc_bf16_f32(BM, BN, 0);
-            constexpr uint32_t ID_O = idesc_bf16_f32(BM, D, 1);
-            const uint32_t ring0 = sbase + L::OFF_RING;
-            // Descriptors are built once; the 14-bit start-address field holds address >> 4
-            // in the low bits, so moving to another K step, chunk or ring entry is an add of
-            // (byte offset >> 4) that cannot carry (shared memory addresses are < 2^18).
-            const uint64_t aq = smem_desc_sw128(sbase + L::OFF_Q + s * L::QBYTES, 16, 1024);
-            const uint64_t dk0 = smem_desc_sw128(ring0, 16, 1024);
-            const uint64_t dv0 = smem_desc_sw128(ring0, BN * 128, 1024);
-            const uint32_t tS = tmem_base + 128u * (uint32_t)s;
-            const uint32_t tO = tmem_base + 256u + 128u * (uint32_t)s;
-            auto issue_S = [&](int entry) {
-                const uint64_t bk = dk0 + (uint64_t)(entry * (L::EBYTES >> 4));
+        // ===================================== MMA issuers (one converged warp per slot)
+        setmaxnreg_dec<56>();
+        // All 32 lanes run the loop and wait on the barriers; each tcgen05 operation is
+        // performed by one elected lane (the *_elect forms).
+        const int s = (warp == MMA_WARP) ? 0 : 1;
+        constexpr uint32_t ID_S = idesc_bf16_f32(BM, BN, 0);
+        constexpr uint32_t ID_O = idesc_bf16_f32(BM, D, 1);
+        const uint32_t ring0 = sbase + L::OFF_RING;
+        // Descriptors are built once; the 14-bit start-address field holds address >> 4
+        // in the low bits, so moving to another K step, chunk or ring entry is an add of
+        // (byte offset >> 4) that cannot carry (shared memory addresses are < 2^18).
+        const uint64_t aq = smem_desc_sw128(sbase + L::OFF_Q + s * L::QBYTES, 16, 1024);
+        const uint64_t dk0 = smem_desc_sw128(ring0, 16, 1024);
+        const uint64_t dv0 = smem_desc_sw128(ring0, BN * 128, 1024);
+        const uint32_t tS = tmem_base + 128u * (uint32_t)s;
+        const uint32_t tO = tmem_base + 256u + 128u * (uint32_t)s;
+        auto issue_S = [&](int entry) {
+            const uint64_t bk = dk0 + (uint64_t)(entry * (L::EBYTES >> 4));
 #pragma unroll
-                for (int k = 0; k < D / 16; ++k) {
-                    const uint32_t offq = ((k >> 2) * (BM * 128) + (k & 3) * 32) >> 4;
-                    const uint32_t offk = ((k >> 2) * (BN * 128) + (k & 3) * 32) >> 4;
-                    mma_ss(tS, aq + offq, bk + offk, ID_S, k > 0 ? 1u : 0u);
-                }
-            };
-            auto issue_PV = [&](int entry, bool acc) {
-                const uint64_t bv = dv0 + (uint64_t)(entry * (L::EBYTES >> 4));
+            for (int k = 0; k < D / 16; ++k) {
+                const uint32_t offq = ((k >> 2) * (BM * 128) + (k & 3) * 32) >> 4;
+                const uint32_t offk = ((k >> 2) * (BN * 128) + (k & 3) * 32) >> 4;
+                mma_ss_elect(tS, aq + offq, bk + offk, ID_S, k > 0 ? 1u : 0u);
+            }
+        };
+        auto issue_PV = [&](int entry, bool acc) {
+            const uint64_t bv = dv0 + (uint64_t)(entry * (L::EBYTES >> 4));
 #pragma unroll
-                for (int k = 0; k < BN / 16; ++k)
-                    mma_ts(tO, tS + (uint32_t)(k * 8), bv + (uint64_t)((k * 2048) >> 4), ID_O,
-                           (acc || k > 0) ? 1u : 0u);
-            };
-            uint32_t st = 0, ph = 0;
-            bool ok = true;
-            auto pop = [&](int& e) -> bool {
-                if (!mbar_wait_bounded(bar(L::BAR_FULL + st), ph, abort_flag, lim)) return false;
-                e = (int)st;
-                if (++st == (uint32_t)L::STAGES) {
-                    st = 0;
-                    ph ^= 1u;
-                }
-                return true;
-            };
-            // Both issuers pop every ring entry (in the producer's order) and release every
-            // entry they popped, so each empty barrier gets its two arrivals; an entry this
-            // slot does not read (the other stream's K in the differential call) is released
-            // after this thread's earlier MMAs, which is merely conservative.
-            int kA = 0, kB = 0;
-            ok = mbar_wait_bounded(bar(L::BAR_Q), 0, abort_flag, lim);
-            if (ok) ok = pop(kA);
-            if (ok && MODE == MODE_DIFF) ok = pop(kB);
-            // turn order: slot 1 issues a batch only after slot 0 has issued its batch of the
-            // same step, and slot 0 only after slot 1 has issued its previous one.  Slot 0
-            // can therefore never be two batches ahead, so the turn phases cannot alias.
-            // Turn barrier t[1] completes once per slot-0 batch, t[0] once per slot-1 batch.
-            if (ok && s == 1) ok = mbar_wait_bounded(bar(L::BAR_TURN + 1), 0u, abort_flag, lim);
-            if (ok) {
-                tc_fence_after();
-                issue_S((MODE == MODE_DIFF && s == 1) ? kB : kA);
-                mma_commit(bar(L::BAR_S + s));
-                mma_commit(bar(L::BAR_EMPTY + kA));
-                if (MODE == MODE_DIFF) mma_commit(bar(L::BAR_EMPTY + kB));
-                mbar_arrive(bar(L::BAR_TURN + (s ^ 1)));
+            for (int k = 0; k < BN / 16; ++k)
+                mma_ts_elect(tO, tS + (uint32_t)(k * 8), bv + (uint64_t)((k * 2048) >> 4), ID_O,
+                             (acc || k > 0) ? 1u : 0u);
+        };
+        // a bounded wait whose outcome every lane agrees on
+        auto wait = [&](uint32_t b, uint32_t parity) -> bool {
+            const bool r = mbar_wait_bounded(b, parity, abort_flag, lim);
+            return __all_sync(0xffffffffu, r);
+        };
+        uint32_t st = 0, ph = 0;
+        bool ok = true;
+        auto pop = [&](int& e) -> bool {
+            if (!wait(bar(L::BAR_FULL + st), ph)) return false;
+            e = (int)st;
+            if (++st == (uint32_t)L::STAGES) {
+                st = 0;
+                ph ^= 1u;
             }
-            for (int jj = 0; jj < n_tiles && ok; ++jj) {
-                int ve = 0, nA = 0, nB = 0;
-                const bool more = jj + 1 < n_tiles;
-                ok = pop(ve);
-                if (ok && more) {
-                    ok = pop(nA);
-                    if (ok && MODE == MODE_DIFF) ok = pop(nB);
-                }
-                if (ok) ok = mbar_wait_bounded(bar(L::BAR_P + s), (uint32_t)jj & 1u, abort_flag, lim);
-                // slot 0's batch jj follows slot 1's batch jj-1 (phase jj of t[0]); slot 1's
-                // batch jj follows slot 0's batch jj (phase jj+1 of t[1])
-                if (ok) ok = mbar_wait_bounded(bar(L::BAR_TURN + s), (uint32_t)(jj + s) & 1u,
-                                               abort_flag, lim);
-                if (!ok) break;
-                tc_fence_after();
-                issue_PV(ve, jj > 0);
-                if (more) {
-                    issue_S((MODE == MODE_DIFF && s == 1) ? nB : nA);
-                    mma_commit(bar(L::BAR_S + s));
-                } else {
-                    mma_commit(bar(L::BAR_O + s));
-                }
-                mbar_arrive(bar(L::BAR_TURN + (s ^ 1)));
-                mma_commit(bar(L::BAR_EMPTY + ve));
-                if (more) {
-                    mma_commit(bar(L::BAR_EMPTY + nA));
-                    if (MODE == MODE_DIFF) mma_commit(bar(L::BAR_EMPTY + nB));
-                }
-            }
-            // drain: all MMAs this thread issued must complete before TMEM is released
-            mma_commit(bar(L::BAR_DRAIN + s));
-            volatile int never = 0;
-            (void)mbar_wait_bounded(bar(L::BAR_DRAIN + s), 0, &never, lim);
+            return true;
+        };
+        // Both issuers pop every ring entry (in the producer's order) and release every
+        // entry they popped, so each empty barrier gets its two arrivals; an entry this
+        // slot does not read (the other stream's K in the differential call) is released
+        // after this warp's earlier MMAs, which is merely conservative.
+        int kA = 0, kB = 0;
+        ok = wait(bar(L::BAR_Q), 0);
+        if (ok) ok = pop(kA);
+        if (ok && MODE == MODE_DIFF) ok = pop(kB);
+        // turn order: slot 1 issues a batch only after slot 0 has issued its batch of the
+        // same step, and slot 0 only after slot 1 has issued its previous one.  Slot 0
+        // can therefore never be two batches ahead, so the turn phases cannot alias.
+        // Turn barrier t[1] completes once per slot-0 batch, t[0] once per slot-1 batch.
+        if (ok && s == 1) ok = wait(bar(L::BAR_TURN + 1), 0u);
+        if (ok) {
+            tc_fence_after();
+            issue_S((MODE == MODE_DIFF && s == 1) ? kB : kA);
+            mma_commit_elect(bar(L::BAR_S + s));
+            mma_commit_elect(bar(L::BAR_EMPTY + kA));
+            if (MODE == MODE_DIFF) mma_commit_elect(bar(L::BAR_EMPTY + kB));
+            mbar_arrive_elect(bar(L::BAR_TURN + (s ^ 1)));
         }
+        for (int jj = 0; jj < n_tiles && ok; ++jj) {
+            int ve = 0, nA = 0, nB = 0;
+            const bool more = jj + 1 < n_tiles;
+            ok = pop(ve);
+            if (ok && more) {
+                ok = pop(nA);
+                if (ok && MODE == MODE_DIFF) ok = pop(nB);
+            }
+            if (ok) ok = wait(bar(L::BAR_P + s), (uint32_t)jj & 1u);
+            // slot 0's batch jj follows slot 1's batch jj-1 (phase jj of t[0]); slot 1's
+            // batch jj follows slot 0's batch jj (phase jj+1 of t[1])
+            if (ok) ok = wait(bar(L::BAR_TURN + s), (uint32_t)(jj + s) & 1u);
+            if (!ok) break;
+            tc_fence_after();
+            issue_PV(ve, jj > 0);
+            if (more) {
+                issue_S((MODE == MODE_DIFF && s == 1) ? nB : nA);
+                mma_commit_elect(bar(L::BAR_S + s));
+            } else {
+                mma_commit_elect(bar(L::BAR_O + s));
+            }
+            mbar_arrive_elect(bar(L::BAR_TURN + (s ^ 1)));
+            mma_commit_elect(bar(L::BAR_EMPTY + ve));
+            if (more) {
+                mma_commit_elect(bar(L::BAR_EMPTY + nA));
+                if (MODE == MODE_DIFF) mma_commit_elect(bar(L::BAR_EMPTY + nB));
+            }
+        }
+        // drain: all MMAs this warp issued must complete before TMEM is released
+        __syncwarp();
+        mma_commit_elect(bar(L::BAR_DRAIN + s));
+        volatile int never = 0;
+        (void)mbar_wait_bounded(bar(L::BAR_DRAIN + s), 0, &never, lim);
         __syncwarp();
     } else if (warp < 8) {
         // ===================================== softmax warpgroups
+        setmaxnreg_inc<224>();
         const int s = (int)(warp >> 2);
         const int wq = (int)(warp & 3);
         const int trow = wq * 32 + (int)lane;
@@ -558,6 +573,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd_kernel(const __grid_c
                 }
             }
         }
+    } else {
+        setmaxnreg_dec<56>();  // idle warp of the TMA / MMA warpgroup
     }
 
     // ---- teardown
