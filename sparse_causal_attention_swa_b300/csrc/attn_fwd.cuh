@@ -1,5 +1,6 @@
 // attn_fwd.cuh -- sm_103a forward kernel for causal sliding-window attention and its two
-// variants (local + strided sparse, differential), one CTA per work item.
+// variants (local + strided sparse, differential); a persistent grid of one CTA per SM
+// walks the work items.
 //
 // What it computes (sources cited by page title and section):
 //   * "SWA：滑动窗口注意力与跨层信息传递" §3.1: out_i = softmax_j(scale q_i.k_j + M_ij) v_j
@@ -86,6 +87,7 @@ struct KParams {
     int pair_mode;      // 1: both slots on the same rows; 0: consecutive row tiles of a head
     float scale_log2;   // scale * log2(e)
     float lambda;       // diff only
+    int n_items;        // work items; the grid is persistent and walks them
 };
 
 template <int D, int MODE>
@@ -107,7 +109,8 @@ struct SmemLayout {
     static constexpr int BAR_L = BAR_O + 2;
     static constexpr int BAR_DRAIN = BAR_L + 1;  // two: one per MMA issuer
     static constexpr int BAR_TURN = BAR_DRAIN + 2;  // two: "slot s may issue its next batch"
-    static constexpr int NBARS = BAR_TURN + 2;
+    static constexpr int BAR_QFREE = BAR_TURN + 2;  // the Q tiles may be replaced
+    static constexpr int NBARS = BAR_QFREE + 1;
     static constexpr int OFF_TMEM = OFF_BAR + NBARS * 8;
     static constexpr int OFF_ABORT = OFF_TMEM + 4;
     static constexpr int OFF_LSM = (OFF_ABORT + 4 + 15) / 16 * 16;
@@ -191,26 +194,40 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd_kernel(const __grid_c
 
     const uint32_t warp = warp_id();
     const uint32_t lane = lane_id();
-    const WorkItem wi = decode_item<MODE>(p, blockIdx.x);
 
-    // ---- tile sequence of this item
-    int n_tiles, kv_lo = 0, list_off = 0;
-    if (MODE == MODE_STRIDED) {
-        const int nblk = p.pair_mode ? p.n_qtiles : (p.n_qtiles + 1) / 2;
-        list_off = nblk + 1 + p.tiles[wi.block];
-        n_tiles = p.tiles[wi.block + 1] - p.tiles[wi.block];
-    } else {
-        kv_lo = (MODE == MODE_DIFF) ? 0 : max(0, wi.R0 - p.W + 1) / BN;
-        n_tiles = wi.R1 / BN - kv_lo + 1;
-    }
-    auto tile_at = [&](int jj, int& kind, int& idx) {
+    // ---- the items of this CTA: a static zig-zag over rounds of gridDim.x items (items are
+    // ordered heaviest first, so alternating the direction of every round evens the load)
+    const int G = (int)gridDim.x;
+    const int n_rounds = (p.n_items + G - 1) / G;
+    auto item_of = [&](int r) -> int {
+        return r * G + ((r & 1) ? (G - 1 - (int)blockIdx.x) : (int)blockIdx.x);
+    };
+    // ---- tile sequence of an item
+    struct TileSeq {
+        int n_tiles, kv_lo, list_off;
+    };
+    auto tile_seq = [&](const WorkItem& wi) -> TileSeq {
+        TileSeq t;
+        t.kv_lo = 0;
+        t.list_off = 0;
         if (MODE == MODE_STRIDED) {
-            const int e = p.tiles[list_off + jj];
+            const int nblk = p.pair_mode ? p.n_qtiles : (p.n_qtiles + 1) / 2;
+            t.list_off = nblk + 1 + p.tiles[wi.block];
+            t.n_tiles = p.tiles[wi.block + 1] - p.tiles[wi.block];
+        } else {
+            t.kv_lo = (MODE == MODE_DIFF) ? 0 : max(0, wi.R0 - p.W + 1) / BN;
+            t.n_tiles = wi.R1 / BN - t.kv_lo + 1;
+        }
+        return t;
+    };
+    auto tile_at = [&](const TileSeq& t, int jj, int& kind, int& idx) {
+        if (MODE == MODE_STRIDED) {
+            const int e = p.tiles[t.list_off + jj];
             kind = e >> TILE_KIND_SHIFT;
             idx = e & ((1 << TILE_KIND_SHIFT) - 1);
         } else {
             kind = TILE_KIND_WINDOW;
-            idx = kv_lo + jj;
+            idx = t.kv_lo + jj;
         }
     };
 
@@ -221,6 +238,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd_kernel(const __grid_c
     }
     if (threadIdx.x == 0) {
         mbar_init(bar(L::BAR_Q), 1);
+        mbar_init(bar(L::BAR_QFREE), 2);  // both issuers' last S of an item
         for (int s = 0; s < L::STAGES; ++s) {
             mbar_init(bar(L::BAR_FULL + s), 1);
             mbar_init(bar(L::BAR_EMPTY + s), 2);  // released by both MMA issuers
@@ -260,47 +278,68 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd_kernel(const __grid_c
         if (lane == 0) {
             constexpr int NCH = D / 64;  // 64-column (128-byte) chunks per row
             uint32_t used_mask = 0, par_mask = 0;  // per stage: filled at least once / parity
-            // Q tiles of both slots
-            mbar_arrive_expect_tx(bar(L::BAR_Q), 2 * L::QBYTES);
-            for (int s = 0; s < 2; ++s) {
-                const CUtensorMap* mq = (MODE == MODE_DIFF && s == 1) ? &p.tm_q2 : &p.tm_q;
-                const int mat = wi.b * p.Hq + wi.h[s];
-                for (int c = 0; c < NCH; ++c)
-                    tma_load_3d(sbase + L::OFF_Q + s * L::QBYTES + c * (BM * 128), mq, bar(L::BAR_Q),
-                                c * 64, wi.r0[s], mat);
-            }
             uint32_t st = 0, ph = 0;
-            const int kmat = wi.b * p.Hkv + wi.hk;
             bool ok = true;
-            auto push = [&](const CUtensorMap* m, int row) -> bool {
-                if (!mbar_wait_bounded(bar(L::BAR_EMPTY + st), ph ^ 1u, abort_flag, lim)) return false;
-                mbar_arrive_expect_tx(bar(L::BAR_FULL + st), L::EBYTES);
-                const uint32_t dst = sbase + L::OFF_RING + st * L::EBYTES;
-                for (int c = 0; c < NCH; ++c)
-                    tma_load_3d(dst + c * (BN * 128), m, bar(L::BAR_FULL + st), c * 64, row, kmat);
-                used_mask |= 1u << st;
-                par_mask = (par_mask & ~(1u << st)) | (ph << st);
-                if (++st == (uint32_t)L::STAGES) {
-                    st = 0;
-                    ph ^= 1u;
+            int it = 0;  // items loaded so far
+            for (int r = 0; r < n_rounds && ok; ++r) {
+                const int item = item_of(r);
+                if (item >= p.n_items) continue;
+                const WorkItem wi = decode_item<MODE>(p, item);
+                const TileSeq ts = tile_seq(wi);
+                const int kmat = wi.b * p.Hkv + wi.hk;
+                auto push = [&](const CUtensorMap* m, int row) -> bool {
+                    if (!mbar_wait_bounded(bar(L::BAR_EMPTY + st), ph ^ 1u, abort_flag, lim))
+                        return false;
+                    mbar_arrive_expect_tx(bar(L::BAR_FULL + st), L::EBYTES);
+                    const uint32_t dst = sbase + L::OFF_RING + st * L::EBYTES;
+                    for (int c = 0; c < NCH; ++c)
+                        tma_load_3d(dst + c * (BN * 128), m, bar(L::BAR_FULL + st), c * 64, row,
+                                    kmat);
+                    used_mask |= 1u << st;
+                    par_mask = (par_mask & ~(1u << st)) | (ph << st);
+                    if (++st == (uint32_t)L::STAGES) {
+                        st = 0;
+                        ph ^= 1u;
+                    }
+                    return true;
+                };
+                // Q tiles of both slots, once the previous item's S products have read them
+                auto load_q = [&]() -> bool {
+                    if (it > 0 && !mbar_wait_bounded(bar(L::BAR_QFREE), (uint32_t)(it - 1) & 1u,
+                                                     abort_flag, lim))
+                        return false;
+                    mbar_arrive_expect_tx(bar(L::BAR_Q), 2 * L::QBYTES);
+                    for (int s = 0; s < 2; ++s) {
+                        const CUtensorMap* mq =
+                            (MODE == MODE_DIFF && s == 1) ? &p.tm_q2 : &p.tm_q;
+                        const int mat = wi.b * p.Hq + wi.h[s];
+                        for (int c = 0; c < NCH; ++c)
+                            tma_load_3d(sbase + L::OFF_Q + s * L::QBYTES + c * (BM * 128), mq,
+                                        bar(L::BAR_Q), c * 64, wi.r0[s], mat);
+                    }
+                    ++it;
+                    return true;
+                };
+                // order: K of the first tile (it can land while the previous item finishes),
+                // then Q, then the rest of the item's tiles
+                for (int jj = 0; jj < ts.n_tiles && ok; ++jj) {
+                    int kind, idx;
+                    tile_at(ts, jj, kind, idx);
+                    const bool compact = (MODE == MODE_STRIDED && kind == TILE_KIND_STRIDED);
+                    const CUtensorMap* mk = compact ? &p.tm_k2 : &p.tm_k;
+                    const CUtensorMap* mv = compact ? &p.tm_v2 : &p.tm_v;
+                    const int row = idx * BN;
+                    ok = push(mk, row);
+                    if (ok && MODE == MODE_DIFF) ok = push(&p.tm_k2, row);
+                    if (ok && jj == 0) ok = load_q();
+                    if (ok) ok = push(mv, row);
                 }
-                return true;
-            };
-            for (int jj = 0; jj < n_tiles && ok; ++jj) {
-                int kind, idx;
-                tile_at(jj, kind, idx);
-                const bool compact = (MODE == MODE_STRIDED && kind == TILE_KIND_STRIDED);
-                const CUtensorMap* mk = compact ? &p.tm_k2 : &p.tm_k;
-                const CUtensorMap* mv = compact ? &p.tm_v2 : &p.tm_v;
-                const int row = idx * BN;
-                ok = push(mk, row);
-                if (ok && MODE == MODE_DIFF) ok = push(&p.tm_k2, row);
-                if (ok) ok = push(mv, row);
             }
             // drain: every issued copy must have landed before the CTA may exit
             {
                 volatile int never = 0;
-                (void)mbar_wait_bounded(bar(L::BAR_Q), 0, &never, lim);
+                if (it > 0)
+                    (void)mbar_wait_bounded(bar(L::BAR_Q), (uint32_t)(it - 1) & 1u, &never, lim);
                 for (int s = 0; s < L::STAGES; ++s)
                     if (used_mask & (1u << s))
                         (void)mbar_wait_bounded(bar(L::BAR_FULL + s), (par_mask >> s) & 1u, &never,
@@ -357,54 +396,71 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd_kernel(const __grid_c
             }
             return true;
         };
+        // Turn order: the slots' batches alternate, slot 0 first, across all items.  Batch
+        // b of slot 0 (b >= 1) waits for the completion of phase b-1 of t[0], which slot 1
+        // completes with its batch b-1; batch b of slot 1 waits for phase b of t[1], which
+        // slot 0 completes with its batch b.  Neither slot can run two batches ahead, so a
+        // parity wait never aliases.
+        uint32_t nb = 0;  // batches this slot has issued
+        auto my_turn = [&]() -> bool {
+            if (s == 0) return nb == 0 ? true : wait(bar(L::BAR_TURN), (nb - 1) & 1u);
+            return wait(bar(L::BAR_TURN + 1), nb & 1u);
+        };
+        uint32_t np = 0;  // P phases consumed
         // Both issuers pop every ring entry (in the producer's order) and release every
         // entry they popped, so each empty barrier gets its two arrivals; an entry this
         // slot does not read (the other stream's K in the differential call) is released
         // after this warp's earlier MMAs, which is merely conservative.
-        int kA = 0, kB = 0;
-        ok = wait(bar(L::BAR_Q), 0);
-        if (ok) ok = pop(kA);
-        if (ok && MODE == MODE_DIFF) ok = pop(kB);
-        // turn order: slot 1 issues a batch only after slot 0 has issued its batch of the
-        // same step, and slot 0 only after slot 1 has issued its previous one.  Slot 0
-        // can therefore never be two batches ahead, so the turn phases cannot alias.
-        // Turn barrier t[1] completes once per slot-0 batch, t[0] once per slot-1 batch.
-        if (ok && s == 1) ok = wait(bar(L::BAR_TURN + 1), 0u);
-        if (ok) {
+        int it = 0;
+        for (int r = 0; r < n_rounds && ok; ++r) {
+            const int item = item_of(r);
+            if (item >= p.n_items) continue;
+            const TileSeq ts = tile_seq(decode_item<MODE>(p, item));
+            int kA = 0, kB = 0;
+            ok = wait(bar(L::BAR_Q), (uint32_t)it & 1u);
+            if (ok) ok = pop(kA);
+            if (ok && MODE == MODE_DIFF) ok = pop(kB);
+            if (ok) ok = my_turn();
+            if (!ok) break;
             tc_fence_after();
             issue_S((MODE == MODE_DIFF && s == 1) ? kB : kA);
             mma_commit_elect(bar(L::BAR_S + s));
+            if (ts.n_tiles == 1) mma_commit_elect(bar(L::BAR_QFREE));
             mma_commit_elect(bar(L::BAR_EMPTY + kA));
             if (MODE == MODE_DIFF) mma_commit_elect(bar(L::BAR_EMPTY + kB));
             mbar_arrive_elect(bar(L::BAR_TURN + (s ^ 1)));
-        }
-        for (int jj = 0; jj < n_tiles && ok; ++jj) {
-            int ve = 0, nA = 0, nB = 0;
-            const bool more = jj + 1 < n_tiles;
-            ok = pop(ve);
-            if (ok && more) {
-                ok = pop(nA);
-                if (ok && MODE == MODE_DIFF) ok = pop(nB);
+            ++nb;
+            for (int jj = 0; jj < ts.n_tiles && ok; ++jj) {
+                int ve = 0, nA = 0, nB = 0;
+                const bool more = jj + 1 < ts.n_tiles;
+                ok = pop(ve);
+                if (ok && more) {
+                    ok = pop(nA);
+                    if (ok && MODE == MODE_DIFF) ok = pop(nB);
+                }
+                if (ok) ok = wait(bar(L::BAR_P + s), np & 1u);
+                ++np;
+                if (ok) ok = my_turn();
+                if (!ok) break;
+                tc_fence_after();
+                issue_PV(ve, jj > 0);
+                if (more) {
+                    issue_S((MODE == MODE_DIFF && s == 1) ? nB : nA);
+                    mma_commit_elect(bar(L::BAR_S + s));
+                    // the item's last S product: its Q tile may be replaced once it is done
+                    if (jj + 2 == ts.n_tiles) mma_commit_elect(bar(L::BAR_QFREE));
+                } else {
+                    mma_commit_elect(bar(L::BAR_O + s));
+                }
+                mbar_arrive_elect(bar(L::BAR_TURN + (s ^ 1)));
+                ++nb;
+                mma_commit_elect(bar(L::BAR_EMPTY + ve));
+                if (more) {
+                    mma_commit_elect(bar(L::BAR_EMPTY + nA));
+                    if (MODE == MODE_DIFF) mma_commit_elect(bar(L::BAR_EMPTY + nB));
+                }
             }
-            if (ok) ok = wait(bar(L::BAR_P + s), (uint32_t)jj & 1u);
-            // slot 0's batch jj follows slot 1's batch jj-1 (phase jj of t[0]); slot 1's
-            // batch jj follows slot 0's batch jj (phase jj+1 of t[1])
-            if (ok) ok = wait(bar(L::BAR_TURN + s), (uint32_t)(jj + s) & 1u);
-            if (!ok) break;
-            tc_fence_after();
-            issue_PV(ve, jj > 0);
-            if (more) {
-                issue_S((MODE == MODE_DIFF && s == 1) ? nB : nA);
-                mma_commit_elect(bar(L::BAR_S + s));
-            } else {
-                mma_commit_elect(bar(L::BAR_O + s));
-            }
-            mbar_arrive_elect(bar(L::BAR_TURN + (s ^ 1)));
-            mma_commit_elect(bar(L::BAR_EMPTY + ve));
-            if (more) {
-                mma_commit_elect(bar(L::BAR_EMPTY + nA));
-                if (MODE == MODE_DIFF) mma_commit_elect(bar(L::BAR_EMPTY + nB));
-            }
+            ++it;
         }
         // drain: all MMAs this warp issued must complete before TMEM is released
         __syncwarp();
@@ -418,115 +474,125 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd_kernel(const __grid_c
         const int s = (int)(warp >> 2);
         const int wq = (int)(warp & 3);
         const int trow = wq * 32 + (int)lane;
-        const int row = wi.r0[s] + trow;
         const uint32_t lane_off = (uint32_t)(wq * 32) << 16;
         const uint32_t tS = tmem_base + lane_off + (uint32_t)(s * 128);
         const uint32_t tO = tmem_base + lane_off + 256u + (uint32_t)(s * 128);
         const float sl2 = p.scale_log2;
-        const int lo_i = (MODE == MODE_DIFF) ? 0 : max(0, row - p.W + 1);
-        const int lo_strided = (MODE == MODE_STRIDED) ? (lo_i + p.stride - 1) / p.stride : 0;
-        float m = -INFINITY, l = 0.f;
         bool ok = true;
-        for (int jj = 0; jj < n_tiles; ++jj) {
-            ok = mbar_wait_bounded(bar(L::BAR_S + s), (uint32_t)jj & 1u, abort_flag, lim);
+        uint32_t ns = 0;  // S phases consumed
+        int it = 0;
+        for (int r = 0; r < n_rounds && ok; ++r) {
+            const int item = item_of(r);
+            if (item >= p.n_items) continue;
+            const WorkItem wi = decode_item<MODE>(p, item);
+            const TileSeq ts = tile_seq(wi);
+            const int row = wi.r0[s] + trow;
+            const int lo_i = (MODE == MODE_DIFF) ? 0 : max(0, row - p.W + 1);
+            const int lo_strided =
+                (MODE == MODE_STRIDED) ? (lo_i + p.stride - 1) / p.stride : 0;
+            float m = -INFINITY, l = 0.f;
+            for (int jj = 0; jj < ts.n_tiles; ++jj) {
+                ok = mbar_wait_bounded(bar(L::BAR_S + s), ns & 1u, abort_flag, lim);
+                ++ns;
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                tc_fence_after();
+                // the whole 128-key score row of this thread, one TMEM load
+                uint32_t xr[BN];
+                tmem_ld128(tS, xr);
+                // allowed columns of this row in this tile: [a, bnd]
+                int kind, idx;
+                tile_at(ts, jj, kind, idx);
+                int a, bnd;
+                if (MODE == MODE_STRIDED && kind == TILE_KIND_STRIDED) {
+                    a = 0;
+                    bnd = lo_strided - idx * BN - 1;
+                } else {
+                    const int c0 = idx * BN;
+                    a = lo_i - c0;
+                    bnd = row - c0;
+                }
+                if (a > 0 || bnd < BN - 1) {
+#pragma unroll
+                    for (int t = 0; t < BN; ++t)
+                        xr[t] = (t >= a && t <= bnd) ? xr[t] : __float_as_uint(-INFINITY);
+                }
+                // row maximum: eight independent 3-input max chains, then a short tree
+                float mc[8];
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    float v = __uint_as_float(xr[c * 16]);
+#pragma unroll
+                    for (int u = 1; u < 15; u += 2)
+                        v = fmax3(v, __uint_as_float(xr[c * 16 + u]),
+                                  __uint_as_float(xr[c * 16 + u + 1]));
+                    mc[c] = fmaxf(v, __uint_as_float(xr[c * 16 + 15]));
+                }
+                const float mt = fmax3(fmax3(mc[0], mc[1], mc[2]), fmax3(mc[3], mc[4], mc[5]),
+                                       fmaxf(mc[6], mc[7]));
+                const float m_new = fmaxf(m, mt);
+                const bool need = (m_new - m) * sl2 > RESCALE_THRESHOLD;
+                const bool rescale = __any_sync(0xffffffffu, need);
+                float alpha = 1.f;
+                if (rescale) {
+                    alpha = (m_new == -INFINITY) ? 1.f : fast_exp2((m - m_new) * sl2);
+                    l *= alpha;
+                    m = m_new;
+                }
+                const float ms = (m == -INFINITY) ? 0.f : m * sl2;
+                // P = exp2(x * scale * log2 e - m * scale * log2 e): the argument two lanes at
+                // a time (packed fma), four packed partial row sums, bf16 pairs stored to TMEM
+                // in 32-column chunks as soon as they are ready
+                const uint64_t sl2x2 = f32x2_pack(sl2, sl2);
+                const uint64_t nmsx2 = f32x2_pack(-ms, -ms);
+                uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+                for (int c = 0; c < BN / 64; ++c) {
+                    uint32_t pk[32];
+#pragma unroll
+                    for (int t = 0; t < 32; ++t) {
+                        const int e = c * 64 + 2 * t;
+                        const uint64_t z = f32x2_fma(
+                            f32x2_pack(__uint_as_float(xr[e]), __uint_as_float(xr[e + 1])), sl2x2,
+                            nmsx2);
+                        float z0, z1;
+                        f32x2_unpack(z, z0, z1);
+                        const float p0 = fast_exp2(z0);
+                        const float p1 = fast_exp2(z1);
+                        acc[t & 3] = f32x2_add(acc[t & 3], f32x2_pack(p0, p1));
+                        pk[t] = pack_bf16x2(p0, p1);
+                    }
+                    tmem_st32(tS + c * 32, pk);
+                }
+                {
+                    const uint64_t s01 = f32x2_add(acc[0], acc[1]);
+                    const uint64_t s23 = f32x2_add(acc[2], acc[3]);
+                    float u0, u1;
+                    f32x2_unpack(f32x2_add(s01, s23), u0, u1);
+                    l += u0 + u1;
+                }
+                // O is complete up to tile jj-1 here (its PV was issued before this tile's S)
+                if (rescale && jj > 0) {
+                    uint32_t rr[32];
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c) {
+                        tmem_ld32(tO + c * 32, rr);
+#pragma unroll
+                        for (int t = 0; t < 32; ++t)
+                            rr[t] = __float_as_uint(__uint_as_float(rr[t]) * alpha);
+                        tmem_st32(tO + c * 32, rr);
+                    }
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(bar(L::BAR_P + s));
+            }
+            if (!ok) break;
+            // ---- epilogue of the item.  Its TMEM reads of O precede this slot's next P
+            // arrival, and the next item's first O product is issued only after that.
+            ok = mbar_wait_bounded(bar(L::BAR_O + s), (uint32_t)it & 1u, abort_flag, lim);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
-            tc_fence_after();
-            // the whole 128-key score row of this thread, one TMEM load
-            uint32_t xr[BN];
-            tmem_ld128(tS, xr);
-            // allowed columns of this row in this tile: [a, bnd]
-            int kind, idx;
-            tile_at(jj, kind, idx);
-            int a, bnd;
-            if (MODE == MODE_STRIDED && kind == TILE_KIND_STRIDED) {
-                a = 0;
-                bnd = lo_strided - idx * BN - 1;
-            } else {
-                const int c0 = idx * BN;
-                a = lo_i - c0;
-                bnd = row - c0;
-            }
-            if (a > 0 || bnd < BN - 1) {
-#pragma unroll
-                for (int t = 0; t < BN; ++t)
-                    xr[t] = (t >= a && t <= bnd) ? xr[t] : __float_as_uint(-INFINITY);
-            }
-            // row maximum: eight independent 3-input max chains, then a short tree
-            float mc[8];
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                float v = __uint_as_float(xr[c * 16]);
-#pragma unroll
-                for (int u = 1; u < 15; u += 2)
-                    v = fmax3(v, __uint_as_float(xr[c * 16 + u]), __uint_as_float(xr[c * 16 + u + 1]));
-                mc[c] = fmaxf(v, __uint_as_float(xr[c * 16 + 15]));
-            }
-            const float mt = fmax3(fmax3(mc[0], mc[1], mc[2]), fmax3(mc[3], mc[4], mc[5]),
-                                   fmaxf(mc[6], mc[7]));
-            const float m_new = fmaxf(m, mt);
-            const bool need = (m_new - m) * sl2 > RESCALE_THRESHOLD;
-            const bool rescale = __any_sync(0xffffffffu, need);
-            float alpha = 1.f;
-            if (rescale) {
-                alpha = (m_new == -INFINITY) ? 1.f : fast_exp2((m - m_new) * sl2);
-                l *= alpha;
-                m = m_new;
-            }
-            const float ms = (m == -INFINITY) ? 0.f : m * sl2;
-            // P = exp2(x * scale * log2 e - m * scale * log2 e): the argument two lanes at a
-            // time (packed fma), four packed partial row sums, bf16 pairs stored to TMEM in
-            // 32-column chunks as soon as they are ready
-            const uint64_t sl2x2 = f32x2_pack(sl2, sl2);
-            const uint64_t nmsx2 = f32x2_pack(-ms, -ms);
-            uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
-#pragma unroll
-            for (int c = 0; c < BN / 64; ++c) {
-                uint32_t pk[32];
-#pragma unroll
-                for (int t = 0; t < 32; ++t) {
-                    const int e = c * 64 + 2 * t;
-                    const uint64_t z = f32x2_fma(
-                        f32x2_pack(__uint_as_float(xr[e]), __uint_as_float(xr[e + 1])), sl2x2,
-                        nmsx2);
-                    float z0, z1;
-                    f32x2_unpack(z, z0, z1);
-                    const float p0 = fast_exp2(z0);
-                    const float p1 = fast_exp2(z1);
-                    acc[t & 3] = f32x2_add(acc[t & 3], f32x2_pack(p0, p1));
-                    pk[t] = pack_bf16x2(p0, p1);
-                }
-                tmem_st32(tS + c * 32, pk);
-            }
-            {
-                const uint64_t s01 = f32x2_add(acc[0], acc[1]);
-                const uint64_t s23 = f32x2_add(acc[2], acc[3]);
-                float u0, u1;
-                f32x2_unpack(f32x2_add(s01, s23), u0, u1);
-                l += u0 + u1;
-            }
-            // O is complete up to tile jj-1 here (its PV was issued before this tile's S)
-            if (rescale && jj > 0) {
-                uint32_t r[32];
-#pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    tmem_ld32(tO + c * 32, r);
-#pragma unroll
-                    for (int t = 0; t < 32; ++t)
-                        r[t] = __float_as_uint(__uint_as_float(r[t]) * alpha);
-                    tmem_st32(tO + c * 32, r);
-                }
-            }
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(bar(L::BAR_P + s));
-        }
-        // ---- epilogue
-        if (ok) {
-            ok = mbar_wait_bounded(bar(L::BAR_O + s), 0, abort_flag, lim);
-            ok = __all_sync(0xffffffffu, ok);
-        }
-        if (ok) {
             tc_fence_after();
             const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
             if (MODE == MODE_DIFF && s == 1) {
@@ -535,43 +601,45 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd_kernel(const __grid_c
             } else {
                 float inv_l2 = 0.f;
                 if (MODE == MODE_DIFF) {
-                    ok = mbar_wait_bounded(bar(L::BAR_L), 0, abort_flag, lim);
-                    if (ok) ok = mbar_wait_bounded(bar(L::BAR_O + 1), 0, abort_flag, lim);
+                    ok = mbar_wait_bounded(bar(L::BAR_L), (uint32_t)it & 1u, abort_flag, lim);
+                    if (ok)
+                        ok = mbar_wait_bounded(bar(L::BAR_O + 1), (uint32_t)it & 1u, abort_flag,
+                                               lim);
                     ok = __all_sync(0xffffffffu, ok);
+                    if (!ok) break;
                     tc_fence_after();
                     inv_l2 = lsm[trow] * p.lambda;
                 }
-                if (ok) {
-                    __nv_bfloat16* orow =
-                        p.out + ((size_t)(wi.b * p.Hq + wi.h[s]) * p.N + (size_t)row) * D;
-                    const uint32_t tO2 = tmem_base + lane_off + 384u;
+                __nv_bfloat16* orow =
+                    p.out + ((size_t)(wi.b * p.Hq + wi.h[s]) * p.N + (size_t)row) * D;
+                const uint32_t tO2 = tmem_base + lane_off + 384u;
 #pragma unroll
-                    for (int c = 0; c < D / 32; ++c) {
-                        uint32_t r[32];
-                        tmem_ld32(tO + c * 32, r);
-                        float y[32];
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t rr[32];
+                    tmem_ld32(tO + c * 32, rr);
+                    float y[32];
 #pragma unroll
-                        for (int t = 0; t < 32; ++t) y[t] = __uint_as_float(r[t]) * inv_l;
-                        if (MODE == MODE_DIFF) {
-                            tmem_ld32(tO2 + c * 32, r);
+                    for (int t = 0; t < 32; ++t) y[t] = __uint_as_float(rr[t]) * inv_l;
+                    if (MODE == MODE_DIFF) {
+                        tmem_ld32(tO2 + c * 32, rr);
 #pragma unroll
-                            for (int t = 0; t < 32; ++t) y[t] -= __uint_as_float(r[t]) * inv_l2;
-                        }
-                        if (row < p.N) {
-                            uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+                        for (int t = 0; t < 32; ++t) y[t] -= __uint_as_float(rr[t]) * inv_l2;
+                    }
+                    if (row < p.N) {
+                        uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
 #pragma unroll
-                            for (int v4 = 0; v4 < 4; ++v4) {
-                                uint4 u;
-                                u.x = pack_bf16x2(y[v4 * 8 + 0], y[v4 * 8 + 1]);
-                                u.y = pack_bf16x2(y[v4 * 8 + 2], y[v4 * 8 + 3]);
-                                u.z = pack_bf16x2(y[v4 * 8 + 4], y[v4 * 8 + 5]);
-                                u.w = pack_bf16x2(y[v4 * 8 + 6], y[v4 * 8 + 7]);
-                                dst[v4] = u;
-                            }
+                        for (int v4 = 0; v4 < 4; ++v4) {
+                            uint4 u;
+                            u.x = pack_bf16x2(y[v4 * 8 + 0], y[v4 * 8 + 1]);
+                            u.y = pack_bf16x2(y[v4 * 8 + 2], y[v4 * 8 + 3]);
+                            u.z = pack_bf16x2(y[v4 * 8 + 4], y[v4 * 8 + 5]);
+                            u.w = pack_bf16x2(y[v4 * 8 + 6], y[v4 * 8 + 7]);
+                            dst[v4] = u;
                         }
                     }
                 }
             }
+            ++it;
         }
     } else {
         setmaxnreg_dec<56>();  // idle warp of the TMA / MMA warpgroup

@@ -32,6 +32,7 @@ struct DeviceState {
     bool probed = false;
     bool supported = false;
     int* status = nullptr;  // device address of g_status_word
+    int num_sms = 0;
     bool attr_set[2][3] = {};
     // strided tile lists, keyed by (N, W, stride, rows per block)
     std::map<std::tuple<int, int, int, int>, int*> tile_lists;
@@ -53,6 +54,9 @@ int current_device_state(DeviceState** out) {
             return SWA_ERR_CUDA;
         st.supported = (major == 10 && minor == 3);
         if (st.supported) {
+            if (cudaDeviceGetAttribute(&st.num_sms, cudaDevAttrMultiProcessorCount, dev) !=
+                cudaSuccess)
+                return SWA_ERR_CUDA;
             void* p = nullptr;
             if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return SWA_ERR_CUDA;
             st.status = static_cast<int*>(p);
@@ -112,12 +116,17 @@ int launch(const KParams& kp, int n_items, cudaStream_t stream, DeviceState& st)
             return SWA_ERR_CUDA;
         set = true;
     }
+    // persistent grid: one CTA per SM (tensor memory and shared memory allow no more),
+    // each walking its share of the items
+    KParams kq = kp;
+    kq.n_items = n_items;
+    const int grid = std::min(n_items, st.num_sms);
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)n_items, 1, 1);
+    cfg.gridDim = dim3((unsigned)grid, 1, 1);
     cfg.blockDim = dim3(swa::NUM_THREADS, 1, 1);
     cfg.dynamicSmemBytes = L::BYTES;
     cfg.stream = stream;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, kp);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, kq);
     return e == cudaSuccess ? SWA_OK : SWA_ERR_CUDA;
 }
 
