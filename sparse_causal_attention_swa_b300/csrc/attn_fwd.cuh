@@ -78,6 +78,7 @@ struct KParams {
     CUtensorMap tm_q2;  // diff: Q2
     CUtensorMap tm_k2;  // diff: K2 ; strided: compact keys, rows 0, s, 2s, ...
     CUtensorMap tm_v2;  // strided: compact values
+    CUtensorMap tm_out; // output, view [B*Hq][N][d] (TMA stores of the epilogue)
     __nv_bfloat16* out;
     const int* tiles;   // strided: [n_blocks + 1] offsets, then encoded entries
     int* status;        // device status word (SWA_ERR_TIMEOUT on a watchdog abort)
@@ -97,7 +98,10 @@ struct SmemLayout {
     static constexpr int STAGES = (D == 128) ? 4 : 8;
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_RING = 2 * QBYTES;
-    static constexpr int OFF_BAR = OFF_RING + STAGES * EBYTES;
+    // epilogue staging: per slot one 128-row x 64-column bf16 box (16 KiB, 128B-swizzled)
+    static constexpr int OFF_STAGE = OFF_RING + STAGES * EBYTES;
+    static constexpr int STAGE_HALF = BM * 64 * 2;
+    static constexpr int OFF_BAR = OFF_STAGE + 2 * STAGE_HALF;
     // barriers: q_full, ring_full[S], ring_empty[S], s_full[2], p_full[2], o_final[2],
     //           lsm_ready, drain
     static constexpr int BAR_Q = 0;
@@ -110,14 +114,17 @@ struct SmemLayout {
     static constexpr int BAR_DRAIN = BAR_L + 1;  // two: one per MMA issuer
     static constexpr int BAR_TURN = BAR_DRAIN + 2;  // two: "slot s may issue its next batch"
     static constexpr int BAR_QFREE = BAR_TURN + 2;  // the Q tiles may be replaced
-    static constexpr int NBARS = BAR_QFREE + 1;
+    static constexpr int BAR_BOXF = BAR_QFREE + 1;  // two: a slot's staging box is written
+    static constexpr int BAR_BOXE = BAR_BOXF + 2;   // two: its TMA store has read the box
+    static constexpr int NBARS = BAR_BOXE + 2;
     static constexpr int OFF_TMEM = OFF_BAR + NBARS * 8;
     static constexpr int OFF_ABORT = OFF_TMEM + 4;
     static constexpr int OFF_LSM = (OFF_ABORT + 4 + 15) / 16 * 16;
     static constexpr int END = OFF_LSM + BM * 4;
     static constexpr int BYTES = END + 1024;  // slack for aligning the base to 1024
     static_assert(BYTES <= 232448, "shared memory budget");
-    static_assert(EBYTES % 1024 == 0 && QBYTES % 1024 == 0, "1024-byte tile alignment");
+    static_assert(EBYTES % 1024 == 0 && QBYTES % 1024 == 0 && STAGE_HALF % 1024 == 0,
+                  "1024-byte tile alignment");
 };
 
 struct WorkItem {
@@ -247,6 +254,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd_kernel(const __grid_c
             mbar_init(bar(L::BAR_S + s), 1);
             mbar_init(bar(L::BAR_P + s), 128);
             mbar_init(bar(L::BAR_O + s), 1);
+            mbar_init(bar(L::BAR_BOXF + s), 128);
+            mbar_init(bar(L::BAR_BOXE + s), 1);
         }
         mbar_init(bar(L::BAR_L), 128);
         mbar_init(bar(L::BAR_DRAIN), 1);
@@ -260,6 +269,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd_kernel(const __grid_c
         tma_prefetch_desc(&p.tm_q);
         tma_prefetch_desc(&p.tm_k);
         tma_prefetch_desc(&p.tm_v);
+        tma_prefetch_desc(&p.tm_out);
         if (MODE != MODE_WINDOW) tma_prefetch_desc(&p.tm_k2);
         if (MODE == MODE_DIFF) tma_prefetch_desc(&p.tm_q2);
         if (MODE == MODE_STRIDED) tma_prefetch_desc(&p.tm_v2);
@@ -480,6 +490,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd_kernel(const __grid_c
         const float sl2 = p.scale_log2;
         bool ok = true;
         uint32_t ns = 0;  // S phases consumed
+        uint32_t nbox = 0;  // staging boxes this slot has written
         int it = 0;
         for (int r = 0; r < n_rounds && ok; ++r) {
             const int item = item_of(r);
@@ -610,37 +621,61 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd_kernel(const __grid_c
                     tc_fence_after();
                     inv_l2 = lsm[trow] * p.lambda;
                 }
-                __nv_bfloat16* orow =
-                    p.out + ((size_t)(wi.b * p.Hq + wi.h[s]) * p.N + (size_t)row) * D;
+                // O / l (differential: O1 / l1 - lambda O2 / l2) to bf16, 64 columns at a time
+                // through this slot's staging box, written out by one TMA store per box;
+                // TMA drops the rows past N
                 const uint32_t tO2 = tmem_base + lane_off + 384u;
+                const uint32_t stage = sbase + L::OFF_STAGE + (uint32_t)(s * L::STAGE_HALF);
+                const uint32_t srow = stage + (uint32_t)trow * 128u;
+                const bool store = wi.r0[s] < p.N;
+                const int mat = wi.b * p.Hq + wi.h[s];
+                for (int c64 = 0; c64 < D / 64 && ok; ++c64) {
+                    // the previous store from this box must have read it
+                    if (nbox > 0)
+                        ok = mbar_wait_bounded(bar(L::BAR_BOXE + s), (nbox - 1) & 1u, abort_flag,
+                                               lim);
+                    if (!ok) break;
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t rr[32];
-                    tmem_ld32(tO + c * 32, rr);
-                    float y[32];
+                    for (int h = 0; h < 2; ++h) {
+                        uint32_t rr[32];
+                        tmem_ld32(tO + c64 * 64 + h * 32, rr);
+                        float y[32];
 #pragma unroll
-                    for (int t = 0; t < 32; ++t) y[t] = __uint_as_float(rr[t]) * inv_l;
-                    if (MODE == MODE_DIFF) {
-                        tmem_ld32(tO2 + c * 32, rr);
+                        for (int t = 0; t < 32; ++t) y[t] = __uint_as_float(rr[t]) * inv_l;
+                        if (MODE == MODE_DIFF) {
+                            tmem_ld32(tO2 + c64 * 64 + h * 32, rr);
 #pragma unroll
-                        for (int t = 0; t < 32; ++t) y[t] -= __uint_as_float(rr[t]) * inv_l2;
-                    }
-                    if (row < p.N) {
-                        uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+                            for (int t = 0; t < 32; ++t) y[t] -= __uint_as_float(rr[t]) * inv_l2;
+                        }
+                        // four 16-byte units; unit u of a 128-byte row sits at u ^ (row & 7)
 #pragma unroll
                         for (int v4 = 0; v4 < 4; ++v4) {
-                            uint4 u;
-                            u.x = pack_bf16x2(y[v4 * 8 + 0], y[v4 * 8 + 1]);
-                            u.y = pack_bf16x2(y[v4 * 8 + 2], y[v4 * 8 + 3]);
-                            u.z = pack_bf16x2(y[v4 * 8 + 4], y[v4 * 8 + 5]);
-                            u.w = pack_bf16x2(y[v4 * 8 + 6], y[v4 * 8 + 7]);
-                            dst[v4] = u;
+                            const uint32_t u = (uint32_t)(h * 4 + v4);
+                            st_shared_v4(srow + ((u ^ (uint32_t)(trow & 7)) << 4),
+                                         pack_bf16x2(y[v4 * 8 + 0], y[v4 * 8 + 1]),
+                                         pack_bf16x2(y[v4 * 8 + 2], y[v4 * 8 + 3]),
+                                         pack_bf16x2(y[v4 * 8 + 4], y[v4 * 8 + 5]),
+                                         pack_bf16x2(y[v4 * 8 + 6], y[v4 * 8 + 7]));
                         }
                     }
+                    fence_proxy_async_smem();
+                    mbar_arrive(bar(L::BAR_BOXF + s));
+                    if (trow == 0) {
+                        ok = mbar_wait_bounded(bar(L::BAR_BOXF + s), nbox & 1u, abort_flag, lim);
+                        if (ok && store) {
+                            tma_store_3d(&p.tm_out, stage, c64 * 64, wi.r0[s], mat);
+                            bulk_commit_group();
+                            bulk_wait_read_all();
+                        }
+                        mbar_arrive(bar(L::BAR_BOXE + s));
+                    }
+                    ++nbox;
                 }
             }
+            if (!ok) break;
             ++it;
         }
+        if (trow == 0) bulk_wait_all();  // the output is written before the CTA exits
     } else {
         setmaxnreg_dec<56>();  // idle warp of the TMA / MMA warpgroup
     }

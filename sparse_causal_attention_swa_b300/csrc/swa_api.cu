@@ -296,6 +296,7 @@ int swa_attn_fwd(const void* q, const void* k, const void* v, void* out, int B, 
     fill_common(kp, B, Hq, Hkv, N, std::min(W, N), 1, scale, out, *st);
     kp.pair_mode = ((Hq / Hkv) % 2 == 0) ? 1 : 0;
     if ((rc = make_map(&kp.tm_q, q, d, N, d, (long long)B * Hq, (long long)N * d))) return rc;
+    if ((rc = make_map(&kp.tm_out, out, d, N, d, (long long)B * Hq, (long long)N * d))) return rc;
     if ((rc = make_map(&kp.tm_k, k, d, N, d, (long long)B * Hkv, (long long)N * d))) return rc;
     if ((rc = make_map(&kp.tm_v, v, d, N, d, (long long)B * Hkv, (long long)N * d))) return rc;
     return dispatch<swa::MODE_WINDOW>(d, kp, n_items_for(kp), static_cast<cudaStream_t>(stream),
@@ -325,6 +326,7 @@ int strided_attn_fwd(const void* q, const void* k, const void* v, void* out, int
     kp.tiles = list;
     const long long ns = (N - 1) / sc + 1;  // keys 0, s, 2s, ... < N
     if ((rc = make_map(&kp.tm_q, q, d, N, d, (long long)B * Hq, (long long)N * d))) return rc;
+    if ((rc = make_map(&kp.tm_out, out, d, N, d, (long long)B * Hq, (long long)N * d))) return rc;
     if ((rc = make_map(&kp.tm_k, k, d, N, d, (long long)B * Hkv, (long long)N * d))) return rc;
     if ((rc = make_map(&kp.tm_v, v, d, N, d, (long long)B * Hkv, (long long)N * d))) return rc;
     if ((rc = make_map(&kp.tm_k2, k, d, ns, (long long)sc * d, (long long)B * Hkv,
@@ -380,6 +382,7 @@ int strided_attn_fwd_noalloc(const void* q, const void* k, const void* v, void* 
     kp.tiles = na.tiles;
     const long long ns = (N - 1) / sc + 1;
     if ((rc = make_map(&kp.tm_q, q, d, N, d, (long long)B * Hq, (long long)N * d))) return rc;
+    if ((rc = make_map(&kp.tm_out, out, d, N, d, (long long)B * Hq, (long long)N * d))) return rc;
     if ((rc = make_map(&kp.tm_k, k, d, N, d, (long long)B * Hkv, (long long)N * d))) return rc;
     if ((rc = make_map(&kp.tm_v, v, d, N, d, (long long)B * Hkv, (long long)N * d))) return rc;
     if ((rc = make_map(&kp.tm_k2, k, d, ns, (long long)sc * d, (long long)B * Hkv,
@@ -410,6 +413,7 @@ int diff_attn_fwd(const void* q1, const void* k1, const void* q2, const void* k2
     kp.lambda = lambda;
     kp.pair_mode = 1;  // the two slots are the two score streams of the same rows
     if ((rc = make_map(&kp.tm_q, q1, d, N, d, (long long)B * Hq, (long long)N * d))) return rc;
+    if ((rc = make_map(&kp.tm_out, out, d, N, d, (long long)B * Hq, (long long)N * d))) return rc;
     if ((rc = make_map(&kp.tm_k, k1, d, N, d, (long long)B * Hkv, (long long)N * d))) return rc;
     if ((rc = make_map(&kp.tm_q2, q2, d, N, d, (long long)B * Hq, (long long)N * d))) return rc;
     if ((rc = make_map(&kp.tm_k2, k2, d, N, d, (long long)B * Hkv, (long long)N * d))) return rc;
