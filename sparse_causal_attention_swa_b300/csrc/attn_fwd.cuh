@@ -252,7 +252,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd_kernel(const __grid_c
         }
         for (int s = 0; s < 2; ++s) {
             mbar_init(bar(L::BAR_S + s), 1);
-            mbar_init(bar(L::BAR_P + s), 128);
+            mbar_init(bar(L::BAR_P + s), 4);  // one arrival per softmax warp
             mbar_init(bar(L::BAR_O + s), 1);
             mbar_init(bar(L::BAR_BOXF + s), 128);
             mbar_init(bar(L::BAR_BOXE + s), 1);
@@ -448,9 +448,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd_kernel(const __grid_c
                     ok = pop(nA);
                     if (ok && MODE == MODE_DIFF) ok = pop(nB);
                 }
-                if (ok) ok = wait(bar(L::BAR_P + s), np & 1u);
+                // Both the slot's P and its turn are needed; wait first on the one that
+                // usually completes first (slot 0: its turn, slot 1: its P), so the second
+                // wait's latency is the only one left on the critical path.
+                if (s == 0) {
+                    if (ok) ok = my_turn();
+                    if (ok) ok = wait(bar(L::BAR_P + s), np & 1u);
+                } else {
+                    if (ok) ok = wait(bar(L::BAR_P + s), np & 1u);
+                    if (ok) ok = my_turn();
+                }
                 ++np;
-                if (ok) ok = my_turn();
                 if (!ok) break;
                 tc_fence_after();
                 issue_PV(ve, jj > 0);
@@ -594,9 +602,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd_kernel(const __grid_c
                         tmem_st32(tO + c * 32, rr);
                     }
                 }
+                // P (and any O rescale) of this warp's 32 rows is in TMEM: one arrival per warp
                 tmem_wait_st();
                 tc_fence_before();
-                mbar_arrive(bar(L::BAR_P + s));
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(L::BAR_P + s));
             }
             if (!ok) break;
             // ---- epilogue of the item.  Its TMEM reads of O precede this slot's next P
