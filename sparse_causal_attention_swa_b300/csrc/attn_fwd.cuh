@@ -17,7 +17,7 @@
 //   warp 8     TMA producer (lane 0): Q tiles once, then K / V tiles into an smem ring
 //   warp 9     TMEM owner; issues slot 0's MMAs: S = Q K^T and O += P V on tcgen05
 //   warp 10    issues slot 1's MMAs
-//   warp 11    idle
+//   warp 11    lane 0 writes the finished output tiles out with TMA stores
 // Each slot has its own issuing warp: tcgen05.mma issue blocks on a shallow queue, so a
 // single issuer cannot run ahead, and its barrier bookkeeping would idle the tensor core;
 // with two issuers one warp's bookkeeping overlaps the other's MMA stream.  The issuing
@@ -61,6 +61,7 @@ constexpr int NUM_THREADS = 384;
 constexpr int PRODUCER_WARP = 8;
 constexpr int MMA_WARP = 9;       // TMEM owner; issues the MMAs of slot 0
 constexpr int MMA_WARP_1 = 10;    // issues the MMAs of slot 1
+constexpr int STORE_WARP = 11;    // lane 0 issues the epilogue's TMA stores
 constexpr uint32_t TMEM_COLS = 512;
 constexpr float RESCALE_THRESHOLD = 8.0f;  // log2 units
 
@@ -98,10 +99,11 @@ struct SmemLayout {
     static constexpr int STAGES = (D == 128) ? 4 : 8;
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_RING = 2 * QBYTES;
-    // epilogue staging: per slot one 128-row x 64-column bf16 box (16 KiB, 128B-swizzled)
+    // epilogue staging: one output tile, 128 rows x D bf16 as D/64 boxes of 64 columns
+    // (16 KiB each, 128B-swizzled), used by one (item, slot) after another
     static constexpr int OFF_STAGE = OFF_RING + STAGES * EBYTES;
-    static constexpr int STAGE_HALF = BM * 64 * 2;
-    static constexpr int OFF_BAR = OFF_STAGE + 2 * STAGE_HALF;
+    static constexpr int STAGE_BOX = BM * 64 * 2;
+    static constexpr int OFF_BAR = OFF_STAGE + (D / 64) * STAGE_BOX;
     // barriers: q_full, ring_full[S], ring_empty[S], s_full[2], p_full[2], o_final[2],
     //           lsm_ready, drain
     static constexpr int BAR_Q = 0;
@@ -114,16 +116,16 @@ struct SmemLayout {
     static constexpr int BAR_DRAIN = BAR_L + 1;  // two: one per MMA issuer
     static constexpr int BAR_TURN = BAR_DRAIN + 2;  // two: "slot s may issue its next batch"
     static constexpr int BAR_QFREE = BAR_TURN + 2;  // the Q tiles may be replaced
-    static constexpr int BAR_BOXF = BAR_QFREE + 1;  // two: a slot's staging box is written
-    static constexpr int BAR_BOXE = BAR_BOXF + 2;   // two: its TMA store has read the box
-    static constexpr int NBARS = BAR_BOXE + 2;
+    static constexpr int BAR_BOXF = BAR_QFREE + 1;  // the staging tile is written
+    static constexpr int BAR_BOXE = BAR_BOXF + 1;   // its TMA stores have read it
+    static constexpr int NBARS = BAR_BOXE + 1;
     static constexpr int OFF_TMEM = OFF_BAR + NBARS * 8;
     static constexpr int OFF_ABORT = OFF_TMEM + 4;
     static constexpr int OFF_LSM = (OFF_ABORT + 4 + 15) / 16 * 16;
     static constexpr int END = OFF_LSM + BM * 4;
     static constexpr int BYTES = END + 1024;  // slack for aligning the base to 1024
     static_assert(BYTES <= 232448, "shared memory budget");
-    static_assert(EBYTES % 1024 == 0 && QBYTES % 1024 == 0 && STAGE_HALF % 1024 == 0,
+    static_assert(EBYTES % 1024 == 0 && QBYTES % 1024 == 0 && STAGE_BOX % 1024 == 0,
                   "1024-byte tile alignment");
 };
 
@@ -254,9 +256,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd_kernel(const __grid_c
             mbar_init(bar(L::BAR_S + s), 1);
             mbar_init(bar(L::BAR_P + s), 4);  // one arrival per softmax warp
             mbar_init(bar(L::BAR_O + s), 1);
-            mbar_init(bar(L::BAR_BOXF + s), 128);
-            mbar_init(bar(L::BAR_BOXE + s), 1);
         }
+        mbar_init(bar(L::BAR_BOXF), 128);
+        mbar_init(bar(L::BAR_BOXE), 1);
         mbar_init(bar(L::BAR_L), 128);
         mbar_init(bar(L::BAR_DRAIN), 1);
         mbar_init(bar(L::BAR_DRAIN + 1), 1);
@@ -498,7 +500,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd_kernel(const __grid_c
         const float sl2 = p.scale_log2;
         bool ok = true;
         uint32_t ns = 0;  // S phases consumed
-        uint32_t nbox = 0;  // staging boxes this slot has written
         int it = 0;
         for (int r = 0; r < n_rounds && ok; ++r) {
             const int item = item_of(r);
@@ -531,10 +532,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd_kernel(const __grid_c
                     a = lo_i - c0;
                     bnd = row - c0;
                 }
+                // Mask, on edge tiles only: columns outside [a, bnd] become -inf.  Usually only
+                // one side cuts the tile (the diagonal tile: t <= bnd; the window-start tile:
+                // t >= a), which needs one compare per element.
                 if (a > 0 || bnd < BN - 1) {
+                    if (a <= 0) {
 #pragma unroll
-                    for (int t = 0; t < BN; ++t)
-                        xr[t] = (t >= a && t <= bnd) ? xr[t] : __float_as_uint(-INFINITY);
+                        for (int t = 0; t < BN; ++t)
+                            xr[t] = (t <= bnd) ? xr[t] : __float_as_uint(-INFINITY);
+                    } else if (bnd >= BN - 1) {
+#pragma unroll
+                        for (int t = 0; t < BN; ++t)
+                            xr[t] = (t >= a) ? xr[t] : __float_as_uint(-INFINITY);
+                    } else {
+#pragma unroll
+                        for (int t = 0; t < BN; ++t)
+                            xr[t] = (t >= a && t <= bnd) ? xr[t] : __float_as_uint(-INFINITY);
+                    }
                 }
                 // row maximum: eight independent 3-input max chains, then a short tree
                 float mc[8];
@@ -631,63 +645,73 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd_kernel(const __grid_c
                     tc_fence_after();
                     inv_l2 = lsm[trow] * p.lambda;
                 }
-                // O / l (differential: O1 / l1 - lambda O2 / l2) to bf16, 64 columns at a time
-                // through this slot's staging box, written out by one TMA store per box;
-                // TMA drops the rows past N
+                // O / l (differential: O1 / l1 - lambda O2 / l2) to bf16 into the staging tile
+                // (128-byte box rows, 16-byte unit u stored at u ^ (row & 7)); the store warp
+                // writes it out with TMA, which drops the rows past N.  Uses of the staging
+                // tile alternate between the slots, item after item: use u waits until the
+                // stores of use u-1 have read it.
                 const uint32_t tO2 = tmem_base + lane_off + 384u;
-                const uint32_t stage = sbase + L::OFF_STAGE + (uint32_t)(s * L::STAGE_HALF);
-                const uint32_t srow = stage + (uint32_t)trow * 128u;
-                const bool store = wi.r0[s] < p.N;
-                const int mat = wi.b * p.Hq + wi.h[s];
-                for (int c64 = 0; c64 < D / 64 && ok; ++c64) {
-                    // the previous store from this box must have read it
-                    if (nbox > 0)
-                        ok = mbar_wait_bounded(bar(L::BAR_BOXE + s), (nbox - 1) & 1u, abort_flag,
-                                               lim);
-                    if (!ok) break;
+                const uint32_t use = (MODE == MODE_DIFF) ? (uint32_t)it : 2u * (uint32_t)it + (uint32_t)s;
+                if (use > 0)
+                    ok = mbar_wait_bounded(bar(L::BAR_BOXE), (use - 1) & 1u, abort_flag, lim);
+                if (!ok) break;
 #pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        uint32_t rr[32];
-                        tmem_ld32(tO + c64 * 64 + h * 32, rr);
-                        float y[32];
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t rr[32];
+                    tmem_ld32(tO + c * 32, rr);
+                    float y[32];
 #pragma unroll
-                        for (int t = 0; t < 32; ++t) y[t] = __uint_as_float(rr[t]) * inv_l;
-                        if (MODE == MODE_DIFF) {
-                            tmem_ld32(tO2 + c64 * 64 + h * 32, rr);
+                    for (int t = 0; t < 32; ++t) y[t] = __uint_as_float(rr[t]) * inv_l;
+                    if (MODE == MODE_DIFF) {
+                        tmem_ld32(tO2 + c * 32, rr);
 #pragma unroll
-                            for (int t = 0; t < 32; ++t) y[t] -= __uint_as_float(rr[t]) * inv_l2;
-                        }
-                        // four 16-byte units; unit u of a 128-byte row sits at u ^ (row & 7)
-#pragma unroll
-                        for (int v4 = 0; v4 < 4; ++v4) {
-                            const uint32_t u = (uint32_t)(h * 4 + v4);
-                            st_shared_v4(srow + ((u ^ (uint32_t)(trow & 7)) << 4),
-                                         pack_bf16x2(y[v4 * 8 + 0], y[v4 * 8 + 1]),
-                                         pack_bf16x2(y[v4 * 8 + 2], y[v4 * 8 + 3]),
-                                         pack_bf16x2(y[v4 * 8 + 4], y[v4 * 8 + 5]),
-                                         pack_bf16x2(y[v4 * 8 + 6], y[v4 * 8 + 7]));
-                        }
+                        for (int t = 0; t < 32; ++t) y[t] -= __uint_as_float(rr[t]) * inv_l2;
                     }
-                    fence_proxy_async_smem();
-                    mbar_arrive(bar(L::BAR_BOXF + s));
-                    if (trow == 0) {
-                        ok = mbar_wait_bounded(bar(L::BAR_BOXF + s), nbox & 1u, abort_flag, lim);
-                        if (ok && store) {
-                            tma_store_3d(&p.tm_out, stage, c64 * 64, wi.r0[s], mat);
-                            bulk_commit_group();
-                            bulk_wait_read_all();
-                        }
-                        mbar_arrive(bar(L::BAR_BOXE + s));
+                    const uint32_t brow = sbase + L::OFF_STAGE + (uint32_t)((c >> 1) * L::STAGE_BOX) +
+                                          (uint32_t)trow * 128u;
+#pragma unroll
+                    for (int v4 = 0; v4 < 4; ++v4) {
+                        const uint32_t u = (uint32_t)((c & 1) * 4 + v4);
+                        st_shared_v4(brow + ((u ^ (uint32_t)(trow & 7)) << 4),
+                                     pack_bf16x2(y[v4 * 8 + 0], y[v4 * 8 + 1]),
+                                     pack_bf16x2(y[v4 * 8 + 2], y[v4 * 8 + 3]),
+                                     pack_bf16x2(y[v4 * 8 + 4], y[v4 * 8 + 5]),
+                                     pack_bf16x2(y[v4 * 8 + 6], y[v4 * 8 + 7]));
                     }
-                    ++nbox;
                 }
+                fence_proxy_async_smem();
+                mbar_arrive(bar(L::BAR_BOXF));
             }
             if (!ok) break;
             ++it;
         }
-        if (trow == 0) bulk_wait_all();  // the output is written before the CTA exits
     } else {
-        setmaxnreg_dec<56>();  // idle warp of the TMA / MMA warpgroup
+        // ===================================== TMA stores of the epilogue (lane 0)
+        setmaxnreg_dec<56>();
+        if (lane == 0) {
+            bool ok = true;
+            uint32_t use = 0;
+            for (int r = 0; r < n_rounds && ok; ++r) {
+                const int item = item_of(r);
+                if (item >= p.n_items) continue;
+                const WorkItem wi = decode_item<MODE>(p, item);
+                constexpr int NOUT = (MODE == MODE_DIFF) ? 1 : 2;  // output tiles per item
+                for (int s = 0; s < NOUT && ok; ++s, ++use) {
+                    ok = mbar_wait_bounded(bar(L::BAR_BOXF), use & 1u, abort_flag, lim);
+                    if (!ok) break;
+                    if (wi.r0[s] < p.N) {
+                        for (int c = 0; c < D / 64; ++c)
+                            tma_store_3d(&p.tm_out, sbase + L::OFF_STAGE + c * L::STAGE_BOX, c * 64,
+                                         wi.r0[s], wi.b * p.Hq + wi.h[s]);
+                    }
+                    bulk_commit_group();
+                    bulk_wait_read_all();
+                    mbar_arrive(bar(L::BAR_BOXE));
+                }
+            }
+            bulk_wait_all();  // the output is written before the CTA exits
+        }
+        __syncwarp();
     }
 
     // ---- teardown
