@@ -18,6 +18,10 @@ Parity status per function (what pins it is listed in the tests):
   attn(kind="causal")  pinned: worked example (full causal 38/8), brute force.
   diff                 pinned: lambda = 0, (Q2, K2) = (Q1, K1), affinity in
                        lambda, brute force of the dense (A1 - lambda A2) V.
+  decode, cache_slot   pinned: the SWA note's W = 3 slot walk-through (§4.2),
+                       equality with row t of attn(kind="window") over the whole
+                       sequence when the cache was filled by rolling writes,
+                       W > t (full causal row), W = 1 (returns v_t).
 """
 from __future__ import annotations
 
@@ -73,6 +77,11 @@ def _load():
             lib.oracle_pair_count.argtypes = [ctypes.c_int, _I64, _I64, _I64]
             lib.oracle_mask_row.restype = ctypes.c_int
             lib.oracle_mask_row.argtypes = [ctypes.c_int, _I64, _I64, _I64, _I64, _P]
+            lib.oracle_decode.restype = ctypes.c_int
+            lib.oracle_decode.argtypes = [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _I64,
+                                          ctypes.c_double]
+            lib.oracle_cache_slot.restype = ctypes.c_int64
+            lib.oracle_cache_slot.argtypes = [_I64, _I64]
             lib.oracle_max_threads.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -160,6 +169,32 @@ def mask_row(N: int, W: int, i: int, kind: str = "window", stride: int = 0) -> n
     if rc != 0:
         raise ValueError("bad mask_row arguments")
     return a.astype(bool)
+
+
+def decode(q, kc, vc, pos, W: int, scale: float) -> np.ndarray:
+    """Decode against a rolling W-slot cache in fp64.  q: [B, Hq, d]; kc, vc: [B, Hkv, W, d];
+    pos: [B] absolute positions.  Returns [B, Hq, d]."""
+    lib = _load()
+    q64, k64, v64 = _f64(q), _f64(kc), _f64(vc)
+    B, Hq, d = q64.shape
+    Hkv = k64.shape[1]
+    if k64.shape[2] != W:
+        raise ValueError("cache slot count does not match W")
+    p = np.ascontiguousarray(pos, dtype=np.int64)
+    out = np.empty((B, Hq, d), dtype=np.float64)
+    rc = lib.oracle_decode(_ptr(q64), _ptr(k64), _ptr(v64), _ptr(p), _ptr(out), B, Hq, Hkv,
+                           int(W), d, float(scale))
+    if rc != 0:
+        raise ValueError(f"oracle_decode rejected its arguments (code {rc})")
+    return out
+
+
+def cache_slot(j: int, W: int) -> int:
+    """Cache slot that holds absolute position j (0-indexed) in a W-slot rolling cache."""
+    r = int(_load().oracle_cache_slot(int(j), int(W)))
+    if r < 0:
+        raise ValueError("bad cache_slot arguments")
+    return r
 
 
 def max_threads() -> int:

@@ -31,6 +31,9 @@
  *   4. out_i = sum_j a_j v_j.
  *   Differential ([AVpt] "Atenção Diferencial"): out_i = sum_j (a1_j - lambda a2_j) v_j
  *   with a1 from (q1, k1) and a2 from (q2, k2), both under the causal mask.
+ *   Decode against a rolling cache ([SWA] §4.2): the K, V of absolute position j sit in
+ *   cache slot j mod W (the note's 1-indexed slot (i-1) mod W); a query at position t reads
+ *   the positions max(0, t-W+1) .. t through their slots, steps 2-4 as above.
  *
  * Inputs are fp64 arrays in layout [B, H, N, d] (q: H = Hq, k and v: H = Hkv).
  * Output is fp64 [B, Hq, nrows, d] where nrows rows (a list, or all N) are computed.
@@ -235,6 +238,58 @@ int oracle_mask_row(int kind, int64_t N, int64_t W, int64_t stride, int64_t i, u
     free(M);
     return 0;
 }
+
+/*
+ * Decode against a rolling W-slot cache ([SWA] §4.2).  q: [B, Hq, d] (one query per
+ * sequence and head), kc, vc: [B, Hkv, W, d], pos: [B] absolute position of each query.
+ * The window of position t is j = max(0, t-W+1) .. t ([SWA] §3.1, 0-indexed); the key and
+ * value of position j are read from slot j mod W, where the rolling writes put them.
+ * out: [B, Hq, d].  Returns 0, or 2 on bad arguments.
+ */
+int oracle_decode(const double* q, const double* kc, const double* vc, const int64_t* pos,
+                  double* out, int64_t B, int64_t Hq, int64_t Hkv, int64_t W, int64_t d,
+                  double scale) {
+    if (check_shape(B, Hq, Hkv, W, d) || W < 1) return 2;
+    for (int64_t b = 0; b < B; ++b)
+        if (pos[b] < 0) return 2;
+    const int64_t g = Hq / Hkv;
+    double* z = (double*)malloc(sizeof(double) * (size_t)W);
+    for (int64_t b = 0; b < B; ++b) {
+        const int64_t t = pos[b];
+        const int64_t lo = t - W + 1 > 0 ? t - W + 1 : 0;
+        for (int64_t h = 0; h < Hq; ++h) {
+            const int64_t hk = h / g;
+            const double* qi = q + (b * Hq + h) * d;
+            const double* kh = kc + (b * Hkv + hk) * W * d;
+            const double* vh = vc + (b * Hkv + hk) * W * d;
+            double m = -INFINITY;
+            for (int64_t j = lo; j <= t; ++j) {  /* absolute positions of the window */
+                const double* kj = kh + (j % W) * d;
+                double dot = 0.0;
+                for (int64_t c = 0; c < d; ++c) dot += qi[c] * kj[c];
+                z[j - lo] = scale * dot;
+                if (z[j - lo] > m) m = z[j - lo];
+            }
+            double l = 0.0;
+            for (int64_t j = lo; j <= t; ++j) {
+                z[j - lo] = exp(z[j - lo] - m);
+                l += z[j - lo];
+            }
+            double* o = out + (b * Hq + h) * d;
+            for (int64_t c = 0; c < d; ++c) o[c] = 0.0;
+            for (int64_t j = lo; j <= t; ++j) {
+                const double a = z[j - lo] / l;
+                const double* vj = vh + (j % W) * d;
+                for (int64_t c = 0; c < d; ++c) o[c] += a * vj[c];
+            }
+        }
+    }
+    free(z);
+    return 0;
+}
+
+/* Slot of absolute position j in a W-slot rolling cache ([SWA] §4.2, 0-indexed). */
+int64_t oracle_cache_slot(int64_t j, int64_t W) { return (W < 1 || j < 0) ? -1 : j % W; }
 
 int oracle_max_threads(void) {
 #ifdef _OPENMP

@@ -50,6 +50,25 @@ def useful_flops(kind: str, B: int, Hq: int, N: int, d: int, W: int, stride: int
     raise ValueError(kind)
 
 
+def decode_keys(pos, W: int) -> int:
+    """Cache rows a decode step reads per (sequence, KV head): the window of position t holds
+    min(t + 1, W) keys (SWA note §3.1 and §4.2)."""
+    p = np.asarray(pos, dtype=np.int64)
+    return int(np.minimum(p + 1, W).sum())
+
+
+def decode_flops(pos, Hq: int, d: int, W: int) -> float:
+    """Useful FLOPs of a decode step: 4 d per (query head, window key)."""
+    return 4.0 * d * Hq * decode_keys(pos, W)
+
+
+def decode_bytes(pos, Hq: int, Hkv: int, d: int, W: int) -> int:
+    """HBM bytes a decode step must move: the K and V rows of every window once, the
+    queries read and the outputs written (bf16)."""
+    B = int(np.asarray(pos).size)
+    return 2 * Hkv * d * 2 * decode_keys(pos, W) + 2 * B * Hq * d * 2
+
+
 def algorithmic_bytes(kind: str, B: int, Hq: int, Hkv: int, N: int, d: int) -> int:
     """HBM bytes that every correct implementation must move: inputs read once, output written once (bf16)."""
     q = B * Hq * N * d * 2

@@ -25,7 +25,7 @@ class Workload:
     """One synthetic workload: the sizes of one call of the hot path."""
 
     name: str
-    kind: str  # "swa" | "strided" | "diff"
+    kind: str  # "swa" | "strided" | "diff" | "decode"
     B: int
     Hq: int
     Hkv: int
@@ -63,6 +63,11 @@ WORKLOADS = {
     # differential causal attention with an attention sink on key 0 of K1
     "diff": Workload("diff", "diff", 1, 16, 16, 8192, 64, 8192, lam=0.8, sink_shift=3.0,
                      seed_index=5),
+    # decode against a W-slot rolling KV cache, Mistral-7B heads: one new query per
+    # sequence, 32 sequences at positions drawn from [0, N); N = 4 W, so most windows
+    # are full (W cache rows) and some are still filling
+    "mistral_decode": Workload("mistral_decode", "decode", 32, 32, 8, 16384, 128, 4096,
+                               seed_index=6),
 }
 
 
@@ -94,12 +99,23 @@ def _normal_bf16(rng: np.random.Generator, shape, shift_row0: float = 0.0) -> np
 
 
 def tensor_names(kind: str) -> tuple[str, ...]:
+    if kind == "decode":
+        return ("q", "kc", "vc")
     return ("q1", "k1", "q2", "k2", "v") if kind == "diff" else ("q", "k", "v")
 
 
 def make_inputs(w: Workload, seed: int | None = None) -> dict[str, np.ndarray]:
     """Draw the workload's inputs as bf16 bit patterns (uint16), layout [B, H, N, d]."""
     rng = np.random.default_rng(w.seed if seed is None else seed)
+    if w.kind == "decode":
+        # q: [B, Hq, d]; the W-slot caches kc, vc: [B, Hkv, W, d] hold i.i.d. N(0, 1)
+        # entries (whatever history filled them); pos: [B] absolute query positions
+        return {
+            "q": f32_to_bf16_bits(rng.standard_normal(size=(w.B, w.Hq, w.d), dtype=np.float32)),
+            "kc": _normal_bf16(rng, (w.B, w.Hkv, w.W, w.d)),
+            "vc": _normal_bf16(rng, (w.B, w.Hkv, w.W, w.d)),
+            "pos": rng.integers(0, w.N, size=w.B, dtype=np.int64).astype(np.int32),
+        }
     qs = (w.B, w.Hq, w.N, w.d)
     ks = (w.B, w.Hkv, w.N, w.d)
     if w.kind == "diff":

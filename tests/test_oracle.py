@@ -356,3 +356,102 @@ def test_bf16_inputs_widen_exactly(oracle_mod):
     ref = oracle_mod.attn(swa_inputs.bf16_bits_to_f64(h), swa_inputs.bf16_bits_to_f64(h),
                           swa_inputs.bf16_bits_to_f64(h), 3, 0.5)
     assert np.array_equal(oracle_mod.attn(h, h, h, 3, 0.5), ref)
+
+
+# ------------------------------------------------------------------ decode, rolling cache
+def _rolling_fill(kseq, vseq, t, W):
+    """Write positions 0..t of a [B, H, T, d] sequence into W-slot caches, in order, the way
+    the SWA note's rolling cache does (§4.2): position j goes to slot cache_slot(j, W)."""
+    import oracle
+
+    B, H, _, d = kseq.shape
+    kc = np.full((B, H, W, d), np.nan)
+    vc = np.full((B, H, W, d), np.nan)
+    for j in range(t + 1):
+        sl = oracle.cache_slot(j, W)
+        kc[:, :, sl] = kseq[:, :, j]
+        vc[:, :, sl] = vseq[:, :, j]
+    return kc, vc
+
+
+def test_rolling_cache_walkthrough(oracle_mod):
+    fx = read_kv_fixture("swa_note_rolling_cache.txt")
+    W = int(fx["W"])
+    pos1 = [int(x) for x in fx["positions_1indexed"].split()]
+    assert [oracle_mod.cache_slot(p - 1, W) for p in pos1] == [int(x) for x in fx["slots"].split()]
+    held = {}
+    for p in range(1, 5):
+        held[oracle_mod.cache_slot(p - 1, W)] = p
+    assert [held[s] for s in range(W)] == [int(x) for x in fx["held_after_4"].split()]
+    # the window of position 4 is exactly what the cache holds after position 1 was overwritten
+    assert sorted(held.values()) == [int(x) for x in fx["window_of_4"].split()]
+    assert [int(x) for x in fx["window_of_4"].split()] == [
+        j + 1 for j in np.flatnonzero(oracle_mod.mask_row(6, W, 3))]
+
+
+@pytest.mark.parametrize("W", [1, 3, 7, 16])
+def test_decode_equals_window_row(oracle_mod, W):
+    rng = np.random.default_rng(40 + W)
+    B, Hq, Hkv, T, d = 2, 4, 2, 37, 8
+    q = rng.standard_normal((B, Hq, T, d))
+    k = rng.standard_normal((B, Hkv, T, d))
+    v = rng.standard_normal((B, Hkv, T, d))
+    full = oracle_mod.attn(q, k, v, W, 0.35, kind="window")
+    for t in (0, 1, W - 1, W, 20, T - 1):
+        if t < 0 or t >= T:
+            continue
+        kc, vc = _rolling_fill(k, v, t, W)
+        # slots never written (t < W - 1) hold NaN: the decode must not read them
+        kc = np.nan_to_num(kc, nan=1e300) if t >= W - 1 else kc
+        got = oracle_mod.decode(q[:, :, t], kc, vc, np.full(B, t), W, 0.35)
+        assert np.all(np.isfinite(got))
+        np.testing.assert_allclose(got, full[:, :, t], rtol=0, atol=1e-12)
+
+
+def test_decode_per_sequence_positions(oracle_mod):
+    rng = np.random.default_rng(50)
+    B, H, W, d = 3, 2, 5, 4
+    T = 12
+    k = rng.standard_normal((B, H, T, d))
+    v = rng.standard_normal((B, H, T, d))
+    q = rng.standard_normal((B, H, T, d))
+    pos = np.array([2, 11, 6])
+    kc = np.empty((B, H, W, d))
+    vc = np.empty((B, H, W, d))
+    for b in range(B):
+        kb, vb = _rolling_fill(k[b:b + 1], v[b:b + 1], int(pos[b]), W)
+        kc[b], vc[b] = np.nan_to_num(kb[0]), np.nan_to_num(vb[0])
+    got = oracle_mod.decode(q[np.arange(B), :, pos], kc, vc, pos, W, 0.5)
+    for b in range(B):
+        ref = oracle_mod.attn(q[b:b + 1], k[b:b + 1], v[b:b + 1], W, 0.5, kind="window",
+                              rows=[int(pos[b])])
+        np.testing.assert_allclose(got[b], ref[0, :, 0], rtol=0, atol=1e-12)
+
+
+def test_decode_w_beyond_position_is_causal_and_w1_is_v(oracle_mod):
+    rng = np.random.default_rng(51)
+    B, H, T, d = 1, 2, 9, 6
+    q = rng.standard_normal((B, H, T, d))
+    k = rng.standard_normal((B, H, T, d))
+    v = rng.standard_normal((B, H, T, d))
+    t = 5
+    W = 16  # larger than the history: every earlier position is in the window
+    kc, vc = _rolling_fill(k, v, t, W)
+    got = oracle_mod.decode(q[:, :, t], np.nan_to_num(kc), np.nan_to_num(vc), [t], W, 0.4)
+    ref = oracle_mod.attn(q, k, v, T, 0.4, kind="causal", rows=[t])
+    np.testing.assert_allclose(got, ref[:, :, 0], rtol=0, atol=1e-12)
+    kc1, vc1 = _rolling_fill(k, v, t, 1)
+    got1 = oracle_mod.decode(q[:, :, t], kc1, vc1, [t], 1, 0.4)
+    np.testing.assert_array_equal(got1, v[:, :, t])
+
+
+def test_decode_gqa_equals_repeated_kv(oracle_mod):
+    rng = np.random.default_rng(52)
+    B, Hq, Hkv, W, d = 2, 6, 2, 9, 4
+    q = rng.standard_normal((B, Hq, d))
+    kc = rng.standard_normal((B, Hkv, W, d))
+    vc = rng.standard_normal((B, Hkv, W, d))
+    pos = np.array([4, 30])
+    a = oracle_mod.decode(q, kc, vc, pos, W, 0.3)
+    b = oracle_mod.decode(q, np.repeat(kc, 3, axis=1), np.repeat(vc, 3, axis=1), pos, W, 0.3)
+    np.testing.assert_array_equal(a, b)
