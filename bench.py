@@ -40,6 +40,7 @@ from sparse_causal_attention_swa_b300 import flops as flopcount  # noqa: E402
 METRIC = "causal SWA fwd band-only TFLOP/s (Mistral shape, 1 B300) and % of BF16 peak"
 DEFAULT_WORKLOAD = "mistral_swa"
 KERNEL_SOURCES = ["sparse_causal_attention_swa_b300/csrc/attn_fwd.cuh",
+                  "sparse_causal_attention_swa_b300/csrc/decode.cuh",
                   "sparse_causal_attention_swa_b300/csrc/ptx.cuh",
                   "sparse_causal_attention_swa_b300/csrc/swa_api.cu"]
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
@@ -76,6 +77,10 @@ def load_peaks():
 
 
 def workload_units(w: swa_inputs.Workload):
+    if w.kind == "decode":
+        pos = swa_inputs.make_inputs(w)["pos"]
+        return (flopcount.decode_flops(pos, w.Hq, w.d, w.W),
+                flopcount.decode_bytes(pos, w.Hq, w.Hkv, w.d, w.W))
     fl = flopcount.useful_flops(w.kind, w.B, w.Hq, w.N, w.d, w.W, w.stride)
     by = flopcount.algorithmic_bytes(w.kind, w.B, w.Hq, w.Hkv, w.N, w.d)
     return fl, by
@@ -197,10 +202,30 @@ def oracle_inputs_f64(inp):
     return {n: swa_inputs.bf16_bits_to_f64(a) for n, a in inp.items()}
 
 
+def cpu_baseline_decode(w, inp, budget_s: float = 15.0):
+    """The oracle's decode on the host cores over a bounded sample of the sequences."""
+    import oracle
+
+    oracle.build()
+    t0 = time.perf_counter()
+    oracle.decode(inp["q"][:1], inp["kc"][:1], inp["vc"][:1], inp["pos"][:1], w.W, w.scale)
+    dt = max(time.perf_counter() - t0, 1e-3)
+    n = int(max(1, min(w.B, budget_s / dt)))
+    t0 = time.perf_counter()
+    oracle.decode(inp["q"][:n], inp["kc"][:n], inp["vc"][:n], inp["pos"][:n], w.W, w.scale)
+    dt = time.perf_counter() - t0
+    fl = flopcount.decode_flops(inp["pos"][:n], w.Hq, w.d, w.W)
+    return {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+            "sample": f"the first {n} of {w.B} sequences of {w.name} ({fl:.3e} useful FLOPs, "
+                      f"{dt:.1f} s, fp64, one thread)"}
+
+
 def cpu_baseline(w, inp, budget_s: float = 15.0):
     """Time the oracle as it stands on the host cores over a bounded row sample."""
     import oracle
 
+    if w.kind == "decode":
+        return cpu_baseline_decode(w, inp, budget_s)
     oracle.build()
     inp = oracle_inputs_f64(inp)
     probe = oracle_sample_rows(w, 4, seed=w.seed)
@@ -280,12 +305,30 @@ def workload_config(w, fl, flush=False):
 def to_device(inp, dev):
     import torch
 
-    return {n: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+    return {n: (torch.from_numpy(a).to(dev) if a.dtype == np.int32 else
+                torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev))
             for n, a in inp.items()}
 
 
+_WORKSPACES = {}
+
+
+def decode_workspace(pkg, w, dev):
+    import torch
+
+    key = (w.name, str(dev))
+    if key not in _WORKSPACES:
+        n = pkg.swa_decode_workspace_bytes(w.B, w.Hq, w.W, w.d)
+        _WORKSPACES[key] = torch.empty(n, dtype=torch.uint8, device=dev)
+    return _WORKSPACES[key]
+
+
 def launch(pkg, w, t, out, stream):
-    if w.kind == "swa":
+    if w.kind == "decode":
+        ws = decode_workspace(pkg, w, t["q"].device)
+        pkg.swa_decode_fwd(t["q"], t["kc"], t["vc"], t["pos"], out, w.B, w.Hq, w.Hkv, w.W, w.d,
+                           w.scale, ws, ws.numel(), stream)
+    elif w.kind == "swa":
         pkg.swa_attn_fwd(t["q"], t["k"], t["v"], out, w.B, w.Hq, w.Hkv, w.N, w.d, w.W, w.scale,
                          stream)
     elif w.kind == "strided":
@@ -361,7 +404,7 @@ def bench_workload(args, w, ws, rank, dev, want_cpu, want_e2e):
     achieved_tf = fl / (launch_ms * 1e-3) / 1e12
     tkey = TRAFFIC.get(w.name)
     traffic = tkey[0] if (tkey and tkey[1] == kernel_hash()) else None
-    tensor_bound = w.name not in ("swa_small",)
+    tensor_bound = w.name not in ("swa_small",) and w.kind != "decode"
     if tensor_bound:
         roofline = {"bound": "tensor", "achieved": achieved_tf, "peak": bf16_peak,
                     "unit": "TFLOP/s", "frac": achieved_tf / bf16_peak, "traffic": traffic,
@@ -374,6 +417,8 @@ def bench_workload(args, w, ws, rank, dev, want_cpu, want_e2e):
         roofline = {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
                     "frac": gbs / hbm_peak, "traffic": traffic,
                     "peak_source": f"{peak_src} hbm_gbs",
+                    "kernel": ("decode_split_kernel + decode_combine_kernel" if w.kind == "decode"
+                               else f"attn_fwd_kernel<{w.d},0>"),
                     "algorithmic_bytes_per_launch": algo_bytes}
 
     line = {
@@ -382,7 +427,8 @@ def bench_workload(args, w, ws, rank, dev, want_cpu, want_e2e):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic", "config": workload_config(w, fl, flush),
         "pct_of_bf16_peak": 100.0 * achieved_tf / bf16_peak,
-        "roofline": roofline, "gpu_launches": args.steps, "clocks": clk,
+        "roofline": roofline, "gpu_launches": args.steps * (2 if w.kind == "decode" else 1),
+        "clocks": clk,
     }
     if ws > 1:
         line["config"]["parallelism"] = f"replicas x{ws} (independent problems per rank)"

@@ -38,6 +38,8 @@
 #ifndef SWA_B300_H
 #define SWA_B300_H
 
+#include <stddef.h>
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -51,7 +53,7 @@ typedef enum swa_status {
     SWA_ERR_CUDA = 5,        /* a CUDA runtime / driver call failed (launch, attribute, map) */
     SWA_ERR_TIMEOUT = 6,     /* a kernel-side bounded wait ran out (read by swa_device_status) */
     SWA_ERR_VALUE = 7,       /* scale not finite and > 0, or lambda not finite */
-    SWA_ERR_TOO_LARGE = 8    /* the problem's tile list exceeds SWA_NOALLOC_TILE_CAPACITY */
+    SWA_ERR_TOO_LARGE = 8    /* a fixed capacity (the no-alloc tile list, a decode workspace) is too small */
 } swa_status;
 
 /* Capacity, in int entries (256 KiB), of the fixed device array that
@@ -108,6 +110,43 @@ int diff_attn_fwd(const void* q1, const void* k1, const void* q2, const void* k2
 int strided_attn_fwd_noalloc(const void* q, const void* k, const void* v, void* out, int B,
                              int Hq, int Hkv, int N, int d, int W, int stride, float scale,
                              void* stream);
+
+/*
+ * Decode step against a rolling W-slot KV cache ([SWA] §4.2; window of [SWA] §3.1).
+ * The cache of every (sequence b, KV head) holds W rows; the key and value of absolute
+ * position j live in slot j mod W (the note's 1-indexed slot (i-1) mod W), written there by
+ * swa_cache_append or by the caller.  For each sequence b the query at absolute position
+ * t = pos[b] reads the positions max(0, t-W+1) .. t, i.e. the slots 0 .. min(t, W-1):
+ *   out[b, h, :] = sum over those slots s of softmax_s(scale * q[b, h] . k_cache[b, h/g, s])
+ *                  * v_cache[b, h/g, s]          (g = Hq / Hkv)
+ * The slot order is not the time order; the softmax over the window does not depend on
+ * it (positional encodings must already be applied to the cached keys).
+ *   q, out:             bf16 [B, Hq, d] device, contiguous
+ *   k_cache, v_cache:   bf16 [B, Hkv, W, d] device, contiguous (only the window slots are
+ *                       read; the others may hold anything)
+ *   pos:                int32 [B] device (read by the kernels, so the call can be
+ *                       captured in a CUDA graph and replayed with new positions); a
+ *                       negative position gives a zero output row
+ *   workspace:          device scratch of at least swa_decode_workspace_bytes(B, Hq, W, d)
+ *                       bytes, 256-byte aligned, owned by the caller; calls that may run
+ *                       at the same time need separate workspaces
+ * Hq / Hkv must be at most 16; d 64 or 128.  Two kernels are launched on `stream`
+ * (split-K over the slots, then the combine).  Errors as for the other calls;
+ * SWA_ERR_TOO_LARGE if workspace_bytes is too small.
+ */
+size_t swa_decode_workspace_bytes(int B, int Hq, int W, int d);
+int swa_decode_fwd(const void* q, const void* k_cache, const void* v_cache, const int* pos,
+                   void* out, int B, int Hq, int Hkv, int W, int d, float scale, void* workspace,
+                   size_t workspace_bytes, void* stream);
+
+/*
+ * Rolling-cache update ([SWA] §4.2): writes k_new[b, h, :] and v_new[b, h, :] (bf16
+ * [B, Hkv, d] device) into slot pos[b] mod W of k_cache / v_cache (bf16 [B, Hkv, W, d]
+ * device), overwriting the position that left the window.  pos: int32 [B] device; a
+ * negative position writes nothing.  One kernel on `stream`.
+ */
+int swa_cache_append(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                     const int* pos, int B, int Hkv, int W, int d, void* stream);
 
 /* Human-readable name of a status code (static storage; never NULL). */
 const char* swa_status_string(int status);

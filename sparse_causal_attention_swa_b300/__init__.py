@@ -8,10 +8,11 @@ and streams.  There is no CPU fallback: if the library is missing, every call ra
 
 Low-level calls (pointers or tensors, explicit sizes, asynchronous on ``stream``):
     swa_attn_fwd, strided_attn_fwd, diff_attn_fwd, strided_attn_fwd_noalloc,
+    swa_decode_workspace_bytes, swa_decode_fwd, swa_cache_append,
     swa_status_string, swa_device_status, swa_watchdog_selftest
 Convenience wrappers on [B, H, N, d] bf16 tensors (allocate ``out``; CPU inputs are
 copied to the current CUDA device and the result copied back):
-    swa_attention, strided_attention, diff_attention
+    swa_attention, strided_attention, diff_attention, swa_decode
 """
 from __future__ import annotations
 
@@ -50,6 +51,13 @@ def load():
         lib.strided_attn_fwd_noalloc.restype = I
         lib.diff_attn_fwd.argtypes = [P, P, P, P, P, F, P, I, I, I, I, I, F, P]
         lib.diff_attn_fwd.restype = I
+        SZ = ctypes.c_size_t
+        lib.swa_decode_workspace_bytes.argtypes = [I, I, I, I]
+        lib.swa_decode_workspace_bytes.restype = SZ
+        lib.swa_decode_fwd.argtypes = [P, P, P, P, P, I, I, I, I, I, F, P, SZ, P]
+        lib.swa_decode_fwd.restype = I
+        lib.swa_cache_append.argtypes = [P, P, P, P, P, I, I, I, I, P]
+        lib.swa_cache_append.restype = I
         lib.swa_status_string.argtypes = [I]
         lib.swa_status_string.restype = ctypes.c_char_p
         lib.swa_device_status.argtypes = [P]
@@ -110,6 +118,22 @@ def diff_attn_fwd(q1, k1, q2, k2, v, lam, out, B, Hq, Hkv, N, d, scale, stream=N
     _check(load().diff_attn_fwd(_ptr(q1), _ptr(k1), _ptr(q2), _ptr(k2), _ptr(v), float(lam),
                                 _ptr(out), B, Hq, Hkv, N, d, float(scale), _stream(stream)),
            "diff_attn_fwd")
+
+
+def swa_decode_workspace_bytes(B, Hq, W, d) -> int:
+    return int(load().swa_decode_workspace_bytes(B, Hq, W, d))
+
+
+def swa_decode_fwd(q, k_cache, v_cache, pos, out, B, Hq, Hkv, W, d, scale, workspace,
+                   workspace_bytes, stream=None):
+    _check(load().swa_decode_fwd(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(pos), _ptr(out), B,
+                                 Hq, Hkv, W, d, float(scale), _ptr(workspace),
+                                 int(workspace_bytes), _stream(stream)), "swa_decode_fwd")
+
+
+def swa_cache_append(k_new, v_new, k_cache, v_cache, pos, B, Hkv, W, d, stream=None):
+    _check(load().swa_cache_append(_ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+                                   _ptr(pos), B, Hkv, W, d, _stream(stream)), "swa_cache_append")
 
 
 def swa_device_status(stream=None) -> int:
@@ -176,3 +200,23 @@ def diff_attention(q1, k1, q2, k2, v, lam: float, scale: float | None = None, ou
     diff_attn_fwd(a, b_, c, e, f, lam, o, B, Hq, b_.shape[1], N, d,
                   scale if scale is not None else 1.0 / math.sqrt(d))
     return _finish(o, q1)
+
+
+def swa_decode(q, k_cache, v_cache, pos, scale: float | None = None, out=None, workspace=None):
+    """One decode step against W-slot rolling caches: q [B, Hq, d], k_cache / v_cache
+    [B, Hkv, W, d] (bf16), pos [B] int32 absolute query positions.  Allocates the output and,
+    unless one is passed, the split workspace (a uint8 tensor)."""
+    import torch
+
+    (qd, kd, vd), dev = _prepare(q.unsqueeze(2), k_cache, v_cache)
+    qd = qd.squeeze(2)
+    pd = pos.to(dev, dtype=torch.int32).contiguous()
+    B, Hq, d = qd.shape
+    Hkv, W = kd.shape[1], kd.shape[2]
+    nbytes = swa_decode_workspace_bytes(B, Hq, W, d)
+    ws = workspace if workspace is not None else torch.empty(nbytes, dtype=torch.uint8,
+                                                             device=dev)
+    o = out if out is not None else torch.empty_like(qd)
+    swa_decode_fwd(qd, kd, vd, pd, o, B, Hq, Hkv, W, d,
+                   scale if scale is not None else 1.0 / math.sqrt(d), ws, ws.numel())
+    return _finish(o, q)

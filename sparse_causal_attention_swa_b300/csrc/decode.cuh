@@ -1,0 +1,265 @@
+// decode.cuh -- sm_103a decode step of causal sliding-window attention against a rolling
+// W-slot KV cache: one new query per sequence and head.
+//
+// What it computes ("SWA：滑动窗口注意力与跨层信息传递" §3.1 and §4.2): the key and value
+// of absolute position j sit in cache slot j mod W, so the window max(0, t-W+1) .. t of a
+// query at position t is exactly the set of slots 0 .. min(t, W-1).  The softmax over a
+// set does not depend on the order of its members (positions are already encoded in the
+// cached keys), so the kernel reads those slots in slot order.
+//
+// The step is bound by HBM: every window key and value row is read once and each feeds
+// Hq/Hkv queries only.  Split-K over the slots:
+//   decode_split_kernel<D, G>   grid (splits of 128 slots, B*Hkv), 128 threads.  TMA loads
+//                               the split's K and V rows (128B-swizzled boxes) into shared
+//                               memory; thread t scores slot t against the G query heads of
+//                               the KV head (fp32 dot products on the CUDA cores), the CTA
+//                               forms max / exp2 / sum per head, then thread t accumulates
+//                               output column t over the split's slots.  Writes the split's
+//                               un-normalised O, its maximum (log2 domain) and its sum l.
+//   decode_combine_kernel<D>    grid (B*Hq), D threads: rescales the splits to a common
+//                               maximum, out = sum O_s 2^(m_s - m) / sum l_s 2^(m_s - m).
+// Tensor cores are not used: with G <= 16 queries per KV head the products are far below
+// one MMA tile and the step is bound by HBM.
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include "ptx.cuh"
+
+namespace swa {
+
+constexpr int DEC_KS = 128;       // cache slots per split (one per thread)
+constexpr int DEC_THREADS = 128;
+
+struct DecParams {
+    CUtensorMap tm_kc;   // k cache, view [B*Hkv][W][d]
+    CUtensorMap tm_vc;   // v cache, view [B*Hkv][W][d]
+    const __nv_bfloat16* q;  // [B, Hq, d]
+    const int* pos;          // [B] absolute position of each sequence's query (device)
+    __nv_bfloat16* out;      // [B, Hq, d]
+    float* part_o;           // [B*Hq][nsplit][d] un-normalised split outputs
+    float* part_ml;          // [B*Hq][nsplit][2]: split maximum (log2 domain), split sum
+    int* status;
+    unsigned long long wait_limit_ns;
+    int B, Hq, Hkv, W, nsplit;
+    float scale_log2;        // scale * log2(e)
+};
+
+template <int D, int G>
+struct DecSmem {
+    static constexpr int KV_BYTES = DEC_KS * D * 2;   // one K or V split, D/64 boxes
+    static constexpr int OFF_K = 0;
+    static constexpr int OFF_V = KV_BYTES;
+    static constexpr int OFF_Q = 2 * KV_BYTES;           // fp32 [G][D]
+    static constexpr int OFF_P = OFF_Q + G * D * 4;      // fp32 [G][DEC_KS]
+    static constexpr int OFF_RED = OFF_P + G * DEC_KS * 4;  // fp32 [2][4 warps][G]
+    static constexpr int OFF_BAR = OFF_RED + 2 * 4 * G * 4;  // two mbarriers (K, V)
+    static constexpr int OFF_ABORT = OFF_BAR + 16;
+    static constexpr int END = OFF_ABORT + 4;
+    static constexpr int BYTES = END + 1024;  // slack for aligning the base to 1024
+    static_assert(KV_BYTES % 1024 == 0, "1024-byte box alignment");
+};
+
+// Shared-memory byte offset of element (row r, column c) of a 128-row tile stored as D/64
+// boxes of 64 columns, 128 bytes per row, 16-byte unit u of a row at u ^ (r & 7).
+__device__ __forceinline__ uint32_t swz_offset(int r, int c) {
+    const int box = c >> 6, u = (c & 63) >> 3, e = c & 7;
+    return (uint32_t)(box * (DEC_KS * 128) + r * 128 + ((u ^ (r & 7)) << 4) + e * 2);
+}
+
+template <int D, int G>
+__global__ void __launch_bounds__(DEC_THREADS) decode_split_kernel(const __grid_constant__ DecParams p) {
+    using L = DecSmem<D, G>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    float* qs = reinterpret_cast<float*>(smem + L::OFF_Q);
+    float* ps = reinterpret_cast<float*>(smem + L::OFF_P);
+    float* red = reinterpret_cast<float*>(smem + L::OFF_RED);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_ABORT);
+    const uint32_t bar_k = sbase + L::OFF_BAR, bar_v = bar_k + 8;
+
+    const int split = blockIdx.x;
+    const int bh = blockIdx.y;  // b * Hkv + hk
+    const int b = bh / p.Hkv, hk = bh % p.Hkv;
+    const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+    const int posb = p.pos[b];
+    const int nvalid = posb < 0 ? 0 : min(posb + 1, p.W);
+    const int k0 = split * DEC_KS;
+    if (k0 >= nvalid) return;  // the combine reads only the splits that hold window keys
+    const int nk = min(DEC_KS, nvalid - k0);
+
+    if (t == 0) {
+        mbar_init(bar_k, 1);
+        mbar_init(bar_v, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+        mbar_arrive_expect_tx(bar_k, L::KV_BYTES);
+        for (int c = 0; c < D / 64; ++c)
+            tma_load_3d(sbase + L::OFF_K + c * (DEC_KS * 128), &p.tm_kc, bar_k, c * 64, k0, bh);
+        mbar_arrive_expect_tx(bar_v, L::KV_BYTES);
+        for (int c = 0; c < D / 64; ++c)
+            tma_load_3d(sbase + L::OFF_V + c * (DEC_KS * 128), &p.tm_vc, bar_v, c * 64, k0, bh);
+    }
+    // the g <= G query heads of this KV head, widened to fp32 (rows h >= g are zero)
+    const int g = p.Hq / p.Hkv;
+    for (int i = t; i < G * D; i += DEC_THREADS) {
+        const int h = i / D, c = i % D;
+        qs[i] = h < g ? __bfloat162float(p.q[((size_t)b * p.Hq + (size_t)hk * g + h) * D + c])
+                      : 0.f;
+    }
+    __syncthreads();
+
+    // ---- scores of slot k0 + t against the G heads (log2 domain)
+    bool ok = mbar_wait_bounded(bar_k, 0, abort_flag, p.wait_limit_ns);
+    float s[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) s[h] = 0.f;
+    if (ok) {
+#pragma unroll 4
+        for (int u = 0; u < D / 8; ++u) {
+            const uint4 kv = *reinterpret_cast<const uint4*>(smem + L::OFF_K + swz_offset(t, u * 8));
+            const __nv_bfloat162* k2 = reinterpret_cast<const __nv_bfloat162*>(&kv);
+            float kf[8];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 f = __bfloat1622float2(k2[e]);
+                kf[2 * e] = f.x;
+                kf[2 * e + 1] = f.y;
+            }
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                const float4 qa = *reinterpret_cast<const float4*>(qs + h * D + u * 8);
+                const float4 qb = *reinterpret_cast<const float4*>(qs + h * D + u * 8 + 4);
+                s[h] += qa.x * kf[0] + qa.y * kf[1] + qa.z * kf[2] + qa.w * kf[3] +
+                        qb.x * kf[4] + qb.y * kf[5] + qb.z * kf[6] + qb.w * kf[7];
+            }
+        }
+    }
+    const bool valid = t < nk;
+#pragma unroll
+    for (int h = 0; h < G; ++h) s[h] = valid ? s[h] * p.scale_log2 : -INFINITY;
+
+    // ---- per head: maximum and sum over the split (warp shuffles, then the four warps)
+    float m[G], e[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+        float v = s[h];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+        if (lane == 0) red[warp * G + h] = v;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+        m[h] = fmaxf(fmaxf(red[h], red[G + h]), fmaxf(red[2 * G + h], red[3 * G + h]));
+        e[h] = valid ? exp2f(s[h] - m[h]) : 0.f;
+        ps[h * DEC_KS + t] = e[h];
+        float v = e[h];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        if (lane == 0) red[4 * G + warp * G + h] = v;
+    }
+    if (ok) ok = mbar_wait_bounded(bar_v, 0, abort_flag, p.wait_limit_ns);
+    __syncthreads();
+
+    // ---- output columns: thread t accumulates column t (D = 64: two halves of the slots)
+    constexpr int HALVES = DEC_THREADS / D;  // 1 (D = 128) or 2 (D = 64)
+    const int c = t % D, half = t / D;
+    float acc[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) acc[h] = 0.f;
+    if (ok) {
+        // only the slots that hold window keys: the others may hold anything, even NaN
+        const int kb = half * (DEC_KS / HALVES);
+        const int ke = min(kb + DEC_KS / HALVES, nk);
+        int k = kb;
+        for (; k + 4 <= ke; k += 4) {
+            float vv[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                vv[j] = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(
+                    smem + L::OFF_V + swz_offset(k + j, c)));
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                const float4 pw = *reinterpret_cast<const float4*>(ps + h * DEC_KS + k);
+                acc[h] += pw.x * vv[0] + pw.y * vv[1] + pw.z * vv[2] + pw.w * vv[3];
+            }
+        }
+        for (; k < ke; ++k) {
+            const float v1 = __bfloat162float(
+                *reinterpret_cast<const __nv_bfloat16*>(smem + L::OFF_V + swz_offset(k, c)));
+#pragma unroll
+            for (int h = 0; h < G; ++h) acc[h] += ps[h * DEC_KS + k] * v1;
+        }
+    }
+    if (HALVES == 2) {
+        __syncthreads();  // every thread is done with ps; reuse it for the second half
+        if (half == 1) {
+#pragma unroll
+            for (int h = 0; h < G; ++h) ps[h * D + c] = acc[h];
+        }
+        __syncthreads();
+        if (half == 0) {
+#pragma unroll
+            for (int h = 0; h < G; ++h) acc[h] += ps[h * D + c];
+        }
+    }
+    if (half == 0) {
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+            if (h >= g) break;
+            const size_t row = ((size_t)b * p.Hq + (size_t)hk * g + h) * p.nsplit + split;
+            p.part_o[row * D + c] = acc[h];
+            if (c == 0) {
+                const float l = red[4 * G + h] + red[4 * G + G + h] + red[4 * G + 2 * G + h] +
+                                red[4 * G + 3 * G + h];
+                p.part_ml[row * 2] = m[h];
+                p.part_ml[row * 2 + 1] = l;
+            }
+        }
+    }
+    if (t == 0 && *abort_flag) atomicExch(p.status, 6 /* SWA_ERR_TIMEOUT */);
+}
+
+template <int D>
+__global__ void __launch_bounds__(D) decode_combine_kernel(const __grid_constant__ DecParams p) {
+    const int bh = blockIdx.x;  // b * Hq + h
+    const int b = bh / p.Hq;
+    const int c = threadIdx.x;
+    const int posb = p.pos[b];
+    const int nvalid = posb < 0 ? 0 : min(posb + 1, p.W);
+    const int ns = (nvalid + DEC_KS - 1) / DEC_KS;
+    const float* ml = p.part_ml + (size_t)bh * p.nsplit * 2;
+    float mx = -INFINITY;
+    for (int s = 0; s < ns; ++s) mx = fmaxf(mx, ml[2 * s]);
+    float l = 0.f, o = 0.f;
+    for (int s = 0; s < ns; ++s) {
+        const float w = exp2f(ml[2 * s] - mx);
+        l += ml[2 * s + 1] * w;
+        o += p.part_o[((size_t)bh * p.nsplit + s) * D + c] * w;
+    }
+    p.out[(size_t)bh * D + c] = __float2bfloat16_rn(l > 0.f ? o / l : 0.f);
+}
+
+// Write one new K and V row per (sequence, KV head) into slot pos mod W of the caches.
+template <int D>
+__global__ void __launch_bounds__(D / 8) cache_append_kernel(const __nv_bfloat16* k_new,
+                                                             const __nv_bfloat16* v_new,
+                                                             __nv_bfloat16* k_cache,
+                                                             __nv_bfloat16* v_cache,
+                                                             const int* pos, int Hkv, int W) {
+    const int bh = blockIdx.x;  // b * Hkv + hk
+    const int b = bh / Hkv;
+    const int posb = pos[b];
+    if (posb < 0) return;
+    const size_t slot = (size_t)(posb % W);
+    const int u = threadIdx.x;  // 16-byte unit of the row
+    const uint4* ks = reinterpret_cast<const uint4*>(k_new + (size_t)bh * D) + u;
+    const uint4* vs = reinterpret_cast<const uint4*>(v_new + (size_t)bh * D) + u;
+    reinterpret_cast<uint4*>(k_cache + ((size_t)bh * W + slot) * D)[u] = *ks;
+    reinterpret_cast<uint4*>(v_cache + ((size_t)bh * W + slot) * D)[u] = *vs;
+}
+
+}  // namespace swa

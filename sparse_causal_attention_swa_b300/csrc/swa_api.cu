@@ -14,6 +14,7 @@
 #include <vector>
 
 #include "attn_fwd.cuh"
+#include "decode.cuh"
 #include "swa_b300.h"
 
 namespace {
@@ -34,6 +35,7 @@ struct DeviceState {
     int* status = nullptr;  // device address of g_status_word
     int num_sms = 0;
     bool attr_set[2][3] = {};
+    bool dec_attr_set[2][5] = {};
     // strided tile lists, keyed by (N, W, stride, rows per block)
     std::map<std::tuple<int, int, int, int>, int*> tile_lists;
 };
@@ -262,6 +264,55 @@ __global__ void noalloc_build_tiles_kernel(int* list, int N, int W, int stride, 
     }
 }
 
+// ---------------------------------------------------------------------------------------
+// Decode against a rolling cache
+// ---------------------------------------------------------------------------------------
+size_t decode_part_o_bytes(long long B, long long Hq, long long nsplit, int d) {
+    return (size_t)(B * Hq * nsplit * d) * sizeof(float);
+}
+
+size_t decode_workspace_bytes(long long B, long long Hq, long long W, int d) {
+    const long long nsplit = (W + swa::DEC_KS - 1) / swa::DEC_KS;
+    const size_t o = (decode_part_o_bytes(B, Hq, nsplit, d) + 255) / 256 * 256;
+    return o + (size_t)(B * Hq * nsplit * 2) * sizeof(float);
+}
+
+template <int D, int G>
+int launch_decode(const swa::DecParams& dp, int B, int Hkv, cudaStream_t stream, DeviceState& st,
+                  int gi) {
+    using L = swa::DecSmem<D, G>;
+    auto kern = swa::decode_split_kernel<D, G>;
+    bool& set = st.dec_attr_set[D == 128 ? 1 : 0][gi];
+    if (!set) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::BYTES) !=
+            cudaSuccess)
+            return SWA_ERR_CUDA;
+        set = true;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)dp.nsplit, (unsigned)(B * Hkv), 1);
+    cfg.blockDim = dim3(swa::DEC_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = L::BYTES;
+    cfg.stream = stream;
+    if (cudaLaunchKernelEx(&cfg, kern, dp) != cudaSuccess) return SWA_ERR_CUDA;
+    cudaLaunchConfig_t cc = {};
+    cc.gridDim = dim3((unsigned)(B * dp.Hq), 1, 1);
+    cc.blockDim = dim3((unsigned)D, 1, 1);
+    cc.stream = stream;
+    return cudaLaunchKernelEx(&cc, swa::decode_combine_kernel<D>, dp) == cudaSuccess ? SWA_OK
+                                                                                      : SWA_ERR_CUDA;
+}
+
+template <int D>
+int dispatch_decode(int g, const swa::DecParams& dp, int B, int Hkv, cudaStream_t stream,
+                    DeviceState& st) {
+    if (g <= 1) return launch_decode<D, 1>(dp, B, Hkv, stream, st, 0);
+    if (g <= 2) return launch_decode<D, 2>(dp, B, Hkv, stream, st, 1);
+    if (g <= 4) return launch_decode<D, 4>(dp, B, Hkv, stream, st, 2);
+    if (g <= 8) return launch_decode<D, 8>(dp, B, Hkv, stream, st, 3);
+    return launch_decode<D, 16>(dp, B, Hkv, stream, st, 4);
+}
+
 }  // namespace
 
 extern "C" {
@@ -276,7 +327,7 @@ const char* swa_status_string(int status) {
         case SWA_ERR_CUDA: return "CUDA runtime or driver error";
         case SWA_ERR_TIMEOUT: return "kernel watchdog: a bounded wait ran out";
         case SWA_ERR_VALUE: return "invalid scalar argument (scale must be finite and > 0; lambda finite)";
-        case SWA_ERR_TOO_LARGE: return "problem too large for the fixed tile-list capacity of the allocation-free call";
+        case SWA_ERR_TOO_LARGE: return "a fixed capacity is too small (the allocation-free tile list, or the decode workspace passed in)";
         default: return "unknown status";
     }
 }
@@ -447,6 +498,82 @@ int swa_watchdog_selftest(int limit_us, void* stream) {
     swa::watchdog_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
         st->status, (unsigned long long)limit_us * 1000ull);
     return cudaPeekAtLastError() == cudaSuccess ? SWA_OK : SWA_ERR_CUDA;
+}
+
+size_t swa_decode_workspace_bytes(int B, int Hq, int W, int d) {
+    if (B < 1 || Hq < 1 || W < 1 || (d != 64 && d != 128)) return 0;
+    return decode_workspace_bytes(B, Hq, W, d);
+}
+
+int swa_decode_fwd(const void* q, const void* k_cache, const void* v_cache, const int* pos,
+                   void* out, int B, int Hq, int Hkv, int W, int d, float scale, void* workspace,
+                   size_t workspace_bytes, void* stream) {
+    if (!q || !k_cache || !v_cache || !pos || !out || !workspace) return SWA_ERR_NULL;
+    if (B < 1 || Hq < 1 || Hkv < 1 || W < 1 || Hq % Hkv != 0) return SWA_ERR_SHAPE;
+    if ((long long)B * Hkv > 65535 || (long long)B * Hq > (1ll << 24) || W > (1 << 30))
+        return SWA_ERR_SHAPE;
+    if (d != 64 && d != 128) return SWA_ERR_UNSUPPORTED;
+    if (Hq / Hkv > 16) return SWA_ERR_UNSUPPORTED;
+    if (!std::isfinite(scale) || !(scale > 0.f)) return SWA_ERR_VALUE;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
+        (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0 ||
+        (reinterpret_cast<uintptr_t>(pos) & 3u) != 0)
+        return SWA_ERR_ALIGN;
+    if (workspace_bytes < decode_workspace_bytes(B, Hq, W, d)) return SWA_ERR_TOO_LARGE;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceState* st = nullptr;
+    int rc = current_device_state(&st);
+    if (rc) return rc;
+    swa::DecParams dp;
+    std::memset(&dp, 0, sizeof(dp));
+    const long long nsplit = (W + swa::DEC_KS - 1) / swa::DEC_KS;
+    if ((rc = make_map(&dp.tm_kc, k_cache, d, W, d, (long long)B * Hkv, (long long)W * d)))
+        return rc;
+    if ((rc = make_map(&dp.tm_vc, v_cache, d, W, d, (long long)B * Hkv, (long long)W * d)))
+        return rc;
+    dp.q = static_cast<const __nv_bfloat16*>(q);
+    dp.pos = pos;
+    dp.out = static_cast<__nv_bfloat16*>(out);
+    dp.part_o = static_cast<float*>(workspace);
+    dp.part_ml = reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                          (decode_part_o_bytes(B, Hq, nsplit, d) + 255) / 256 * 256);
+    dp.status = st->status;
+    dp.wait_limit_ns = kWaitLimitNs;
+    dp.B = B;
+    dp.Hq = Hq;
+    dp.Hkv = Hkv;
+    dp.W = W;
+    dp.nsplit = (int)nsplit;
+    dp.scale_log2 = scale * 1.4426950408889634f;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (d == 128) return dispatch_decode<128>(Hq / Hkv, dp, B, Hkv, s, *st);
+    return dispatch_decode<64>(Hq / Hkv, dp, B, Hkv, s, *st);
+}
+
+int swa_cache_append(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                     const int* pos, int B, int Hkv, int W, int d, void* stream) {
+    if (!k_new || !v_new || !k_cache || !v_cache || !pos) return SWA_ERR_NULL;
+    if (B < 1 || Hkv < 1 || W < 1 || (long long)B * Hkv > (1ll << 30)) return SWA_ERR_SHAPE;
+    if (d != 64 && d != 128) return SWA_ERR_UNSUPPORTED;
+    if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache) ||
+        (reinterpret_cast<uintptr_t>(pos) & 3u) != 0)
+        return SWA_ERR_ALIGN;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceState* st = nullptr;
+    int rc = current_device_state(&st);
+    if (rc) return rc;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(B * Hkv), 1, 1);
+    cfg.blockDim = dim3((unsigned)(d / 8), 1, 1);
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    const auto* kn = static_cast<const __nv_bfloat16*>(k_new);
+    const auto* vn = static_cast<const __nv_bfloat16*>(v_new);
+    auto* kc = static_cast<__nv_bfloat16*>(k_cache);
+    auto* vc = static_cast<__nv_bfloat16*>(v_cache);
+    cudaError_t e = (d == 128)
+                        ? cudaLaunchKernelEx(&cfg, swa::cache_append_kernel<128>, kn, vn, kc, vc, pos, Hkv, W)
+                        : cudaLaunchKernelEx(&cfg, swa::cache_append_kernel<64>, kn, vn, kc, vc, pos, Hkv, W);
+    return e == cudaSuccess ? SWA_OK : SWA_ERR_CUDA;
 }
 
 }  // extern "C"

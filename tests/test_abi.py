@@ -15,7 +15,7 @@ HEADER = os.path.join(ROOT, "include", "swa_b300.h")
 def declared_functions():
     src = open(HEADER, encoding="utf-8").read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"^\s*(?:const\s+)?(?:int|char\s*\*|const char\s*\*|void)\s*\*?\s*"
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?(?:int|size_t|char\s*\*|const char\s*\*|void)\s*\*?\s*"
                                  r"([a-z_][a-z0-9_]*)\s*\(", src, flags=re.M)))
 
 
