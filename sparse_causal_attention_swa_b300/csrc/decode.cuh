@@ -9,13 +9,15 @@
 //
 // The step is bound by HBM: every window key and value row is read once and each feeds
 // Hq/Hkv queries only.  Split-K over the slots:
-//   decode_split_kernel<D, G>   grid (splits of 128 slots, B*Hkv), 128 threads.  TMA loads
-//                               the split's K and V rows (128B-swizzled boxes) into shared
-//                               memory; thread t scores slot t against the G query heads of
-//                               the KV head (fp32 dot products on the CUDA cores), the CTA
-//                               forms max / exp2 / sum per head, then thread t accumulates
-//                               output column t over the split's slots.  Writes the split's
-//                               un-normalised O, its maximum (log2 domain) and its sum l.
+//   decode_split_kernel<D, G>   grid (splits of DEC_KS slots, B*Hkv), DEC_KS threads.  TMA
+//                               loads the split's K and V rows (128B-swizzled boxes) into
+//                               shared memory; thread t scores slot t against the G query
+//                               heads of the KV head (packed fp32x2 products on the CUDA
+//                               cores), the CTA forms max / exp2 / sum per head, then warp w
+//                               accumulates the output columns over slots 32w .. 32w+31
+//                               (lane l: CPL adjacent columns) and the warps' sums are added.
+//                               Writes the split's un-normalised O, its maximum (log2
+//                               domain) and its sum l.
 //   decode_combine_kernel<D>    grid (B*Hq), D threads: rescales the splits to a common
 //                               maximum, out = sum O_s 2^(m_s - m) / sum l_s 2^(m_s - m).
 // Tensor cores are not used: with G <= 16 queries per KV head the products are far below
@@ -28,8 +30,12 @@
 
 namespace swa {
 
-constexpr int DEC_KS = 128;       // cache slots per split (one per thread)
-constexpr int DEC_THREADS = 128;
+#ifndef SWA_DEC_KS
+#define SWA_DEC_KS 128
+#endif
+constexpr int DEC_KS = SWA_DEC_KS;   // cache slots per split, one thread per slot
+constexpr int DEC_THREADS = DEC_KS;
+constexpr int DEC_WARPS = DEC_KS / 32;
 
 struct DecParams {
     CUtensorMap tm_kc;   // k cache, view [B*Hkv][W][d]
@@ -50,21 +56,27 @@ struct DecSmem {
     static constexpr int KV_BYTES = DEC_KS * D * 2;   // one K or V split, D/64 boxes
     static constexpr int OFF_K = 0;
     static constexpr int OFF_V = KV_BYTES;
-    static constexpr int OFF_Q = 2 * KV_BYTES;           // fp32 [G][D]
-    static constexpr int OFF_P = OFF_Q + G * D * 4;      // fp32 [G][DEC_KS]
-    static constexpr int OFF_RED = OFF_P + G * DEC_KS * 4;  // fp32 [2][4 warps][G]
-    static constexpr int OFF_BAR = OFF_RED + 2 * 4 * G * 4;  // two mbarriers (K, V)
+    static constexpr int OFF_Q = 2 * KV_BYTES;                 // fp32 [G][D]
+    static constexpr int OFF_P = OFF_Q + G * D * 4;            // fp32 [G][DEC_KS]
+    static constexpr int OFF_RED = OFF_P + G * DEC_KS * 4;     // fp32 [2][DEC_WARPS][G]
+    static constexpr int OFF_BAR = OFF_RED + 2 * DEC_WARPS * G * 4;  // two mbarriers (K, V)
     static constexpr int OFF_ABORT = OFF_BAR + 16;
     static constexpr int END = OFF_ABORT + 4;
     static constexpr int BYTES = END + 1024;  // slack for aligning the base to 1024
     static_assert(KV_BYTES % 1024 == 0, "1024-byte box alignment");
+    static_assert(DEC_WARPS * G * D * 4 <= 2 * KV_BYTES, "the cross-warp sums fit in the tiles");
 };
 
-// Shared-memory byte offset of element (row r, column c) of a 128-row tile stored as D/64
+// Shared-memory byte offset of element (row r, column c) of a DEC_KS-row tile stored as D/64
 // boxes of 64 columns, 128 bytes per row, 16-byte unit u of a row at u ^ (r & 7).
 __device__ __forceinline__ uint32_t swz_offset(int r, int c) {
     const int box = c >> 6, u = (c & 63) >> 3, e = c & 7;
     return (uint32_t)(box * (DEC_KS * 128) + r * 128 + ((u ^ (r & 7)) << 4) + e * 2);
+}
+
+__device__ __forceinline__ uint64_t bf16x2_to_f32x2(uint32_t w) {
+    // the bf16 bits are the high half of the fp32 bits
+    return f32x2_pack(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
 }
 
 template <int D, int G>
@@ -104,45 +116,59 @@ __global__ void __launch_bounds__(DEC_THREADS) decode_split_kernel(const __grid_
     }
     // the g <= G query heads of this KV head, widened to fp32 (rows h >= g are zero)
     const int g = p.Hq / p.Hkv;
-    for (int i = t; i < G * D; i += DEC_THREADS) {
-        const int h = i / D, c = i % D;
-        qs[i] = h < g ? __bfloat162float(p.q[((size_t)b * p.Hq + (size_t)hk * g + h) * D + c])
-                      : 0.f;
+    for (int i = t; i < G * (D / 8); i += DEC_THREADS) {
+        const int h = i / (D / 8), u = i % (D / 8);
+        uint4 raw = make_uint4(0u, 0u, 0u, 0u);
+        if (h < g)
+            raw = *reinterpret_cast<const uint4*>(p.q + ((size_t)b * p.Hq + (size_t)hk * g + h) * D +
+                                                  u * 8);
+        const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
+        float4* dst = reinterpret_cast<float4*>(qs + h * D + u * 8);
+        dst[0] = make_float4(__uint_as_float(w4[0] << 16), __uint_as_float(w4[0] & 0xffff0000u),
+                             __uint_as_float(w4[1] << 16), __uint_as_float(w4[1] & 0xffff0000u));
+        dst[1] = make_float4(__uint_as_float(w4[2] << 16), __uint_as_float(w4[2] & 0xffff0000u),
+                             __uint_as_float(w4[3] << 16), __uint_as_float(w4[3] & 0xffff0000u));
     }
     __syncthreads();
 
-    // ---- scores of slot k0 + t against the G heads (log2 domain)
+    // ---- scores of slot k0 + t against the G heads (log2 domain); two packed partial sums
+    // per head keep the dependent chains short
     bool ok = mbar_wait_bounded(bar_k, 0, abort_flag, p.wait_limit_ns);
     float s[G];
+    {
+        uint64_t sa[G], sb[G];
 #pragma unroll
-    for (int h = 0; h < G; ++h) s[h] = 0.f;
-    if (ok) {
+        for (int h = 0; h < G; ++h) sa[h] = sb[h] = 0ull;
+        if (ok) {
 #pragma unroll 4
-        for (int u = 0; u < D / 8; ++u) {
-            const uint4 kv = *reinterpret_cast<const uint4*>(smem + L::OFF_K + swz_offset(t, u * 8));
-            const __nv_bfloat162* k2 = reinterpret_cast<const __nv_bfloat162*>(&kv);
-            float kf[8];
+            for (int u = 0; u < D / 8; ++u) {
+                const uint4 kv = *reinterpret_cast<const uint4*>(smem + L::OFF_K + swz_offset(t, u * 8));
+                const uint64_t k0p = bf16x2_to_f32x2(kv.x), k1p = bf16x2_to_f32x2(kv.y);
+                const uint64_t k2p = bf16x2_to_f32x2(kv.z), k3p = bf16x2_to_f32x2(kv.w);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float2 f = __bfloat1622float2(k2[e]);
-                kf[2 * e] = f.x;
-                kf[2 * e + 1] = f.y;
+                for (int h = 0; h < G; ++h) {
+                    const uint4 qa = *reinterpret_cast<const uint4*>(qs + h * D + u * 8);
+                    const uint4 qb = *reinterpret_cast<const uint4*>(qs + h * D + u * 8 + 4);
+                    sa[h] = f32x2_fma(k0p, (uint64_t)qa.x | ((uint64_t)qa.y << 32), sa[h]);
+                    sb[h] = f32x2_fma(k1p, (uint64_t)qa.z | ((uint64_t)qa.w << 32), sb[h]);
+                    sa[h] = f32x2_fma(k2p, (uint64_t)qb.x | ((uint64_t)qb.y << 32), sa[h]);
+                    sb[h] = f32x2_fma(k3p, (uint64_t)qb.z | ((uint64_t)qb.w << 32), sb[h]);
+                }
             }
+        }
 #pragma unroll
-            for (int h = 0; h < G; ++h) {
-                const float4 qa = *reinterpret_cast<const float4*>(qs + h * D + u * 8);
-                const float4 qb = *reinterpret_cast<const float4*>(qs + h * D + u * 8 + 4);
-                s[h] += qa.x * kf[0] + qa.y * kf[1] + qa.z * kf[2] + qa.w * kf[3] +
-                        qb.x * kf[4] + qb.y * kf[5] + qb.z * kf[6] + qb.w * kf[7];
-            }
+        for (int h = 0; h < G; ++h) {
+            float a0, a1, b0, b1;
+            f32x2_unpack(sa[h], a0, a1);
+            f32x2_unpack(sb[h], b0, b1);
+            s[h] = (a0 + a1) + (b0 + b1);
         }
     }
     const bool valid = t < nk;
 #pragma unroll
     for (int h = 0; h < G; ++h) s[h] = valid ? s[h] * p.scale_log2 : -INFINITY;
 
-    // ---- per head: maximum and sum over the split (warp shuffles, then the four warps)
-    float m[G], e[G];
+    // ---- per head: maximum and sum over the split (warp shuffles, then the warps)
 #pragma unroll
     for (int h = 0; h < G; ++h) {
         float v = s[h];
@@ -153,71 +179,106 @@ __global__ void __launch_bounds__(DEC_THREADS) decode_split_kernel(const __grid_
     __syncthreads();
 #pragma unroll
     for (int h = 0; h < G; ++h) {
-        m[h] = fmaxf(fmaxf(red[h], red[G + h]), fmaxf(red[2 * G + h], red[3 * G + h]));
-        e[h] = valid ? exp2f(s[h] - m[h]) : 0.f;
-        ps[h * DEC_KS + t] = e[h];
-        float v = e[h];
+        float mh = red[h];
+#pragma unroll
+        for (int w = 1; w < DEC_WARPS; ++w) mh = fmaxf(mh, red[w * G + h]);
+        const float e = valid ? exp2f(s[h] - mh) : 0.f;
+        ps[h * DEC_KS + t] = e;
+        float v = e;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-        if (lane == 0) red[4 * G + warp * G + h] = v;
+        if (lane == 0) red[DEC_WARPS * G + warp * G + h] = v;
     }
     if (ok) ok = mbar_wait_bounded(bar_v, 0, abort_flag, p.wait_limit_ns);
     __syncthreads();
 
-    // ---- output columns: thread t accumulates column t (D = 64: two halves of the slots)
-    constexpr int HALVES = DEC_THREADS / D;  // 1 (D = 128) or 2 (D = 64)
-    const int c = t % D, half = t / D;
-    float acc[G];
+    // ---- output columns: warp w takes the split's slots 32w .. 32w+31 and lane l the
+    // columns CPL*l .. CPL*l+CPL-1 (one 8- or 4-byte shared load of a V row per slot); the
+    // warps' partial sums then meet in shared memory (over the K and V tiles)
+    constexpr int CPL = D / 32;  // columns per lane: 4 (D = 128) or 2 (D = 64)
+    uint64_t acc[G][CPL / 2];
 #pragma unroll
-    for (int h = 0; h < G; ++h) acc[h] = 0.f;
+    for (int h = 0; h < G; ++h)
+#pragma unroll
+        for (int j = 0; j < CPL / 2; ++j) acc[h][j] = 0ull;
     if (ok) {
         // only the slots that hold window keys: the others may hold anything, even NaN
-        const int kb = half * (DEC_KS / HALVES);
-        const int ke = min(kb + DEC_KS / HALVES, nk);
+        const int kb = warp * 32, ke = min(kb + 32, nk);
+        const int c0 = lane * CPL;
         int k = kb;
         for (; k + 4 <= ke; k += 4) {
-            float vv[4];
+            uint64_t v2[4][CPL / 2];
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-                vv[j] = __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(
-                    smem + L::OFF_V + swz_offset(k + j, c)));
+            for (int j = 0; j < 4; ++j) {
+                const uint8_t* src = smem + L::OFF_V + swz_offset(k + j, c0);
+                if (CPL == 4) {
+                    const uint2 u2 = *reinterpret_cast<const uint2*>(src);
+                    v2[j][0] = bf16x2_to_f32x2(u2.x);
+                    v2[j][CPL / 2 - 1] = bf16x2_to_f32x2(u2.y);
+                } else {
+                    v2[j][0] = bf16x2_to_f32x2(*reinterpret_cast<const uint32_t*>(src));
+                }
+            }
 #pragma unroll
             for (int h = 0; h < G; ++h) {
                 const float4 pw = *reinterpret_cast<const float4*>(ps + h * DEC_KS + k);
-                acc[h] += pw.x * vv[0] + pw.y * vv[1] + pw.z * vv[2] + pw.w * vv[3];
+                const float pj[4] = {pw.x, pw.y, pw.z, pw.w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint64_t pp = f32x2_pack(pj[j], pj[j]);
+#pragma unroll
+                    for (int c = 0; c < CPL / 2; ++c) acc[h][c] = f32x2_fma(pp, v2[j][c], acc[h][c]);
+                }
             }
         }
         for (; k < ke; ++k) {
-            const float v1 = __bfloat162float(
-                *reinterpret_cast<const __nv_bfloat16*>(smem + L::OFF_V + swz_offset(k, c)));
-#pragma unroll
-            for (int h = 0; h < G; ++h) acc[h] += ps[h * DEC_KS + k] * v1;
-        }
-    }
-    if (HALVES == 2) {
-        __syncthreads();  // every thread is done with ps; reuse it for the second half
-        if (half == 1) {
-#pragma unroll
-            for (int h = 0; h < G; ++h) ps[h * D + c] = acc[h];
-        }
-        __syncthreads();
-        if (half == 0) {
-#pragma unroll
-            for (int h = 0; h < G; ++h) acc[h] += ps[h * D + c];
-        }
-    }
-    if (half == 0) {
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-            if (h >= g) break;
-            const size_t row = ((size_t)b * p.Hq + (size_t)hk * g + h) * p.nsplit + split;
-            p.part_o[row * D + c] = acc[h];
-            if (c == 0) {
-                const float l = red[4 * G + h] + red[4 * G + G + h] + red[4 * G + 2 * G + h] +
-                                red[4 * G + 3 * G + h];
-                p.part_ml[row * 2] = m[h];
-                p.part_ml[row * 2 + 1] = l;
+            const uint8_t* src = smem + L::OFF_V + swz_offset(k, c0);
+            uint64_t v2[CPL / 2];
+            if (CPL == 4) {
+                const uint2 u2 = *reinterpret_cast<const uint2*>(src);
+                v2[0] = bf16x2_to_f32x2(u2.x);
+                v2[CPL / 2 - 1] = bf16x2_to_f32x2(u2.y);
+            } else {
+                v2[0] = bf16x2_to_f32x2(*reinterpret_cast<const uint32_t*>(src));
             }
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                const uint64_t pp = f32x2_pack(ps[h * DEC_KS + k], ps[h * DEC_KS + k]);
+#pragma unroll
+                for (int c = 0; c < CPL / 2; ++c) acc[h][c] = f32x2_fma(pp, v2[c], acc[h][c]);
+            }
+        }
+    }
+    // warps -> one: partial sums through shared memory (over the K and V tiles)
+    float* xs = reinterpret_cast<float*>(smem + L::OFF_K);  // [DEC_WARPS][G][D]
+    __syncthreads();  // every thread is done reading the K and V tiles
+#pragma unroll
+    for (int h = 0; h < G; ++h)
+#pragma unroll
+        for (int c = 0; c < CPL / 2; ++c) {
+            float lo, hi;
+            f32x2_unpack(acc[h][c], lo, hi);
+            xs[(warp * G + h) * D + lane * CPL + 2 * c] = lo;
+            xs[(warp * G + h) * D + lane * CPL + 2 * c + 1] = hi;
+        }
+    __syncthreads();
+    for (int i = t; i < G * D; i += DEC_THREADS) {
+        const int h = i / D, c = i % D;
+        if (h >= g) break;
+        float o = 0.f;
+#pragma unroll
+        for (int w = 0; w < DEC_WARPS; ++w) o += xs[(w * G + h) * D + c];
+        const size_t row = ((size_t)b * p.Hq + (size_t)hk * g + h) * p.nsplit + split;
+        p.part_o[row * D + c] = o;
+        if (c == 0) {
+            float l = 0.f, mh = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < DEC_WARPS; ++w) {
+                l += red[DEC_WARPS * G + w * G + h];
+                mh = fmaxf(mh, red[w * G + h]);
+            }
+            p.part_ml[row * 2] = mh;
+            p.part_ml[row * 2 + 1] = l;
         }
     }
     if (t == 0 && *abort_flag) atomicExch(p.status, 6 /* SWA_ERR_TIMEOUT */);

@@ -81,12 +81,12 @@ int current_device_state(DeviceState** out) {
 
 // 3-D view [nmat][rows][d] of a bf16 tensor; consecutive rows are `row_stride` elements
 // apart and consecutive matrices (heads) `mat_stride` elements apart.  The box is
-// 64 columns (128 bytes, one swizzle span) x 128 rows x 1 matrix, 128-byte swizzled.
+// 64 columns (128 bytes, one swizzle span) x box_rows rows x 1 matrix, 128-byte swizzled.
 int make_map(CUtensorMap* m, const void* base, int d, long long rows, long long row_stride,
-             long long nmat, long long mat_stride) {
+             long long nmat, long long mat_stride, int box_rows = 128) {
     cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)rows, (cuuint64_t)nmat};
     cuuint64_t strides[2] = {(cuuint64_t)row_stride * 2, (cuuint64_t)mat_stride * 2};
-    cuuint32_t box[3] = {64, 128, 1};
+    cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -527,9 +527,11 @@ int swa_decode_fwd(const void* q, const void* k_cache, const void* v_cache, cons
     swa::DecParams dp;
     std::memset(&dp, 0, sizeof(dp));
     const long long nsplit = (W + swa::DEC_KS - 1) / swa::DEC_KS;
-    if ((rc = make_map(&dp.tm_kc, k_cache, d, W, d, (long long)B * Hkv, (long long)W * d)))
+    if ((rc = make_map(&dp.tm_kc, k_cache, d, W, d, (long long)B * Hkv, (long long)W * d,
+                       swa::DEC_KS)))
         return rc;
-    if ((rc = make_map(&dp.tm_vc, v_cache, d, W, d, (long long)B * Hkv, (long long)W * d)))
+    if ((rc = make_map(&dp.tm_vc, v_cache, d, W, d, (long long)B * Hkv, (long long)W * d,
+                       swa::DEC_KS)))
         return rc;
     dp.q = static_cast<const __nv_bfloat16*>(q);
     dp.pos = pos;
