@@ -110,8 +110,8 @@ struct SmemLayout {
     static constexpr int BAR_FULL = 1;
     static constexpr int BAR_EMPTY = 1 + STAGES;
     static constexpr int BAR_S = 1 + 2 * STAGES;
-    static constexpr int BAR_P = BAR_S + 2;
-    static constexpr int BAR_O = BAR_P + 2;
+    static constexpr int BAR_P = BAR_S + 2;  // four [slot][half]: half of P is in TMEM
+    static constexpr int BAR_O = BAR_P + 4;
     static constexpr int BAR_L = BAR_O + 2;
     static constexpr int BAR_DRAIN = BAR_L + 1;  // two: one per MMA issuer
     static constexpr int BAR_TURN = BAR_DRAIN + 2;  // two: "slot s may issue its next batch"
@@ -254,7 +254,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd_kernel(const __grid_c
         }
         for (int s = 0; s < 2; ++s) {
             mbar_init(bar(L::BAR_S + s), 1);
-            mbar_init(bar(L::BAR_P + s), 4);  // one arrival per softmax warp
+            mbar_init(bar(L::BAR_P + 2 * s), 4);  // one arrival per softmax warp
+            mbar_init(bar(L::BAR_P + 2 * s + 1), 4);
             mbar_init(bar(L::BAR_O + s), 1);
         }
         mbar_init(bar(L::BAR_BOXF), 128);
@@ -385,12 +386,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd_kernel(const __grid_c
                 mma_ss_elect(tS, aq + offq, bk + offk, ID_S, k > 0 ? 1u : 0u);
             }
         };
-        auto issue_PV = [&](int entry, bool acc) {
+        // O += P V over one half of the tile's keys (k-steps 4 half .. 4 half + 3)
+        auto issue_PV = [&](int entry, int half, bool acc) {
             const uint64_t bv = dv0 + (uint64_t)(entry * (L::EBYTES >> 4));
 #pragma unroll
-            for (int k = 0; k < BN / 16; ++k)
+            for (int kk = 0; kk < BN / 32; ++kk) {
+                const int k = half * (BN / 32) + kk;
                 mma_ts_elect(tO, tS + (uint32_t)(k * 8), bv + (uint64_t)((k * 2048) >> 4), ID_O,
                              (acc || k > 0) ? 1u : 0u);
+            }
         };
         // a bounded wait whose outcome every lane agrees on
         auto wait = [&](uint32_t b, uint32_t parity) -> bool {
@@ -452,18 +456,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd_kernel(const __grid_c
                 }
                 // Both the slot's P and its turn are needed; wait first on the one that
                 // usually completes first (slot 0: its turn, slot 1: its P), so the second
-                // wait's latency is the only one left on the critical path.
+                // wait's latency is the only one left on the critical path.  P arrives in two
+                // halves; the first half's products start while the softmax finishes the
+                // second.
                 if (s == 0) {
                     if (ok) ok = my_turn();
-                    if (ok) ok = wait(bar(L::BAR_P + s), np & 1u);
+                    if (ok) ok = wait(bar(L::BAR_P + 2 * s), np & 1u);
                 } else {
-                    if (ok) ok = wait(bar(L::BAR_P + s), np & 1u);
+                    if (ok) ok = wait(bar(L::BAR_P + 2 * s), np & 1u);
                     if (ok) ok = my_turn();
                 }
+                if (!ok) break;
+                tc_fence_after();
+                issue_PV(ve, 0, jj > 0);
+                ok = wait(bar(L::BAR_P + 2 * s + 1), np & 1u);
                 ++np;
                 if (!ok) break;
                 tc_fence_after();
-                issue_PV(ve, jj > 0);
+                issue_PV(ve, 1, true);
                 if (more) {
                     issue_S((MODE == MODE_DIFF && s == 1) ? nB : nA);
                     mma_commit_elect(bar(L::BAR_S + s));
@@ -572,10 +582,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd_kernel(const __grid_c
                     l *= alpha;
                     m = m_new;
                 }
+                // O is complete up to tile jj-1 here (its PV was issued before this tile's S);
+                // a rescale must reach O before the first half of P is published
+                if (rescale && jj > 0) {
+                    uint32_t rr[32];
+#pragma unroll
+                    for (int c = 0; c < D / 32; ++c) {
+                        tmem_ld32(tO + c * 32, rr);
+#pragma unroll
+                        for (int t = 0; t < 32; ++t)
+                            rr[t] = __float_as_uint(__uint_as_float(rr[t]) * alpha);
+                        tmem_st32(tO + c * 32, rr);
+                    }
+                }
                 const float ms = (m == -INFINITY) ? 0.f : m * sl2;
                 // P = exp2(x * scale * log2 e - m * scale * log2 e): the argument two lanes at
                 // a time (packed fma), four packed partial row sums, bf16 pairs stored to TMEM
-                // in 32-column chunks as soon as they are ready
+                // per 64-column half, each half published (one arrival per warp) as soon as
+                // it is in TMEM
                 const uint64_t sl2x2 = f32x2_pack(sl2, sl2);
                 const uint64_t nmsx2 = f32x2_pack(-ms, -ms);
                 uint64_t acc[4] = {0ull, 0ull, 0ull, 0ull};
@@ -596,6 +620,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd_kernel(const __grid_c
                         pk[t] = pack_bf16x2(p0, p1);
                     }
                     tmem_st32(tS + c * 32, pk);
+                    tmem_wait_st();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(L::BAR_P + 2 * s + c));
                 }
                 {
                     const uint64_t s01 = f32x2_add(acc[0], acc[1]);
@@ -604,23 +632,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd_kernel(const __grid_c
                     f32x2_unpack(f32x2_add(s01, s23), u0, u1);
                     l += u0 + u1;
                 }
-                // O is complete up to tile jj-1 here (its PV was issued before this tile's S)
-                if (rescale && jj > 0) {
-                    uint32_t rr[32];
-#pragma unroll
-                    for (int c = 0; c < D / 32; ++c) {
-                        tmem_ld32(tO + c * 32, rr);
-#pragma unroll
-                        for (int t = 0; t < 32; ++t)
-                            rr[t] = __float_as_uint(__uint_as_float(rr[t]) * alpha);
-                        tmem_st32(tO + c * 32, rr);
-                    }
-                }
-                // P (and any O rescale) of this warp's 32 rows is in TMEM: one arrival per warp
-                tmem_wait_st();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar(L::BAR_P + s));
             }
             if (!ok) break;
             // ---- epilogue of the item.  Its TMEM reads of O precede this slot's next P
