@@ -18,6 +18,8 @@ Parity status per function (what pins it is listed in the tests):
   attn(kind="causal")  pinned: worked example (full causal 38/8), brute force.
   diff                 pinned: lambda = 0, (Q2, K2) = (Q1, K1), affinity in
                        lambda, brute force of the dense (A1 - lambda A2) V.
+  diff_heads           pinned: equal lambdas reproduce diff bitwise; a head with
+                       lambda = 0 is that head's causal attention.
   decode, cache_slot   pinned: the SWA note's W = 3 slot walk-through (§4.2),
                        equality with row t of attn(kind="window") over the whole
                        sequence when the cache was filled by rolling writes,
@@ -136,6 +138,28 @@ def diff(q1, k1, q2, k2, v, lam: float, scale: float, rows=None, nthreads: int =
                          float(scale), None if r is None else _ptr(r), nrows, int(nthreads))
     if rc != 0:
         raise ValueError(f"oracle_diff rejected its arguments (code {rc})")
+    return out
+
+
+def diff_heads(q1, k1, q2, k2, v, lams, scale: float, rows=None, nthreads: int = 0):
+    """Differential causal attention with one lambda per query head (the attention-variants
+    lesson's exercise 4, a learnable lambda per head): head h uses lams[h].  Computed head by
+    head with ``diff``."""
+    q1, q2 = np.asarray(q1), np.asarray(q2)
+    k1, k2, v = np.asarray(k1), np.asarray(k2), np.asarray(v)
+    lams = np.asarray(lams, dtype=np.float64)
+    B, Hq, N, d = q1.shape
+    Hkv = k1.shape[1]
+    if lams.shape != (Hq,):
+        raise ValueError("one lambda per query head expected")
+    g = Hq // Hkv
+    nrows = N if rows is None else len(rows)
+    out = np.empty((B, Hq, nrows, d), dtype=np.float64)
+    for h in range(Hq):
+        hk = h // g
+        out[:, h] = diff(q1[:, h:h + 1], k1[:, hk:hk + 1], q2[:, h:h + 1], k2[:, hk:hk + 1],
+                         v[:, hk:hk + 1], float(lams[h]), scale, rows=rows,
+                         nthreads=nthreads)[:, 0]
     return out
 
 

@@ -455,3 +455,24 @@ def test_decode_gqa_equals_repeated_kv(oracle_mod):
     a = oracle_mod.decode(q, kc, vc, pos, W, 0.3)
     b = oracle_mod.decode(q, np.repeat(kc, 3, axis=1), np.repeat(vc, 3, axis=1), pos, W, 0.3)
     np.testing.assert_array_equal(a, b)
+
+
+# ------------------------------------------------------------------ per-head lambda
+def test_diff_heads_equal_lambdas_is_diff(oracle_mod):
+    rng = np.random.default_rng(60)
+    B, Hq, Hkv, N, d = 2, 4, 2, 19, 8
+    a = [rng.standard_normal((B, Hq if i in (0, 2) else Hkv, N, d)) for i in range(5)]
+    ref = oracle_mod.diff(*a, 0.7, 0.3)
+    got = oracle_mod.diff_heads(*a, np.full(Hq, 0.7), 0.3)
+    np.testing.assert_array_equal(got, ref)
+
+
+def test_diff_heads_lambda_zero_head_is_causal(oracle_mod):
+    rng = np.random.default_rng(61)
+    B, Hq, Hkv, N, d = 1, 3, 3, 15, 4
+    a = [rng.standard_normal((B, Hq, N, d)) for _ in range(5)]
+    got = oracle_mod.diff_heads(*a, np.array([0.0, 0.5, 1.0]), 0.4)
+    causal = oracle_mod.attn(a[0], a[1], a[4], N, 0.4, kind="causal")
+    np.testing.assert_allclose(got[:, 0], causal[:, 0], rtol=0, atol=1e-12)
+    half = oracle_mod.diff(*a, 0.5, 0.4)
+    np.testing.assert_array_equal(got[:, 1], half[:, 1])
