@@ -87,6 +87,17 @@ int diff_attn_fwd(const void* q1, const void* k1, const void* q2, const void* k2
                   float scale, void* stream);
 
 /*
+ * Differential causal attention with one lambda per query head (the attention-variants
+ * lesson's exercise 4, "a learnable lambda per head"): head h of out is
+ *   (softmax_causal(scale Q1_h K1^T) - lambda[h] softmax_causal(scale Q2_h K2^T)) V.
+ * lambda: float32 [Hq] DEVICE array (read by the kernel, so a training loop can update it
+ * in place), 4-byte aligned.  Everything else as diff_attn_fwd.
+ */
+int diff_attn_fwd_heads(const void* q1, const void* k1, const void* q2, const void* k2,
+                        const void* v, const float* lambda, void* out, int B, int Hq, int Hkv,
+                        int N, int d, float scale, void* stream);
+
+/*
  * strided_attn_fwd without any device allocation.  The pages have no counterpart to
  * this call; it exists for callers that cannot call cudaMalloc, for example code that
  * runs under an external memory manager or an allocator that forbids foreign device

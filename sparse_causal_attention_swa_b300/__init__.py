@@ -7,7 +7,7 @@ module is a thin ctypes binding with the same names as the C ABI declared in
 and streams.  There is no CPU fallback: if the library is missing, every call raises.
 
 Low-level calls (pointers or tensors, explicit sizes, asynchronous on ``stream``):
-    swa_attn_fwd, strided_attn_fwd, diff_attn_fwd, strided_attn_fwd_noalloc,
+    swa_attn_fwd, strided_attn_fwd, diff_attn_fwd, diff_attn_fwd_heads, strided_attn_fwd_noalloc,
     swa_decode_workspace_bytes, swa_decode_fwd, swa_cache_append,
     swa_status_string, swa_device_status, swa_watchdog_selftest
 Convenience wrappers on [B, H, N, d] bf16 tensors (allocate ``out``; CPU inputs are
@@ -51,6 +51,8 @@ def load():
         lib.strided_attn_fwd_noalloc.restype = I
         lib.diff_attn_fwd.argtypes = [P, P, P, P, P, F, P, I, I, I, I, I, F, P]
         lib.diff_attn_fwd.restype = I
+        lib.diff_attn_fwd_heads.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, F, P]
+        lib.diff_attn_fwd_heads.restype = I
         SZ = ctypes.c_size_t
         lib.swa_decode_workspace_bytes.argtypes = [I, I, I, I]
         lib.swa_decode_workspace_bytes.restype = SZ
@@ -134,6 +136,13 @@ def swa_decode_fwd(q, k_cache, v_cache, pos, out, B, Hq, Hkv, W, d, scale, works
 def swa_cache_append(k_new, v_new, k_cache, v_cache, pos, B, Hkv, W, d, stream=None):
     _check(load().swa_cache_append(_ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
                                    _ptr(pos), B, Hkv, W, d, _stream(stream)), "swa_cache_append")
+
+
+def diff_attn_fwd_heads(q1, k1, q2, k2, v, lam, out, B, Hq, Hkv, N, d, scale, stream=None):
+    """diff_attn_fwd with one lambda per query head; ``lam`` is a float32 [Hq] device tensor."""
+    _check(load().diff_attn_fwd_heads(_ptr(q1), _ptr(k1), _ptr(q2), _ptr(k2), _ptr(v), _ptr(lam),
+                                      _ptr(out), B, Hq, Hkv, N, d, float(scale), _stream(stream)),
+           "diff_attn_fwd_heads")
 
 
 def swa_device_status(stream=None) -> int:

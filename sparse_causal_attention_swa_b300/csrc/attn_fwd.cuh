@@ -89,6 +89,7 @@ struct KParams {
     int pair_mode;      // 1: both slots on the same rows; 0: consecutive row tiles of a head
     float scale_log2;   // scale * log2(e)
     float lambda;       // diff only
+    const float* lambda_heads;  // diff: one lambda per query head (device), or null
     int n_items;        // work items; the grid is persistent and walks them
 };
 
@@ -654,7 +655,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd_kernel(const __grid_c
                     ok = __all_sync(0xffffffffu, ok);
                     if (!ok) break;
                     tc_fence_after();
-                    inv_l2 = lsm[trow] * p.lambda;
+                    inv_l2 = lsm[trow] * (p.lambda_heads ? p.lambda_heads[wi.h[0]] : p.lambda);
                 }
                 // O / l (differential: O1 / l1 - lambda O2 / l2) to bf16 into the staging tile
                 // (128-byte box rows, 16-byte unit u stored at u ^ (row & 7)); the store warp

@@ -445,8 +445,9 @@ int strided_attn_fwd_noalloc(const void* q, const void* k, const void* v, void* 
     return dispatch<swa::MODE_STRIDED>(d, kp, n_items_for(kp), s, *st);
 }
 
-int diff_attn_fwd(const void* q1, const void* k1, const void* q2, const void* k2, const void* v,
-                  float lambda, void* out, int B, int Hq, int Hkv, int N, int d, float scale,
+namespace {
+int diff_common(const void* q1, const void* k1, const void* q2, const void* k2, const void* v,
+                float lambda, const float* lambda_heads, void* out, int B, int Hq, int Hkv, int N, int d, float scale,
                   void* stream) {
     if (!q1 || !k1 || !q2 || !k2 || !v || !out) return SWA_ERR_NULL;
     int rc = check_common(B, Hq, Hkv, N, d, scale);
@@ -462,6 +463,7 @@ int diff_attn_fwd(const void* q1, const void* k1, const void* q2, const void* k2
     std::memset(&kp, 0, sizeof(kp));
     fill_common(kp, B, Hq, Hkv, N, N, 1, scale, out, *st);
     kp.lambda = lambda;
+    kp.lambda_heads = lambda_heads;
     kp.pair_mode = 1;  // the two slots are the two score streams of the same rows
     if ((rc = make_map(&kp.tm_q, q1, d, N, d, (long long)B * Hq, (long long)N * d))) return rc;
     if ((rc = make_map(&kp.tm_out, out, d, N, d, (long long)B * Hq, (long long)N * d))) return rc;
@@ -471,6 +473,21 @@ int diff_attn_fwd(const void* q1, const void* k1, const void* q2, const void* k2
     if ((rc = make_map(&kp.tm_v, v, d, N, d, (long long)B * Hkv, (long long)N * d))) return rc;
     const int n_items = B * Hq * kp.n_qtiles;
     return dispatch<swa::MODE_DIFF>(d, kp, n_items, static_cast<cudaStream_t>(stream), *st);
+}
+}  // namespace
+
+int diff_attn_fwd(const void* q1, const void* k1, const void* q2, const void* k2, const void* v,
+                  float lambda, void* out, int B, int Hq, int Hkv, int N, int d, float scale,
+                  void* stream) {
+    return diff_common(q1, k1, q2, k2, v, lambda, nullptr, out, B, Hq, Hkv, N, d, scale, stream);
+}
+
+int diff_attn_fwd_heads(const void* q1, const void* k1, const void* q2, const void* k2,
+                        const void* v, const float* lambda, void* out, int B, int Hq, int Hkv,
+                        int N, int d, float scale, void* stream) {
+    if (!lambda) return SWA_ERR_NULL;
+    if ((reinterpret_cast<uintptr_t>(lambda) & 3u) != 0) return SWA_ERR_ALIGN;
+    return diff_common(q1, k1, q2, k2, v, 0.f, lambda, out, B, Hq, Hkv, N, d, scale, stream);
 }
 
 int swa_device_status(void* stream) {

@@ -149,6 +149,37 @@ def test_diff_full_size_sampled():
     _full_size("diff")
 
 
+@pytest.mark.parametrize("heads", [(4, 2), (3, 3)])
+def test_diff_per_head_lambda(heads):
+    import oracle
+
+    Hq, Hkv = heads
+    for d, N in ((64, 300), (128, 129)):
+        w = _w("diff", 2, Hq, Hkv, N, d, N, lam=0.0, seed=N + d)
+        inp = swa_inputs.make_inputs(w)
+        lams = np.linspace(-0.5, 1.2, Hq).astype(np.float32)
+        t = {n: to_dev(a) for n, a in inp.items()}
+        out, buf = out_like(t["q1"])
+        lam_dev = torch.from_numpy(lams).cuda()
+        pkg.diff_attn_fwd_heads(t["q1"], t["k1"], t["q2"], t["k2"], t["v"], lam_dev, out, w.B,
+                                Hq, Hkv, N, d, w.scale)
+        torch.cuda.synchronize()
+        assert pkg.swa_device_status() == 0
+        got = to_f64(out)
+        ref = oracle.diff_heads(inp["q1"], inp["k1"], inp["q2"], inp["k2"], inp["v"], lams,
+                                w.scale)
+        assert_close(w, got, ref, f"per-head lambda {heads} d={d}")
+        # a scalar call with every head's lambda equal matches the per-head call bitwise
+        lam_dev.fill_(0.8)
+        pkg.diff_attn_fwd_heads(t["q1"], t["k1"], t["q2"], t["k2"], t["v"], lam_dev, out, w.B,
+                                Hq, Hkv, N, d, w.scale)
+        out2, _ = out_like(t["q1"])
+        pkg.diff_attn_fwd(t["q1"], t["k1"], t["q2"], t["k2"], t["v"], 0.8, out2, w.B, Hq, Hkv,
+                          N, d, w.scale)
+        torch.cuda.synchronize()
+        assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
+
+
 # ------------------------------------------------------------------------- watchdog
 def test_watchdog_reports_timeout_and_clears():
     assert pkg.swa_device_status() == 0
