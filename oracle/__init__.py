@@ -20,6 +20,10 @@ Parity status per function (what pins it is listed in the tests):
                        lambda, brute force of the dense (A1 - lambda A2) V.
   diff_heads           pinned: equal lambdas reproduce diff bitwise; a head with
                        lambda = 0 is that head's causal attention.
+  lse                  pinned: the worked example's exponentials 1, 2, 3 (ln 6) and
+                       the full causal denominator 8 (ln 8); W = 1 (the row's own
+                       score); exp(lse) equals the softmax denominator used by attn
+                       (weights_row); brute force on tiny inputs.
   decode, cache_slot   pinned: the SWA note's W = 3 slot walk-through (§4.2),
                        equality with row t of attn(kind="window") over the whole
                        sequence when the cache was filled by rolling writes,
@@ -82,6 +86,9 @@ def _load():
             lib.oracle_decode.restype = ctypes.c_int
             lib.oracle_decode.argtypes = [_P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _I64,
                                           ctypes.c_double]
+            lib.oracle_lse.restype = ctypes.c_int
+            lib.oracle_lse.argtypes = [ctypes.c_int, _P, _P, _P, _I64, _I64, _I64, _I64, _I64,
+                                       _I64, _I64, ctypes.c_double, _P, _I64]
             lib.oracle_cache_slot.restype = ctypes.c_int64
             lib.oracle_cache_slot.argtypes = [_I64, _I64]
             lib.oracle_max_threads.restype = ctypes.c_int
@@ -210,6 +217,21 @@ def decode(q, kc, vc, pos, W: int, scale: float) -> np.ndarray:
                            int(W), d, float(scale))
     if rc != 0:
         raise ValueError(f"oracle_decode rejected its arguments (code {rc})")
+    return out
+
+
+def lse(q, k, W: int, scale: float, kind: str = "window", stride: int = 0, rows=None):
+    """Log-sum-exp of every row's masked scores, fp64 [B, Hq, nrows]."""
+    lib = _load()
+    q64, k64 = _f64(q), _f64(k)
+    B, Hq, N, d = q64.shape
+    Hkv = k64.shape[1]
+    r, nrows = _rows_arg(rows, N)
+    out = np.empty((B, Hq, nrows), dtype=np.float64)
+    rc = lib.oracle_lse(KINDS[kind], _ptr(q64), _ptr(k64), _ptr(out), B, Hq, Hkv, N, d, int(W),
+                        int(stride), float(scale), None if r is None else _ptr(r), nrows)
+    if rc != 0:
+        raise ValueError(f"oracle_lse rejected its arguments (code {rc})")
     return out
 
 

@@ -288,6 +288,50 @@ int oracle_decode(const double* q, const double* kc, const double* vc, const int
     return 0;
 }
 
+/*
+ * Log-sum-exp of every row's masked scores: lse_i = log sum_j exp(scale q_i . k_j) over the
+ * allowed keys of row i (the normaliser of the row softmax, steps 1-3 above), written with the
+ * row maximum taken out: m + log sum_j exp(z_j - m).  lse: [B, Hq, nrows].
+ */
+int oracle_lse(int kind, const double* q, const double* k, double* lse, int64_t B, int64_t Hq,
+               int64_t Hkv, int64_t N, int64_t d, int64_t W, int64_t stride, double scale,
+               const int64_t* rows, int64_t nrows) {
+    if (check_shape(B, Hq, Hkv, N, d)) return 2;
+    if (kind != MASK_WINDOW && kind != MASK_STRIDED && kind != MASK_CAUSAL) return 2;
+    if (kind != MASK_CAUSAL && W < 1) return 2;
+    if (kind == MASK_STRIDED && stride < 1) return 2;
+    if (rows == NULL && nrows != N) return 2;
+    for (int64_t r = 0; rows && r < nrows; ++r)
+        if (rows[r] < 0 || rows[r] >= N) return 2;
+    const int64_t g = Hq / Hkv;
+    double* M = (double*)malloc(sizeof(double) * (size_t)N);
+    double* z = (double*)malloc(sizeof(double) * (size_t)N);
+    for (int64_t b = 0; b < B; ++b)
+        for (int64_t h = 0; h < Hq; ++h)
+            for (int64_t r = 0; r < nrows; ++r) {
+                const int64_t i = rows ? rows[r] : r;
+                const double* qi = q + ((b * Hq + h) * N + i) * d;
+                const double* kh = k + (b * Hkv + h / g) * N * d;
+                mask_row(kind, i, W, stride, M);
+                double m = -INFINITY;
+                for (int64_t j = 0; j <= i; ++j) {
+                    z[j] = -INFINITY;
+                    if (M[j] == 0.0) {
+                        double dot = 0.0;
+                        for (int64_t c = 0; c < d; ++c) dot += qi[c] * kh[j * d + c];
+                        z[j] = scale * dot;
+                    }
+                    if (z[j] > m) m = z[j];
+                }
+                double sum = 0.0;
+                for (int64_t j = 0; j <= i; ++j) sum += (z[j] == -INFINITY) ? 0.0 : exp(z[j] - m);
+                lse[(b * Hq + h) * nrows + r] = m + log(sum);
+            }
+    free(M);
+    free(z);
+    return 0;
+}
+
 /* Slot of absolute position j in a W-slot rolling cache ([SWA] §4.2, 0-indexed). */
 int64_t oracle_cache_slot(int64_t j, int64_t W) { return (W < 1 || j < 0) ? -1 : j % W; }
 

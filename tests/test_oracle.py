@@ -476,3 +476,44 @@ def test_diff_heads_lambda_zero_head_is_causal(oracle_mod):
     np.testing.assert_allclose(got[:, 0], causal[:, 0], rtol=0, atol=1e-12)
     half = oracle_mod.diff(*a, 0.5, 0.4)
     np.testing.assert_array_equal(got[:, 1], half[:, 1])
+
+
+# ------------------------------------------------------------------ row log-sum-exp
+def test_lse_worked_example(oracle_mod):
+    # the worked example's window scores exponentiate to 1, 2, 3 (denominator 6); under full
+    # causal attention positions 1..3 add 1 each (denominator 8)
+    fx, q, k, _ = _worked_inputs("v_split_a")
+    assert abs(oracle_mod.lse(q, k, int(fx["W"]), 1.0)[0, 0, 4] - math.log(6.0)) < 1e-14
+    assert abs(oracle_mod.lse(q, k, 5, 1.0)[0, 0, 4] - math.log(8.0)) < 1e-14
+    assert abs(oracle_mod.lse(q, k, 0, 1.0, kind="causal")[0, 0, 4] - math.log(8.0)) < 1e-14
+
+
+def test_lse_w1_is_own_score_and_matches_weights(oracle_mod):
+    rng = np.random.default_rng(70)
+    B, Hq, Hkv, N, d = 1, 4, 2, 23, 8
+    q = rng.standard_normal((B, Hq, N, d))
+    k = rng.standard_normal((B, Hkv, N, d))
+    own = 0.3 * np.einsum("bhnd,bhnd->bhn", q, np.repeat(k, 2, axis=1))
+    np.testing.assert_allclose(oracle_mod.lse(q, k, 1, 0.3), own, rtol=0, atol=1e-12)
+    # exp(scale q.k_j - lse) are the softmax weights of the row
+    for kind, W, s in (("window", 5, 0), ("strided", 3, 4), ("causal", 0, 0)):
+        L = oracle_mod.lse(q, k, W, 0.3, kind=kind, stride=s)
+        for i in (0, 7, 22):
+            w = oracle_mod.weights_row(q, k, W, 0.3, 0, 3, i, kind=kind, stride=s)
+            allowed = oracle_mod.mask_row(N, W, i, kind=kind, stride=s)
+            z = 0.3 * (np.repeat(k, 2, axis=1)[0, 3] @ q[0, 3, i])
+            np.testing.assert_allclose(np.where(allowed, np.exp(z - L[0, 3, i]), 0.0), w,
+                                       rtol=0, atol=1e-12)
+
+
+def test_lse_brute_force(oracle_mod):
+    rng = np.random.default_rng(71)
+    N, d = 17, 4
+    q = rng.standard_normal((1, 1, N, d))
+    k = rng.standard_normal((1, 1, N, d))
+    for W in (1, 3, 17, 20):
+        L = oracle_mod.lse(q, k, W, 0.5)
+        for i in range(N):
+            lo = max(0, i - W + 1)
+            z = 0.5 * (k[0, 0, lo:i + 1] @ q[0, 0, i])
+            assert abs(L[0, 0, i] - math.log(np.exp(z).sum())) < 1e-12
