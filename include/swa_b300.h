@@ -69,6 +69,15 @@ int swa_attn_fwd(const void* q, const void* k, const void* v, void* out, int B, 
                  int Hkv, int N, int d, int W, float scale, void* stream);
 
 /*
+ * swa_attn_fwd that also writes each row's log-sum-exp, the normaliser of its softmax:
+ *   lse[b, h, i] = ln sum_{j in the window of i} exp(scale * q_i . k_j)     (float32)
+ * (what a backward pass or a combination of partial attention results needs).
+ * lse: float32 [B, Hq, N] device, 4-byte aligned; NULL behaves as swa_attn_fwd.
+ */
+int swa_attn_fwd_lse(const void* q, const void* k, const void* v, void* out, float* lse, int B,
+                     int Hq, int Hkv, int N, int d, int W, float scale, void* stream);
+
+/*
  * Local + strided sparse causal attention forward ([AV] step 3): row i reads the
  * window keys max(0, i-W+1) <= j <= i and every key j = 0, stride, 2*stride, ... <= i
  * (absolute multiples of stride; a key in both sets counts once).
@@ -76,6 +85,11 @@ int swa_attn_fwd(const void* q, const void* k, const void* v, void* out, int B, 
  */
 int strided_attn_fwd(const void* q, const void* k, const void* v, void* out, int B, int Hq,
                      int Hkv, int N, int d, int W, int stride, float scale, void* stream);
+
+/* strided_attn_fwd that also writes each row's log-sum-exp over its mask (as swa_attn_fwd_lse). */
+int strided_attn_fwd_lse(const void* q, const void* k, const void* v, void* out, float* lse,
+                         int B, int Hq, int Hkv, int N, int d, int W, int stride, float scale,
+                         void* stream);
 
 /*
  * Differential causal attention forward ([AVpt] "Atenção Diferencial"; [AV] step 4):

@@ -8,6 +8,7 @@ and streams.  There is no CPU fallback: if the library is missing, every call ra
 
 Low-level calls (pointers or tensors, explicit sizes, asynchronous on ``stream``):
     swa_attn_fwd, strided_attn_fwd, diff_attn_fwd, diff_attn_fwd_heads, strided_attn_fwd_noalloc,
+    swa_attn_fwd_lse, strided_attn_fwd_lse,
     swa_decode_workspace_bytes, swa_decode_fwd, swa_cache_append,
     swa_status_string, swa_device_status, swa_watchdog_selftest
 Convenience wrappers on [B, H, N, d] bf16 tensors (allocate ``out``; CPU inputs are
@@ -47,6 +48,10 @@ def load():
         lib.swa_attn_fwd.restype = I
         lib.strided_attn_fwd.argtypes = [P, P, P, P, I, I, I, I, I, I, I, F, P]
         lib.strided_attn_fwd.restype = I
+        lib.swa_attn_fwd_lse.argtypes = [P, P, P, P, P, I, I, I, I, I, I, F, P]
+        lib.swa_attn_fwd_lse.restype = I
+        lib.strided_attn_fwd_lse.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, F, P]
+        lib.strided_attn_fwd_lse.restype = I
         lib.strided_attn_fwd_noalloc.argtypes = [P, P, P, P, I, I, I, I, I, I, I, F, P]
         lib.strided_attn_fwd_noalloc.restype = I
         lib.diff_attn_fwd.argtypes = [P, P, P, P, P, F, P, I, I, I, I, I, F, P]
@@ -106,6 +111,18 @@ def swa_attn_fwd(q, k, v, out, B, Hq, Hkv, N, d, W, scale, stream=None):
 def strided_attn_fwd(q, k, v, out, B, Hq, Hkv, N, d, W, stride, scale, stream=None):
     _check(load().strided_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, Hq, Hkv, N, d, W,
                                    stride, float(scale), _stream(stream)), "strided_attn_fwd")
+
+
+def swa_attn_fwd_lse(q, k, v, out, lse, B, Hq, Hkv, N, d, W, scale, stream=None):
+    """swa_attn_fwd that also writes each row's log-sum-exp (float32 [B, Hq, N])."""
+    _check(load().swa_attn_fwd_lse(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, N,
+                                   d, W, float(scale), _stream(stream)), "swa_attn_fwd_lse")
+
+
+def strided_attn_fwd_lse(q, k, v, out, lse, B, Hq, Hkv, N, d, W, stride, scale, stream=None):
+    _check(load().strided_attn_fwd_lse(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq,
+                                       Hkv, N, d, W, stride, float(scale), _stream(stream)),
+           "strided_attn_fwd_lse")
 
 
 def strided_attn_fwd_noalloc(q, k, v, out, B, Hq, Hkv, N, d, W, stride, scale, stream=None):

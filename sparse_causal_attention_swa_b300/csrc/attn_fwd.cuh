@@ -90,6 +90,8 @@ struct KParams {
     float scale_log2;   // scale * log2(e)
     float lambda;       // diff only
     const float* lambda_heads;  // diff: one lambda per query head (device), or null
+    float* lse;         // window / strided: per-row log-sum-exp [B, Hq, N] (device), or null
+    float scale;        // scale (natural units), for the log-sum-exp
     int n_items;        // work items; the grid is persistent and walks them
 };
 
@@ -642,6 +644,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd_kernel(const __grid_c
             if (!ok) break;
             tc_fence_after();
             const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+            // log-sum-exp of the row's scores: l sums exp2((x - m) scale log2 e), so
+            // ln sum_j exp(scale x_j) = m scale + ln l for whichever maximum m was used
+            if (MODE != MODE_DIFF && p.lse != nullptr && row < p.N)
+                p.lse[(size_t)(wi.b * p.Hq + wi.h[s]) * p.N + row] =
+                    (l > 0.f) ? m * p.scale + logf(l) : -INFINITY;
             if (MODE == MODE_DIFF && s == 1) {
                 lsm[trow] = inv_l;
                 mbar_arrive(bar(L::BAR_L));

@@ -152,6 +152,7 @@ void fill_common(KParams& kp, int B, int Hq, int Hkv, int N, int W, int stride, 
     kp.stride = stride;
     kp.n_qtiles = (N + BM - 1) / BM;
     kp.scale_log2 = scale * 1.4426950408889634f;
+    kp.scale = scale;
     kp.lambda = 0.f;
 }
 
@@ -332,9 +333,10 @@ const char* swa_status_string(int status) {
     }
 }
 
-int swa_attn_fwd(const void* q, const void* k, const void* v, void* out, int B, int Hq, int Hkv,
-                 int N, int d, int W, float scale, void* stream) {
+int swa_attn_fwd_lse(const void* q, const void* k, const void* v, void* out, float* lse, int B,
+                     int Hq, int Hkv, int N, int d, int W, float scale, void* stream) {
     if (!q || !k || !v || !out) return SWA_ERR_NULL;
+    if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return SWA_ERR_ALIGN;
     if (W < 1) return SWA_ERR_SHAPE;
     int rc = check_common(B, Hq, Hkv, N, d, scale);
     if (rc) return rc;
@@ -345,6 +347,7 @@ int swa_attn_fwd(const void* q, const void* k, const void* v, void* out, int B, 
     KParams kp;
     std::memset(&kp, 0, sizeof(kp));
     fill_common(kp, B, Hq, Hkv, N, std::min(W, N), 1, scale, out, *st);
+    kp.lse = lse;
     kp.pair_mode = ((Hq / Hkv) % 2 == 0) ? 1 : 0;
     if ((rc = make_map(&kp.tm_q, q, d, N, d, (long long)B * Hq, (long long)N * d))) return rc;
     if ((rc = make_map(&kp.tm_out, out, d, N, d, (long long)B * Hq, (long long)N * d))) return rc;
@@ -354,9 +357,16 @@ int swa_attn_fwd(const void* q, const void* k, const void* v, void* out, int B, 
                                       *st);
 }
 
-int strided_attn_fwd(const void* q, const void* k, const void* v, void* out, int B, int Hq,
-                     int Hkv, int N, int d, int W, int stride, float scale, void* stream) {
+int swa_attn_fwd(const void* q, const void* k, const void* v, void* out, int B, int Hq, int Hkv,
+                 int N, int d, int W, float scale, void* stream) {
+    return swa_attn_fwd_lse(q, k, v, out, nullptr, B, Hq, Hkv, N, d, W, scale, stream);
+}
+
+int strided_attn_fwd_lse(const void* q, const void* k, const void* v, void* out, float* lse,
+                         int B, int Hq, int Hkv, int N, int d, int W, int stride, float scale,
+                         void* stream) {
     if (!q || !k || !v || !out) return SWA_ERR_NULL;
+    if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return SWA_ERR_ALIGN;
     if (W < 1 || stride < 1) return SWA_ERR_SHAPE;
     int rc = check_common(B, Hq, Hkv, N, d, scale);
     if (rc) return rc;
@@ -369,6 +379,7 @@ int strided_attn_fwd(const void* q, const void* k, const void* v, void* out, int
     const int Wc = std::min(W, N);
     const int sc = std::min(stride, N);  // a stride >= N opens key 0 only, as stride N does
     fill_common(kp, B, Hq, Hkv, N, Wc, sc, scale, out, *st);
+    kp.lse = lse;
     kp.pair_mode = ((Hq / Hkv) % 2 == 0) ? 1 : 0;
     const int* list = nullptr;
     if ((rc = get_tile_list(*st, N, Wc, sc, kp.pair_mode ? BM : 2 * BM,
@@ -388,6 +399,11 @@ int strided_attn_fwd(const void* q, const void* k, const void* v, void* out, int
         return rc;
     return dispatch<swa::MODE_STRIDED>(d, kp, n_items_for(kp), static_cast<cudaStream_t>(stream),
                                        *st);
+}
+
+int strided_attn_fwd(const void* q, const void* k, const void* v, void* out, int B, int Hq,
+                     int Hkv, int N, int d, int W, int stride, float scale, void* stream) {
+    return strided_attn_fwd_lse(q, k, v, out, nullptr, B, Hq, Hkv, N, d, W, stride, scale, stream);
 }
 
 int strided_attn_fwd_noalloc(const void* q, const void* k, const void* v, void* out, int B,

@@ -118,6 +118,43 @@ def test_gemma_global_full_size_sampled():
     _full_size("gemma_global", n_random=40, boundary_step=16)
 
 
+LSE_ATOL, LSE_RTOL = 1e-3, 1e-4  # fp32 log-sum-exp: fp32 scores and sums, approximate exp2
+
+
+@pytest.mark.parametrize("kind", ["swa", "strided"])
+def test_lse_output(kind):
+    import oracle
+
+    for (Hq, Hkv, N, d, W, s) in ((4, 2, 300, 128, 77, 16), (3, 1, 513, 64, 200, 7),
+                                  (2, 2, 129, 128, 1, 3), (8, 2, 1000, 128, 1000, 128)):
+        w = _w(kind, 2, Hq, Hkv, N, d, W, stride=s, seed=N + W)
+        inp = swa_inputs.make_inputs(w)
+        t = {n: to_dev(a) for n, a in inp.items()}
+        out, _ = out_like(t["q"])
+        lse = torch.full((w.B, Hq, N), float("nan"), dtype=torch.float32, device="cuda")
+        if kind == "swa":
+            pkg.swa_attn_fwd_lse(t["q"], t["k"], t["v"], out, lse, w.B, Hq, Hkv, N, d, W, w.scale)
+        else:
+            pkg.strided_attn_fwd_lse(t["q"], t["k"], t["v"], out, lse, w.B, Hq, Hkv, N, d, W, s,
+                                     w.scale)
+        torch.cuda.synchronize()
+        assert pkg.swa_device_status() == 0
+        mk = "window" if kind == "swa" else "strided"
+        ref = oracle.lse(inp["q"], inp["k"], W, w.scale, kind=mk, stride=s)
+        got = lse.double().cpu().numpy()
+        assert np.all(np.isfinite(got))
+        err = np.abs(got - ref)
+        assert np.all(err <= LSE_ATOL + LSE_RTOL * np.abs(ref)), f"{kind} {N} {W}: {err.max():.3e}"
+        # the output matches the call without the log-sum-exp bitwise
+        out2, _ = out_like(t["q"])
+        if kind == "swa":
+            pkg.swa_attn_fwd(t["q"], t["k"], t["v"], out2, w.B, Hq, Hkv, N, d, W, w.scale)
+        else:
+            pkg.strided_attn_fwd(t["q"], t["k"], t["v"], out2, w.B, Hq, Hkv, N, d, W, s, w.scale)
+        torch.cuda.synchronize()
+        assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
+
+
 # ------------------------------------------------------------------------- local + strided
 @pytest.mark.parametrize("d", [64, 128])
 @pytest.mark.parametrize("heads", [(1, 1), (4, 2), (3, 1)])
