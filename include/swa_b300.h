@@ -165,13 +165,37 @@ int swa_decode_fwd(const void* q, const void* k_cache, const void* v_cache, cons
                    size_t workspace_bytes, void* stream);
 
 /*
- * Rolling-cache update ([SWA] §4.2): writes k_new[b, h, :] and v_new[b, h, :] (bf16
- * [B, Hkv, d] device) into slot pos[b] mod W of k_cache / v_cache (bf16 [B, Hkv, W, d]
- * device), overwriting the position that left the window.  pos: int32 [B] device; a
- * negative position writes nothing.  One kernel on `stream`.
+ * Rolling-cache update ([SWA] §4.2): writes n new rows per (sequence b, KV head h),
+ * k_new[b, h, r, :] and v_new[b, h, r, :] (bf16 [B, Hkv, n, d] device), which hold positions
+ * pos[b] + r, into slot (pos[b] + r) mod W of k_cache / v_cache (bf16 [B, Hkv, W, d] device),
+ * overwriting the positions that left the window.  Of a block longer than W only the last W
+ * rows are written.  pos: int32 [B] device; a negative position writes nothing.  n = 1 is
+ * the per-token update of a decode step.  One kernel on `stream`.
  */
 int swa_cache_append(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
-                     const int* pos, int B, int Hkv, int W, int d, void* stream);
+                     const int* pos, int B, int Hkv, int W, int d, int n, void* stream);
+
+/*
+ * Chunked prefill ([SWA] §4.3: the queries of a chunk need different windows, across the
+ * history and the chunk, under the local causal mask).  The queries q (bf16 [B, Hq, C, d])
+ * are the LAST C positions of a contiguous key/value context k, v (bf16 [B, Hkv, L, d],
+ * C <= L): query row c sits at key position L - C + c and reads the keys
+ * max(0, L-C+c-W+1) .. L-C+c.  out: bf16 [B, Hq, C, d].  With C = L this is swa_attn_fwd.
+ * For a rolling cache, build the context with swa_cache_gather (the W-1 positions before the
+ * chunk, in time order) followed by the chunk's own keys and values, then append the chunk
+ * with swa_cache_append (n = C).  Same kernel, layout and error rules as swa_attn_fwd.
+ */
+int swa_chunk_fwd(const void* q, const void* k, const void* v, void* out, int B, int Hq,
+                  int Hkv, int C, int L, int d, int W, float scale, void* stream);
+
+/*
+ * Copy positions pos0 - nctx .. pos0 - 1 (0 <= nctx <= min(W, pos0)) out of the rolling caches
+ * (slot = position mod W, [SWA] §4.2), in time order, into rows 0 .. nctx-1 of the contiguous
+ * context buffers k_ctx, v_ctx (bf16 [B, Hkv, ctx_rows, d] device, ctx_rows >= nctx).
+ * pos0 is the same for every sequence of the batch.  One kernel on `stream`.
+ */
+int swa_cache_gather(const void* k_cache, const void* v_cache, void* k_ctx, void* v_ctx, int B,
+                     int Hkv, int W, int d, int pos0, int nctx, int ctx_rows, void* stream);
 
 /* Human-readable name of a status code (static storage; never NULL). */
 const char* swa_status_string(int status);

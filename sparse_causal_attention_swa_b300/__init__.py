@@ -9,7 +9,8 @@ and streams.  There is no CPU fallback: if the library is missing, every call ra
 Low-level calls (pointers or tensors, explicit sizes, asynchronous on ``stream``):
     swa_attn_fwd, strided_attn_fwd, diff_attn_fwd, diff_attn_fwd_heads, strided_attn_fwd_noalloc,
     swa_attn_fwd_lse, strided_attn_fwd_lse,
-    swa_decode_workspace_bytes, swa_decode_fwd, swa_cache_append,
+    swa_decode_workspace_bytes, swa_decode_fwd, swa_cache_append, swa_chunk_fwd,
+    swa_cache_gather,
     swa_status_string, swa_device_status, swa_watchdog_selftest
 Convenience wrappers on [B, H, N, d] bf16 tensors (allocate ``out``; CPU inputs are
 copied to the current CUDA device and the result copied back):
@@ -63,8 +64,12 @@ def load():
         lib.swa_decode_workspace_bytes.restype = SZ
         lib.swa_decode_fwd.argtypes = [P, P, P, P, P, I, I, I, I, I, F, P, SZ, P]
         lib.swa_decode_fwd.restype = I
-        lib.swa_cache_append.argtypes = [P, P, P, P, P, I, I, I, I, P]
+        lib.swa_cache_append.argtypes = [P, P, P, P, P, I, I, I, I, I, P]
         lib.swa_cache_append.restype = I
+        lib.swa_chunk_fwd.argtypes = [P, P, P, P, I, I, I, I, I, I, I, F, P]
+        lib.swa_chunk_fwd.restype = I
+        lib.swa_cache_gather.argtypes = [P, P, P, P, I, I, I, I, I, I, I, P]
+        lib.swa_cache_gather.restype = I
         lib.swa_status_string.argtypes = [I]
         lib.swa_status_string.restype = ctypes.c_char_p
         lib.swa_device_status.argtypes = [P]
@@ -150,9 +155,23 @@ def swa_decode_fwd(q, k_cache, v_cache, pos, out, B, Hq, Hkv, W, d, scale, works
                                  int(workspace_bytes), _stream(stream)), "swa_decode_fwd")
 
 
-def swa_cache_append(k_new, v_new, k_cache, v_cache, pos, B, Hkv, W, d, stream=None):
+def swa_cache_append(k_new, v_new, k_cache, v_cache, pos, B, Hkv, W, d, n=1, stream=None):
     _check(load().swa_cache_append(_ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
-                                   _ptr(pos), B, Hkv, W, d, _stream(stream)), "swa_cache_append")
+                                   _ptr(pos), B, Hkv, W, d, n, _stream(stream)),
+           "swa_cache_append")
+
+
+def swa_chunk_fwd(q, k, v, out, B, Hq, Hkv, C, L, d, W, scale, stream=None):
+    """Queries are the last C of L context positions (chunked prefill)."""
+    _check(load().swa_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, Hq, Hkv, C, L, d, W,
+                                float(scale), _stream(stream)), "swa_chunk_fwd")
+
+
+def swa_cache_gather(k_cache, v_cache, k_ctx, v_ctx, B, Hkv, W, d, pos0, nctx, ctx_rows,
+                     stream=None):
+    _check(load().swa_cache_gather(_ptr(k_cache), _ptr(v_cache), _ptr(k_ctx), _ptr(v_ctx), B, Hkv,
+                                   W, d, pos0, nctx, ctx_rows, _stream(stream)),
+           "swa_cache_gather")
 
 
 def diff_attn_fwd_heads(q1, k1, q2, k2, v, lam, out, B, Hq, Hkv, N, d, scale, stream=None):

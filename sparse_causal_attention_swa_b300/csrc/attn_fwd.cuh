@@ -92,6 +92,8 @@ struct KParams {
     const float* lambda_heads;  // diff: one lambda per query head (device), or null
     float* lse;         // window / strided: per-row log-sum-exp [B, Hq, N] (device), or null
     float scale;        // scale (natural units), for the log-sum-exp
+    int q_off;          // window mode: query row r sits at key position r + q_off (a chunk
+                        // after q_off earlier positions); 0 otherwise
     int n_items;        // work items; the grid is persistent and walks them
 };
 
@@ -227,8 +229,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd_kernel(const __grid_c
             t.list_off = nblk + 1 + p.tiles[wi.block];
             t.n_tiles = p.tiles[wi.block + 1] - p.tiles[wi.block];
         } else {
-            t.kv_lo = (MODE == MODE_DIFF) ? 0 : max(0, wi.R0 - p.W + 1) / BN;
-            t.n_tiles = wi.R1 / BN - t.kv_lo + 1;
+            t.kv_lo = (MODE == MODE_DIFF) ? 0 : max(0, wi.R0 + p.q_off - p.W + 1) / BN;
+            t.n_tiles = (wi.R1 + p.q_off) / BN - t.kv_lo + 1;
         }
         return t;
     };
@@ -520,7 +522,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd_kernel(const __grid_c
             const WorkItem wi = decode_item<MODE>(p, item);
             const TileSeq ts = tile_seq(wi);
             const int row = wi.r0[s] + trow;
-            const int lo_i = (MODE == MODE_DIFF) ? 0 : max(0, row - p.W + 1);
+            const int rowk = row + p.q_off;  // the query's key position
+            const int lo_i = (MODE == MODE_DIFF) ? 0 : max(0, rowk - p.W + 1);
             const int lo_strided =
                 (MODE == MODE_STRIDED) ? (lo_i + p.stride - 1) / p.stride : 0;
             float m = -INFINITY, l = 0.f;
@@ -543,7 +546,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd_kernel(const __grid_c
                 } else {
                     const int c0 = idx * BN;
                     a = lo_i - c0;
-                    bnd = row - c0;
+                    bnd = rowk - c0;
                 }
                 // Mask, on edge tiles only: columns outside [a, bnd] become -inf.  Usually only
                 // one side cuts the tile (the diagonal tile: t <= bnd; the window-start tile:

@@ -153,6 +153,7 @@ void fill_common(KParams& kp, int B, int Hq, int Hkv, int N, int W, int stride, 
     kp.n_qtiles = (N + BM - 1) / BM;
     kp.scale_log2 = scale * 1.4426950408889634f;
     kp.scale = scale;
+    kp.q_off = 0;
     kp.lambda = 0.f;
 }
 
@@ -360,6 +361,30 @@ int swa_attn_fwd_lse(const void* q, const void* k, const void* v, void* out, flo
 int swa_attn_fwd(const void* q, const void* k, const void* v, void* out, int B, int Hq, int Hkv,
                  int N, int d, int W, float scale, void* stream) {
     return swa_attn_fwd_lse(q, k, v, out, nullptr, B, Hq, Hkv, N, d, W, scale, stream);
+}
+
+int swa_chunk_fwd(const void* q, const void* k, const void* v, void* out, int B, int Hq,
+                  int Hkv, int C, int L, int d, int W, float scale, void* stream) {
+    if (!q || !k || !v || !out) return SWA_ERR_NULL;
+    if (W < 1 || C < 1 || L < C) return SWA_ERR_SHAPE;
+    int rc = check_common(B, Hq, Hkv, L, d, scale);
+    if (rc) return rc;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return SWA_ERR_ALIGN;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceState* st = nullptr;
+    if ((rc = current_device_state(&st))) return rc;
+    KParams kp;
+    std::memset(&kp, 0, sizeof(kp));
+    // queries: C rows; keys: L rows; query row c sits at key position L - C + c
+    fill_common(kp, B, Hq, Hkv, C, std::min(W, L), 1, scale, out, *st);
+    kp.q_off = L - C;
+    kp.pair_mode = ((Hq / Hkv) % 2 == 0) ? 1 : 0;
+    if ((rc = make_map(&kp.tm_q, q, d, C, d, (long long)B * Hq, (long long)C * d))) return rc;
+    if ((rc = make_map(&kp.tm_out, out, d, C, d, (long long)B * Hq, (long long)C * d))) return rc;
+    if ((rc = make_map(&kp.tm_k, k, d, L, d, (long long)B * Hkv, (long long)L * d))) return rc;
+    if ((rc = make_map(&kp.tm_v, v, d, L, d, (long long)B * Hkv, (long long)L * d))) return rc;
+    return dispatch<swa::MODE_WINDOW>(d, kp, n_items_for(kp), static_cast<cudaStream_t>(stream),
+                                      *st);
 }
 
 int strided_attn_fwd_lse(const void* q, const void* k, const void* v, void* out, float* lse,
@@ -586,9 +611,9 @@ int swa_decode_fwd(const void* q, const void* k_cache, const void* v_cache, cons
 }
 
 int swa_cache_append(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
-                     const int* pos, int B, int Hkv, int W, int d, void* stream) {
+                     const int* pos, int B, int Hkv, int W, int d, int n, void* stream) {
     if (!k_new || !v_new || !k_cache || !v_cache || !pos) return SWA_ERR_NULL;
-    if (B < 1 || Hkv < 1 || W < 1 || (long long)B * Hkv > (1ll << 30)) return SWA_ERR_SHAPE;
+    if (B < 1 || Hkv < 1 || W < 1 || n < 1 || (long long)B * Hkv > (1ll << 30)) return SWA_ERR_SHAPE;
     if (d != 64 && d != 128) return SWA_ERR_UNSUPPORTED;
     if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache) ||
         (reinterpret_cast<uintptr_t>(pos) & 3u) != 0)
@@ -598,7 +623,7 @@ int swa_cache_append(const void* k_new, const void* v_new, void* k_cache, void* 
     int rc = current_device_state(&st);
     if (rc) return rc;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(B * Hkv), 1, 1);
+    cfg.gridDim = dim3((unsigned)(B * Hkv), (unsigned)std::min(n, W), 1);
     cfg.blockDim = dim3((unsigned)(d / 8), 1, 1);
     cfg.stream = static_cast<cudaStream_t>(stream);
     const auto* kn = static_cast<const __nv_bfloat16*>(k_new);
@@ -606,8 +631,36 @@ int swa_cache_append(const void* k_new, const void* v_new, void* k_cache, void* 
     auto* kc = static_cast<__nv_bfloat16*>(k_cache);
     auto* vc = static_cast<__nv_bfloat16*>(v_cache);
     cudaError_t e = (d == 128)
-                        ? cudaLaunchKernelEx(&cfg, swa::cache_append_kernel<128>, kn, vn, kc, vc, pos, Hkv, W)
-                        : cudaLaunchKernelEx(&cfg, swa::cache_append_kernel<64>, kn, vn, kc, vc, pos, Hkv, W);
+        ? cudaLaunchKernelEx(&cfg, swa::cache_append_kernel<128>, kn, vn, kc, vc, pos, Hkv, W, n)
+        : cudaLaunchKernelEx(&cfg, swa::cache_append_kernel<64>, kn, vn, kc, vc, pos, Hkv, W, n);
+    return e == cudaSuccess ? SWA_OK : SWA_ERR_CUDA;
+}
+
+int swa_cache_gather(const void* k_cache, const void* v_cache, void* k_ctx, void* v_ctx, int B,
+                     int Hkv, int W, int d, int pos0, int nctx, int ctx_rows, void* stream) {
+    if (!k_cache || !v_cache || !k_ctx || !v_ctx) return SWA_ERR_NULL;
+    if (B < 1 || Hkv < 1 || W < 1 || nctx < 0 || nctx > W || nctx > pos0 || ctx_rows < nctx ||
+        (long long)B * Hkv > (1ll << 30))
+        return SWA_ERR_SHAPE;
+    if (d != 64 && d != 128) return SWA_ERR_UNSUPPORTED;
+    if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(k_ctx) || !aligned16(v_ctx))
+        return SWA_ERR_ALIGN;
+    if (nctx == 0) return SWA_OK;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceState* st = nullptr;
+    int rc = current_device_state(&st);
+    if (rc) return rc;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(B * Hkv), (unsigned)nctx, 1);
+    cfg.blockDim = dim3((unsigned)(d / 8), 1, 1);
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    const auto* kc = static_cast<const __nv_bfloat16*>(k_cache);
+    const auto* vc = static_cast<const __nv_bfloat16*>(v_cache);
+    auto* kx = static_cast<__nv_bfloat16*>(k_ctx);
+    auto* vx = static_cast<__nv_bfloat16*>(v_ctx);
+    cudaError_t e = (d == 128)
+        ? cudaLaunchKernelEx(&cfg, swa::cache_gather_kernel<128>, kc, vc, kx, vx, W, pos0, nctx, ctx_rows)
+        : cudaLaunchKernelEx(&cfg, swa::cache_gather_kernel<64>, kc, vc, kx, vx, W, pos0, nctx, ctx_rows);
     return e == cudaSuccess ? SWA_OK : SWA_ERR_CUDA;
 }
 
