@@ -18,6 +18,10 @@ Parity status per function (what pins it is listed in the tests):
   attn(kind="causal")  pinned: worked example (full causal 38/8), brute force.
   diff                 pinned: lambda = 0, (Q2, K2) = (Q1, K1), affinity in
                        lambda, brute force of the dense (A1 - lambda A2) V.
+  attn(kind="global")  pinned: n_g = 0 is the window bitwise, n_g >= N or W >= N is
+                       causal, n_g = 1 equals strided with stride >= N (window plus
+                       key 0), brute force of the dense mask, closed-form pair count.
+                       For this kind the ``stride`` argument carries n_g.
   diff_heads           pinned: equal lambdas reproduce diff bitwise; a head with
                        lambda = 0 is that head's causal attention.
   lse                  pinned: the worked example's exponentials 1, 2, 3 (ln 6) and
@@ -44,7 +48,7 @@ _LIB = os.path.join(_HERE, "_liboracle.so")
 _lock = threading.Lock()
 _lib = None
 
-KINDS = {"window": 0, "strided": 1, "causal": 2}
+KINDS = {"window": 0, "strided": 1, "causal": 2, "global": 3}
 
 _P = ctypes.c_void_p
 _I64 = ctypes.c_int64

@@ -23,6 +23,10 @@
  *        causal  : j <= i                                   ([AV] step 1)
  *        window  : max(0, i - W + 1) <= j <= i               ([AV] step 2, [SWA] §3.1)
  *        strided : window  plus  j = 0, s, 2s, ... <= i       ([AV] step 3)
+ *        global  : window  plus  the global prefix j < n_g (j <= i); the `stride`
+ *                  argument carries n_g for this kind ([AV] "稀疏 / 块注意力": a few
+ *                  global tokens such as [CLS] attend to all and are attended by all;
+ *                  under the causal mask a global row i < n_g reads every j <= i)
  *   2. z_j = scale * (q_i . k_j) + M_ij in fp64 (masked j give -inf and are not
  *      dotted: -inf + finite = -inf),
  *   3. a two-pass softmax over the row: m = max_j z_j, p_j = exp(z_j - m),
@@ -46,7 +50,7 @@
 #include <omp.h>
 #endif
 
-enum { MASK_WINDOW = 0, MASK_STRIDED = 1, MASK_CAUSAL = 2 };
+enum { MASK_WINDOW = 0, MASK_STRIDED = 1, MASK_CAUSAL = 2, MASK_GLOBAL = 3 };
 
 /* Row i of the additive mask, for keys 0..i (keys j > i are -inf in every mask
  * kind, so they are neither stored nor visited). */
@@ -61,6 +65,9 @@ static void mask_row(int kind, int64_t i, int64_t window, int64_t stride, double
     for (int64_t j = lo; j <= i; ++j) M[j] = 0.0;
     if (kind == MASK_STRIDED) {
         for (int64_t j = 0; j <= i; j += stride) M[j] = 0.0;
+    }
+    if (kind == MASK_GLOBAL) {
+        for (int64_t j = 0; j <= i && j < stride; ++j) M[j] = 0.0;
     }
 }
 
@@ -103,9 +110,11 @@ int oracle_attn(int kind, const double* q, const double* k, const double* v, dou
                 int64_t stride, double scale, const int64_t* rows, int64_t nrows,
                 int nthreads) {
     if (check_shape(B, Hq, Hkv, N, d)) return 2;
-    if (kind != MASK_WINDOW && kind != MASK_STRIDED && kind != MASK_CAUSAL) return 2;
+    if (kind != MASK_WINDOW && kind != MASK_STRIDED && kind != MASK_CAUSAL && kind != MASK_GLOBAL)
+        return 2;
     if (kind != MASK_CAUSAL && W < 1) return 2;
     if (kind == MASK_STRIDED && stride < 1) return 2;
+    if (kind == MASK_GLOBAL && stride < 0) return 2;
     if (rows == NULL && nrows != N) return 2;
     for (int64_t r = 0; rows && r < nrows; ++r)
         if (rows[r] < 0 || rows[r] >= N) return 2;
@@ -205,6 +214,7 @@ int oracle_weights_row(int kind, const double* q, const double* k, int64_t B, in
     if (b < 0 || b >= B || h < 0 || h >= Hq || i < 0 || i >= N) return 2;
     if (kind != MASK_CAUSAL && W < 1) return 2;
     if (kind == MASK_STRIDED && stride < 1) return 2;
+    if (kind == MASK_GLOBAL && stride < 0) return 2;
     const int64_t hk = h / (Hq / Hkv);
     double* M = (double*)malloc(sizeof(double) * (size_t)N);
     double* z = (double*)malloc(sizeof(double) * (size_t)N);
@@ -218,7 +228,9 @@ int oracle_weights_row(int kind, const double* q, const double* k, int64_t B, in
 
 /* Number of allowed (i, j) pairs of one head: the zeros of the mask, counted row by row. */
 int64_t oracle_pair_count(int kind, int64_t N, int64_t W, int64_t stride) {
-    if (N < 1 || (kind != MASK_CAUSAL && W < 1) || (kind == MASK_STRIDED && stride < 1)) return -1;
+    if (N < 1 || (kind != MASK_CAUSAL && W < 1) || (kind == MASK_STRIDED && stride < 1) ||
+        (kind == MASK_GLOBAL && stride < 0))
+        return -1;
     double* M = (double*)malloc(sizeof(double) * (size_t)N);
     int64_t count = 0;
     for (int64_t i = 0; i < N; ++i) {
@@ -297,9 +309,11 @@ int oracle_lse(int kind, const double* q, const double* k, double* lse, int64_t 
                int64_t Hkv, int64_t N, int64_t d, int64_t W, int64_t stride, double scale,
                const int64_t* rows, int64_t nrows) {
     if (check_shape(B, Hq, Hkv, N, d)) return 2;
-    if (kind != MASK_WINDOW && kind != MASK_STRIDED && kind != MASK_CAUSAL) return 2;
+    if (kind != MASK_WINDOW && kind != MASK_STRIDED && kind != MASK_CAUSAL && kind != MASK_GLOBAL)
+        return 2;
     if (kind != MASK_CAUSAL && W < 1) return 2;
     if (kind == MASK_STRIDED && stride < 1) return 2;
+    if (kind == MASK_GLOBAL && stride < 0) return 2;
     if (rows == NULL && nrows != N) return 2;
     for (int64_t r = 0; rows && r < nrows; ++r)
         if (rows[r] < 0 || rows[r] >= N) return 2;

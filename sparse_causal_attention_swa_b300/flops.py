@@ -36,6 +36,14 @@ def pairs_strided(N: int, W: int, stride: int) -> int:
     return int(win.sum() + extra.sum())
 
 
+def pairs_global(N: int, W: int, n_global: int) -> int:
+    """Window pairs plus, per row, the global prefix keys j < n_global that precede the window."""
+    i = np.arange(N, dtype=np.int64)
+    lo = np.maximum(0, i - W + 1)
+    win = np.minimum(i + 1, W)
+    return int(win.sum() + np.minimum(lo, n_global).sum())
+
+
 def useful_flops(kind: str, B: int, Hq: int, N: int, d: int, W: int, stride: int = 0) -> float:
     """Band-only useful FLOPs of one forward call."""
     if kind == "swa":
@@ -43,6 +51,9 @@ def useful_flops(kind: str, B: int, Hq: int, N: int, d: int, W: int, stride: int
         return 4.0 * d * p * B * Hq
     if kind == "strided":
         p = pairs_strided(N, W, stride)
+        return 4.0 * d * p * B * Hq
+    if kind == "global":  # stride carries the number of global prefix tokens
+        p = pairs_global(N, W, stride)
         return 4.0 * d * p * B * Hq
     if kind == "diff":
         p = pairs_causal(N)

@@ -517,3 +517,50 @@ def test_lse_brute_force(oracle_mod):
             lo = max(0, i - W + 1)
             z = 0.5 * (k[0, 0, lo:i + 1] @ q[0, 0, i])
             assert abs(L[0, 0, i] - math.log(np.exp(z).sum())) < 1e-12
+
+
+# ------------------------------------------------------------------ global prefix tokens
+def _dense_global_mask(N, W, ng):
+    i = np.arange(N)[:, None]
+    j = np.arange(N)[None, :]
+    return (j <= i) & ((j >= i - W + 1) | (j < ng))
+
+
+def test_global_special_cases(oracle_mod):
+    rng = np.random.default_rng(80)
+    B, Hq, Hkv, N, d = 1, 2, 1, 40, 8
+    q = rng.standard_normal((B, Hq, N, d))
+    k = rng.standard_normal((B, Hkv, N, d))
+    v = rng.standard_normal((B, Hkv, N, d))
+    win = oracle_mod.attn(q, k, v, 7, 0.3, kind="window")
+    np.testing.assert_array_equal(oracle_mod.attn(q, k, v, 7, 0.3, kind="global", stride=0), win)
+    causal = oracle_mod.attn(q, k, v, N, 0.3, kind="causal")
+    np.testing.assert_array_equal(oracle_mod.attn(q, k, v, 7, 0.3, kind="global", stride=N), causal)
+    np.testing.assert_array_equal(oracle_mod.attn(q, k, v, N, 0.3, kind="global", stride=5), causal)
+    # one global token = the window plus key 0 = strided with a stride past the sequence
+    np.testing.assert_array_equal(oracle_mod.attn(q, k, v, 7, 0.3, kind="global", stride=1),
+                                  oracle_mod.attn(q, k, v, 7, 0.3, kind="strided", stride=N))
+
+
+@pytest.mark.parametrize("N", [1, 9, 33])
+def test_global_brute_force_and_pair_count(oracle_mod, N):
+    rng = np.random.default_rng(81 + N)
+    d = 4
+    q = rng.standard_normal((1, 1, N, d))
+    k = rng.standard_normal((1, 1, N, d))
+    v = rng.standard_normal((1, 1, N, d))
+    for W in (1, 3, N, N + 2):
+        for ng in (0, 1, 4, N + 1):
+            allowed = _dense_global_mask(N, W, ng)
+            for i in range(N):
+                assert np.array_equal(oracle_mod.mask_row(N, W, i, kind="global", stride=ng),
+                                      allowed[i])
+            z = 0.5 * q[0, 0] @ k[0, 0].T
+            z = np.where(allowed, z, -np.inf)
+            a = np.exp(z - z.max(axis=1, keepdims=True))
+            a /= a.sum(axis=1, keepdims=True)
+            np.testing.assert_allclose(oracle_mod.attn(q, k, v, W, 0.5, kind="global",
+                                                       stride=ng)[0, 0], a @ v[0, 0],
+                                       rtol=0, atol=1e-12)
+            assert oracle_mod.pair_count(N, W, "global", ng) == int(allowed.sum())
+            assert flops.pairs_global(N, W, ng) == int(allowed.sum())
