@@ -183,6 +183,10 @@ def sample_flops(w: swa_inputs.Workload, rows: np.ndarray) -> float:
         lo = np.maximum(0, i - w.W + 1)
         per = np.minimum(i + 1, w.W) + np.where(lo > 0, (lo - 1) // w.stride + 1, 0)
         return 4.0 * w.d * float(per.sum()) * w.B * w.Hq
+    if w.kind == "global":
+        lo = np.maximum(0, i - w.W + 1)
+        per = np.minimum(i + 1, w.W) + np.minimum(lo, w.stride)
+        return 4.0 * w.d * float(per.sum()) * w.B * w.Hq
     return 8.0 * w.d * float((i + 1).sum()) * w.B * w.Hq
 
 
@@ -192,7 +196,7 @@ def run_oracle_rows(w, inp, rows):
     if w.kind == "diff":
         return oracle.diff(inp["q1"], inp["k1"], inp["q2"], inp["k2"], inp["v"], w.lam, w.scale,
                            rows=rows)
-    kind = "window" if w.kind == "swa" else "strided"
+    kind = {"swa": "window", "strided": "strided", "global": "global"}[w.kind]
     return oracle.attn(inp["q"], inp["k"], inp["v"], w.W, w.scale, kind=kind, stride=w.stride,
                        rows=rows)
 
@@ -295,6 +299,8 @@ def workload_config(w, fl, flush=False):
                  "inputs+output larger than twice the 126 MB L2; no flush between steps"}
     if w.kind == "strided":
         cfg["stride"] = w.stride
+    if w.kind == "global":
+        cfg["n_global"] = w.stride
     if w.kind == "diff":
         cfg["lambda"] = w.lam
         cfg["flop_convention"] = "8 d per causal pair (two attention maps)"
@@ -334,6 +340,9 @@ def launch(pkg, w, t, out, stream):
     elif w.kind == "strided":
         pkg.strided_attn_fwd(t["q"], t["k"], t["v"], out, w.B, w.Hq, w.Hkv, w.N, w.d, w.W,
                              w.stride, w.scale, stream)
+    elif w.kind == "global":
+        pkg.global_attn_fwd(t["q"], t["k"], t["v"], out, w.B, w.Hq, w.Hkv, w.N, w.d, w.W,
+                            w.stride, w.scale, stream)
     else:
         pkg.diff_attn_fwd(t["q1"], t["k1"], t["q2"], t["k2"], t["v"], w.lam, out, w.B, w.Hq,
                           w.Hkv, w.N, w.d, w.scale, stream)
@@ -409,7 +418,7 @@ def bench_workload(args, w, ws, rank, dev, want_cpu, want_e2e):
         roofline = {"bound": "tensor", "achieved": achieved_tf, "peak": bf16_peak,
                     "unit": "TFLOP/s", "frac": achieved_tf / bf16_peak, "traffic": traffic,
                     "peak_source": f"{peak_src} bf16_tflops (burst, kernel timed alone)",
-                    "kernel": f"attn_fwd_kernel<{w.d},{ {'swa': 0, 'strided': 1, 'diff': 2}[w.kind]}>",
+                    "kernel": f"attn_fwd_kernel<{w.d},{ {'swa': 0, 'strided': 1, 'global': 1, 'diff': 2}[w.kind]}>",
                     "algorithmic_flops_per_launch": fl,
                     "hbm_gbs_algorithmic": algo_bytes / (launch_ms * 1e-3) / 1e9}
     else:

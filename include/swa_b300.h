@@ -92,6 +92,18 @@ int strided_attn_fwd_lse(const void* q, const void* k, const void* v, void* out,
                          void* stream);
 
 /*
+ * Sliding window plus a global prefix ([AV] "稀疏 / 块注意力": Longformer-style global
+ * tokens such as [CLS] attend to all and are attended by all): row i reads its window
+ * max(0, i-W+1) <= j <= i and every key j < n_global with j <= i, a key in both counted once.
+ * Under the causal mask a global row (i < n_global) reads every j <= i.  n_global >= 0
+ * (0 is swa_attn_fwd; n_global >= N is full causal).  Runs the strided kernel with stride 1
+ * and the compact keys capped at n_global; the first call for a new (N, W, n_global) builds
+ * and caches a device tile list.
+ */
+int global_attn_fwd(const void* q, const void* k, const void* v, void* out, int B, int Hq,
+                    int Hkv, int N, int d, int W, int n_global, float scale, void* stream);
+
+/*
  * Differential causal attention forward ([AVpt] "Atenção Diferencial"; [AV] step 4):
  *   out = (softmax_causal(scale Q1 K1^T) - lambda softmax_causal(scale Q2 K2^T)) V.
  * q1, q2, out: Hq heads; k1, k2, v: Hkv heads.  Both maps are full causal.

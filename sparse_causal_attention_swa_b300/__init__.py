@@ -8,7 +8,7 @@ and streams.  There is no CPU fallback: if the library is missing, every call ra
 
 Low-level calls (pointers or tensors, explicit sizes, asynchronous on ``stream``):
     swa_attn_fwd, strided_attn_fwd, diff_attn_fwd, diff_attn_fwd_heads, strided_attn_fwd_noalloc,
-    swa_attn_fwd_lse, strided_attn_fwd_lse,
+    swa_attn_fwd_lse, strided_attn_fwd_lse, global_attn_fwd,
     swa_decode_workspace_bytes, swa_decode_fwd, swa_cache_append, swa_chunk_fwd,
     swa_cache_gather,
     swa_status_string, swa_device_status, swa_watchdog_selftest
@@ -49,6 +49,8 @@ def load():
         lib.swa_attn_fwd.restype = I
         lib.strided_attn_fwd.argtypes = [P, P, P, P, I, I, I, I, I, I, I, F, P]
         lib.strided_attn_fwd.restype = I
+        lib.global_attn_fwd.argtypes = [P, P, P, P, I, I, I, I, I, I, I, F, P]
+        lib.global_attn_fwd.restype = I
         lib.swa_attn_fwd_lse.argtypes = [P, P, P, P, P, I, I, I, I, I, I, F, P]
         lib.swa_attn_fwd_lse.restype = I
         lib.strided_attn_fwd_lse.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, F, P]
@@ -116,6 +118,12 @@ def swa_attn_fwd(q, k, v, out, B, Hq, Hkv, N, d, W, scale, stream=None):
 def strided_attn_fwd(q, k, v, out, B, Hq, Hkv, N, d, W, stride, scale, stream=None):
     _check(load().strided_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, Hq, Hkv, N, d, W,
                                    stride, float(scale), _stream(stream)), "strided_attn_fwd")
+
+
+def global_attn_fwd(q, k, v, out, B, Hq, Hkv, N, d, W, n_global, scale, stream=None):
+    """Window plus a global prefix of n_global tokens (causal)."""
+    _check(load().global_attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), B, Hq, Hkv, N, d, W,
+                                  n_global, float(scale), _stream(stream)), "global_attn_fwd")
 
 
 def swa_attn_fwd_lse(q, k, v, out, lse, B, Hq, Hkv, N, d, W, scale, stream=None):

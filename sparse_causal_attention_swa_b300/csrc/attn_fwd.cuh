@@ -92,6 +92,8 @@ struct KParams {
     const float* lambda_heads;  // diff: one lambda per query head (device), or null
     float* lse;         // window / strided: per-row log-sum-exp [B, Hq, N] (device), or null
     float scale;        // scale (natural units), for the log-sum-exp
+    int strided_cap;    // strided mode: at most this many compact keys (the global-prefix
+                        // form: stride 1, cap n_g); INT_MAX otherwise
     int q_off;          // window mode: query row r sits at key position r + q_off (a chunk
                         // after q_off earlier positions); 0 otherwise
     int n_items;        // work items; the grid is persistent and walks them
@@ -524,8 +526,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd_kernel(const __grid_c
             const int row = wi.r0[s] + trow;
             const int rowk = row + p.q_off;  // the query's key position
             const int lo_i = (MODE == MODE_DIFF) ? 0 : max(0, rowk - p.W + 1);
+            // compact keys of this row: the multiples of the stride before its window start
+            // (at most strided_cap of them: the global prefix j < n_g when the stride is 1)
             const int lo_strided =
-                (MODE == MODE_STRIDED) ? (lo_i + p.stride - 1) / p.stride : 0;
+                (MODE == MODE_STRIDED) ? min((lo_i + p.stride - 1) / p.stride, p.strided_cap) : 0;
             float m = -INFINITY, l = 0.f;
             for (int jj = 0; jj < ts.n_tiles; ++jj) {
                 ok = mbar_wait_bounded(bar(L::BAR_S + s), ns & 1u, abort_flag, lim);

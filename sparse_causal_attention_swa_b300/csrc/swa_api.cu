@@ -36,8 +36,8 @@ struct DeviceState {
     int num_sms = 0;
     bool attr_set[2][3] = {};
     bool dec_attr_set[2][5] = {};
-    // strided tile lists, keyed by (N, W, stride, rows per block)
-    std::map<std::tuple<int, int, int, int>, int*> tile_lists;
+    // strided tile lists, keyed by (N, W, stride, rows per block, compact-key cap)
+    std::map<std::tuple<int, int, int, int, int>, int*> tile_lists;
 };
 
 std::mutex g_mutex;
@@ -154,6 +154,7 @@ void fill_common(KParams& kp, int B, int Hq, int Hkv, int N, int W, int stride, 
     kp.scale_log2 = scale * 1.4426950408889634f;
     kp.scale = scale;
     kp.q_off = 0;
+    kp.strided_cap = 0x7fffffff;
     kp.lambda = 0.f;
 }
 
@@ -167,9 +168,9 @@ int n_items_for(const KParams& kp) {
 // The strided tile list: for every row block (the union of an item's rows), the compact
 // strided-key tiles that hold keys 0, s, 2s, ... before the block's last window start,
 // then the window tiles from the first row's window start to the block's last row.
-int get_tile_list(DeviceState& st, int N, int W, int stride, int rows_per_block,
+int get_tile_list(DeviceState& st, int N, int W, int stride, int rows_per_block, int cap,
                   cudaStream_t stream, const int** out) {
-    auto key = std::make_tuple(N, W, stride, rows_per_block);
+    auto key = std::make_tuple(N, W, stride, rows_per_block, cap);
     auto it = st.tile_lists.find(key);
     if (it != st.tile_lists.end()) {
         *out = it->second;
@@ -182,7 +183,8 @@ int get_tile_list(DeviceState& st, int N, int W, int stride, int rows_per_block,
         const long long R1 = std::min<long long>(R0 + rows_per_block, N) - 1;
         const long long lo0 = std::max<long long>(0, R0 - W + 1);
         const long long lo1 = std::max<long long>(0, R1 - W + 1);
-        const long long nkeys = (lo1 + stride - 1) / stride;  // multiples of s below lo1
+        // multiples of s below lo1, at most cap of them
+        const long long nkeys = std::min<long long>((lo1 + stride - 1) / stride, cap);
         const long long ncompact = (nkeys + BN - 1) / BN;
         for (long long c = 0; c < ncompact; ++c)
             ents.push_back((swa::TILE_KIND_STRIDED << swa::TILE_KIND_SHIFT) | (int)c);
@@ -387,9 +389,12 @@ int swa_chunk_fwd(const void* q, const void* k, const void* v, void* out, int B,
                                       *st);
 }
 
-int strided_attn_fwd_lse(const void* q, const void* k, const void* v, void* out, float* lse,
-                         int B, int Hq, int Hkv, int N, int d, int W, int stride, float scale,
-                         void* stream) {
+namespace {
+// The strided kernel over window tiles plus compact tiles of the keys 0, s, 2s, ... that lie
+// before a row's window, at most `cap` of them.
+int strided_common(const void* q, const void* k, const void* v, void* out, float* lse, int B,
+                   int Hq, int Hkv, int N, int d, int W, int stride, int cap, float scale,
+                   void* stream) {
     if (!q || !k || !v || !out) return SWA_ERR_NULL;
     if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u) != 0) return SWA_ERR_ALIGN;
     if (W < 1 || stride < 1) return SWA_ERR_SHAPE;
@@ -405,9 +410,10 @@ int strided_attn_fwd_lse(const void* q, const void* k, const void* v, void* out,
     const int sc = std::min(stride, N);  // a stride >= N opens key 0 only, as stride N does
     fill_common(kp, B, Hq, Hkv, N, Wc, sc, scale, out, *st);
     kp.lse = lse;
+    kp.strided_cap = cap;
     kp.pair_mode = ((Hq / Hkv) % 2 == 0) ? 1 : 0;
     const int* list = nullptr;
-    if ((rc = get_tile_list(*st, N, Wc, sc, kp.pair_mode ? BM : 2 * BM,
+    if ((rc = get_tile_list(*st, N, Wc, sc, kp.pair_mode ? BM : 2 * BM, cap,
                             static_cast<cudaStream_t>(stream), &list)))
         return rc;
     kp.tiles = list;
@@ -424,6 +430,21 @@ int strided_attn_fwd_lse(const void* q, const void* k, const void* v, void* out,
         return rc;
     return dispatch<swa::MODE_STRIDED>(d, kp, n_items_for(kp), static_cast<cudaStream_t>(stream),
                                        *st);
+}
+}  // namespace
+
+int strided_attn_fwd_lse(const void* q, const void* k, const void* v, void* out, float* lse,
+                         int B, int Hq, int Hkv, int N, int d, int W, int stride, float scale,
+                         void* stream) {
+    return strided_common(q, k, v, out, lse, B, Hq, Hkv, N, d, W, stride, 0x7fffffff, scale,
+                          stream);
+}
+
+int global_attn_fwd(const void* q, const void* k, const void* v, void* out, int B, int Hq,
+                    int Hkv, int N, int d, int W, int n_global, float scale, void* stream) {
+    if (n_global < 0) return SWA_ERR_SHAPE;
+    return strided_common(q, k, v, out, nullptr, B, Hq, Hkv, N, d, W, 1, std::min(n_global, N),
+                          scale, stream);
 }
 
 int strided_attn_fwd(const void* q, const void* k, const void* v, void* out, int B, int Hq,

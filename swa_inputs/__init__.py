@@ -25,7 +25,9 @@ class Workload:
     """One synthetic workload: the sizes of one call of the hot path."""
 
     name: str
-    kind: str  # "swa" | "strided" | "diff" | "decode"
+    kind: str  # "swa" | "strided" | "diff" | "decode" | "global"
+    # (for "strided" the stride field is the stride; for "global" it is the number of global
+    # prefix tokens)
     B: int
     Hq: int
     Hkv: int
@@ -63,6 +65,8 @@ WORKLOADS = {
     # differential causal attention with an attention sink on key 0 of K1
     "diff": Workload("diff", "diff", 1, 16, 16, 8192, 64, 8192, lam=0.8, sink_shift=3.0,
                      seed_index=5),
+    # window plus a global prefix (Longformer-style [CLS] / question tokens): W=512, 64 global
+    "global": Workload("global", "global", 1, 16, 16, 16384, 64, 512, stride=64, seed_index=7),
     # decode against a W-slot rolling KV cache, Mistral-7B heads: one new query per
     # sequence, 32 sequences at positions drawn from [0, N); N = 4 W, so most windows
     # are full (W cache rows) and some are still filling

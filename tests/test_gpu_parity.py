@@ -8,7 +8,7 @@ import torch
 import swa_inputs
 from swa_inputs import Workload
 import sparse_causal_attention_swa_b300 as pkg
-from gpu_util import assert_close, run_gpu, run_oracle, to_dev, to_f64, out_like
+from gpu_util import assert_close, canary_intact, run_gpu, run_oracle, to_dev, to_f64, out_like
 
 pytestmark = pytest.mark.gpu
 
@@ -169,6 +169,27 @@ def test_strided_sweep(d, heads):
 
 def test_strided_full_size_sampled():
     _full_size("strided")
+
+
+# ------------------------------------------------------------------------- global prefix
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("heads", [(4, 2), (3, 1)])
+def test_global_prefix_sweep(d, heads):
+    import oracle
+
+    Hq, Hkv = heads
+    for N in (100, 300, 700):
+        for W, ng in ((16, 0), (16, 1), (128, 16), (200, 129), (64, N), (1, 5), (N, 3)):
+            w = _w("swa", 2, Hq, Hkv, N, d, W, seed=N + 7 * W + ng)
+            inp = swa_inputs.make_inputs(w)
+            t = {n: to_dev(a) for n, a in inp.items()}
+            out, buf = out_like(t["q"])
+            pkg.global_attn_fwd(t["q"], t["k"], t["v"], out, w.B, Hq, Hkv, N, d, W, ng, w.scale)
+            torch.cuda.synchronize()
+            assert pkg.swa_device_status() == 0
+            assert canary_intact(buf, out.numel())
+            ref = oracle.attn(inp["q"], inp["k"], inp["v"], W, w.scale, kind="global", stride=ng)
+            assert_close(w, to_f64(out), ref, f"global N={N} W={W} n_g={ng} d={d} {heads}")
 
 
 # ------------------------------------------------------------------------- differential
