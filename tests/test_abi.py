@@ -103,3 +103,54 @@ def test_binding_raises_with_status():
     with pytest.raises(pkg.SwaError) as e:
         pkg.swa_attn_fwd(P, P, P, P, 1, 2, 2, 128, 64, 0, 0.125, stream=0)
     assert e.value.code == 2
+
+
+def test_decode_validation(L):
+    f = L.swa_decode_fwd
+    n = L.swa_decode_workspace_bytes(2, 8, 300, 128)
+    assert n > 0 and n % 4 == 0
+    assert L.swa_decode_workspace_bytes(2, 8, 300, 96) == 0
+    ok = dict(q=P, kc=P, vc=P, pos=P, out=P, B=2, Hq=8, Hkv=2, W=300, d=128, scale=0.1, ws=P,
+              nb=n)
+
+    def call(**kw):
+        a = {**ok, **kw}
+        return f(a["q"], a["kc"], a["vc"], a["pos"], a["out"], a["B"], a["Hq"], a["Hkv"], a["W"],
+                 a["d"], a["scale"], a["ws"], a["nb"], None)
+
+    assert call(pos=None) == 1
+    assert call(ws=None) == 1
+    assert call(W=0) == 2
+    assert call(Hq=8, Hkv=3) == 2
+    assert call(Hq=32, Hkv=1) == 4  # more than 16 query heads per KV head
+    assert call(d=80) == 4
+    assert call(scale=0.0) == 7
+    assert call(q=P + 8) == 3
+    assert call(pos=P + 2) == 3
+    assert call(ws=P + 16) == 3  # the workspace wants 256-byte alignment
+    assert call(nb=n - 1) == 8
+
+
+def test_cache_and_chunk_validation(L):
+    assert L.swa_cache_append(P, P, P, P, None, 2, 2, 64, 128, 1, None) == 1
+    assert L.swa_cache_append(P, P, P, P, P, 2, 2, 64, 128, 0, None) == 2
+    assert L.swa_cache_append(P, P, P, P, P, 2, 2, 64, 96, 1, None) == 4
+    g = L.swa_cache_gather
+    assert g(P, P, P, None, 2, 2, 64, 128, 100, 63, 80, None) == 1
+    assert g(P, P, P, P, 2, 2, 64, 128, 10, 11, 80, None) == 2  # more history than positions
+    assert g(P, P, P, P, 2, 2, 64, 128, 100, 65, 80, None) == 2  # more than W slots
+    assert g(P, P, P, P, 2, 2, 64, 128, 100, 63, 40, None) == 2  # context shorter than history
+    c = L.swa_chunk_fwd
+    assert c(P, P, P, None, 1, 4, 2, 16, 100, 128, 32, 0.1, None) == 1
+    assert c(P, P, P, P, 1, 4, 2, 101, 100, 128, 32, 0.1, None) == 2  # C > L
+    assert c(P, P, P, P, 1, 4, 2, 0, 100, 128, 32, 0.1, None) == 2
+    assert c(P, P, P, P, 1, 4, 2, 16, 100, 128, 0, 0.1, None) == 2
+
+
+def test_lse_global_and_per_head_lambda_validation(L):
+    assert L.swa_attn_fwd_lse(P, P, P, P, P + 2, 1, 2, 2, 128, 64, 16, 0.125, None) == 3
+    assert L.strided_attn_fwd_lse(P, P, P, P, P + 1, 1, 2, 2, 128, 64, 16, 4, 0.125, None) == 3
+    assert L.global_attn_fwd(P, P, P, P, 1, 2, 2, 128, 64, 16, -1, 0.125, None) == 2
+    assert L.global_attn_fwd(None, P, P, P, 1, 2, 2, 128, 64, 16, 4, 0.125, None) == 1
+    assert L.diff_attn_fwd_heads(P, P, P, P, P, None, P, 1, 2, 2, 128, 64, 0.125, None) == 1
+    assert L.diff_attn_fwd_heads(P, P, P, P, P, P + 2, P, 1, 2, 2, 128, 64, 0.125, None) == 3
