@@ -77,7 +77,7 @@ def _load():
                                         ctypes.c_int]
             lib.oracle_diff.restype = ctypes.c_int
             lib.oracle_diff.argtypes = [_P, _P, _P, _P, _P, ctypes.c_double, _P, _I64, _I64,
-                                        _I64, _I64, _I64, ctypes.c_double, _P, _I64,
+                                        _I64, _I64, _I64, _I64, ctypes.c_double, _P, _I64,
                                         ctypes.c_int]
             lib.oracle_weights_row.restype = ctypes.c_int
             lib.oracle_weights_row.argtypes = [ctypes.c_int, _P, _P, _I64, _I64, _I64, _I64,
@@ -137,22 +137,26 @@ def attn(q, k, v, W: int, scale: float, kind: str = "window", stride: int = 0,
     return out
 
 
-def diff(q1, k1, q2, k2, v, lam: float, scale: float, rows=None, nthreads: int = 0):
-    """Differential causal attention (A1 - lam A2) V in fp64."""
+def diff(q1, k1, q2, k2, v, lam: float, scale: float, rows=None, nthreads: int = 0,
+         W: int = 0):
+    """Differential attention (A1 - lam A2) V in fp64, both maps under the window mask of
+    width W (0 or W >= N: the causal mask)."""
     lib = _load()
     a = [_f64(x) for x in (q1, k1, q2, k2, v)]
     B, Hq, N, d = a[0].shape
     Hkv = a[1].shape[1]
     r, nrows = _rows_arg(rows, N)
     out = np.empty((B, Hq, nrows, d), dtype=np.float64)
-    rc = lib.oracle_diff(*[_ptr(x) for x in a], float(lam), _ptr(out), B, Hq, Hkv, N, d,
+    Wm = N if W == 0 else int(W)
+    rc = lib.oracle_diff(*[_ptr(x) for x in a], float(lam), _ptr(out), B, Hq, Hkv, N, d, Wm,
                          float(scale), None if r is None else _ptr(r), nrows, int(nthreads))
     if rc != 0:
         raise ValueError(f"oracle_diff rejected its arguments (code {rc})")
     return out
 
 
-def diff_heads(q1, k1, q2, k2, v, lams, scale: float, rows=None, nthreads: int = 0):
+def diff_heads(q1, k1, q2, k2, v, lams, scale: float, rows=None, nthreads: int = 0,
+               W: int = 0):
     """Differential causal attention with one lambda per query head (the attention-variants
     lesson's exercise 4, a learnable lambda per head): head h uses lams[h].  Computed head by
     head with ``diff``."""
@@ -170,7 +174,7 @@ def diff_heads(q1, k1, q2, k2, v, lams, scale: float, rows=None, nthreads: int =
         hk = h // g
         out[:, h] = diff(q1[:, h:h + 1], k1[:, hk:hk + 1], q2[:, h:h + 1], k2[:, hk:hk + 1],
                          v[:, hk:hk + 1], float(lams[h]), scale, rows=rows,
-                         nthreads=nthreads)[:, 0]
+                         nthreads=nthreads, W=W)[:, 0]
     return out
 
 

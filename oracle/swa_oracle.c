@@ -34,7 +34,10 @@
  *      [SWA] §3.1),
  *   4. out_i = sum_j a_j v_j.
  *   Differential ([AVpt] "Atenção Diferencial"): out_i = sum_j (a1_j - lambda a2_j) v_j
- *   with a1 from (q1, k1) and a2 from (q2, k2), both under the causal mask.
+ *   with a1 from (q1, k1) and a2 from (q2, k2), both under the same window mask of width
+ *   W; W >= N is the causal mask of the page's formulas, a smaller W a differential head
+ *   inside an SWA layer ([AV] opening list: the variants coexist, most layers SWA and a few
+ *   differential heads).
  *   Decode against a rolling cache ([SWA] §4.2): the K, V of absolute position j sit in
  *   cache slot j mod W (the note's 1-indexed slot (i-1) mod W); a query at position t reads
  *   the positions max(0, t-W+1) .. t through their slots, steps 2-4 as above.
@@ -156,14 +159,16 @@ int oracle_attn(int kind, const double* q, const double* k, const double* v, dou
 }
 
 /*
- * Differential causal attention: out = (A1 - lambda A2) V, A1 = softmax_causal(Q1 K1^T * scale),
- * A2 = softmax_causal(Q2 K2^T * scale).  Same layouts and row selection as oracle_attn.
+ * Differential attention: out = (A1 - lambda A2) V, A1 = softmax(Q1 K1^T * scale + M),
+ * A2 = softmax(Q2 K2^T * scale + M), M the window mask of width W (W >= N: causal).  Same
+ * layouts and row selection as oracle_attn.
  */
 int oracle_diff(const double* q1, const double* k1, const double* q2, const double* k2,
                 const double* v, double lambda, double* out, int64_t B, int64_t Hq, int64_t Hkv,
-                int64_t N, int64_t d, double scale, const int64_t* rows, int64_t nrows,
-                int nthreads) {
+                int64_t N, int64_t d, int64_t W, double scale, const int64_t* rows,
+                int64_t nrows, int nthreads) {
     if (check_shape(B, Hq, Hkv, N, d)) return 2;
+    if (W < 1) return 2;
     if (rows == NULL && nrows != N) return 2;
     for (int64_t r = 0; rows && r < nrows; ++r)
         if (rows[r] < 0 || rows[r] >= N) return 2;
@@ -187,7 +192,7 @@ int oracle_diff(const double* q1, const double* k1, const double* q2, const doub
             const int64_t hk = h / g;
             const size_t qoff = (size_t)(((b * Hq + h) * N + i) * d);
             const size_t koff = (size_t)((b * Hkv + hk) * N * d);
-            mask_row(MASK_CAUSAL, i, 0, 0, M);
+            mask_row(MASK_WINDOW, i, W, 0, M);
             softmax_row(q1 + qoff, k1 + koff, d, i, scale, M, z, a1);
             softmax_row(q2 + qoff, k2 + koff, d, i, scale, M, z, a2);
             double* o = out + ((b * Hq + h) * nrows + r) * d;

@@ -310,6 +310,45 @@ def test_diff_brute_force(oracle_mod):
     assert np.max(np.abs(out - ref)) < 1e-12
 
 
+# A differential head inside an SWA layer: both maps under the same window mask.
+def test_diff_window_brute_force(oracle_mod):
+    q1, k1, q2, k2, v = _diff_inputs(12, B=2, Hq=4, Hkv=2, N=41, d=8)
+    N = q1.shape[2]
+    for W in (1, 5, 17, 40, 41, 60):
+        M = dense_mask(N, "window", window=W)
+        ref = np.empty_like(q1)
+        for b in range(2):
+            for h in range(4):
+                A1 = dense_softmax(q1[b, h], k1[b, h // 2], 0.3, M)
+                A2 = dense_softmax(q2[b, h], k2[b, h // 2], 0.3, M)
+                ref[b, h] = (A1 - 0.8 * A2) @ v[b, h // 2]
+        out = oracle_mod.diff(q1, k1, q2, k2, v, 0.8, 0.3, W=W)
+        assert np.max(np.abs(out - ref)) < 1e-12, W
+
+
+def test_diff_window_reductions(oracle_mod):
+    q1, k1, q2, k2, v = _diff_inputs(13, N=37)
+    N = q1.shape[2]
+    for W in (3, 16):
+        # lambda = 0: the window attention of the first map alone
+        ref = oracle_mod.attn(q1, k1, v, W, 0.35, kind="window")
+        out = oracle_mod.diff(q1, k1, q2, k2, v, 0.0, 0.35, W=W)
+        np.testing.assert_allclose(out, ref, rtol=0, atol=1e-14)
+        # equal maps: (1 - lambda) times the window attention
+        out = oracle_mod.diff(q1, k1, q1, k1, v, 0.8, 0.35, W=W)
+        np.testing.assert_allclose(out, 0.2 * ref, rtol=0, atol=1e-13)
+    # W = 1: each row keeps only its own key in both maps, out_i = (1 - lambda) v_i
+    out = oracle_mod.diff(q1, k1, q2, k2, v, 0.8, 0.35, W=1)
+    np.testing.assert_allclose(out, 0.2 * v, rtol=0, atol=1e-15)
+    # W >= N is the causal form, bit for bit
+    assert np.array_equal(oracle_mod.diff(q1, k1, q2, k2, v, 0.8, 0.35, W=N),
+                          oracle_mod.diff(q1, k1, q2, k2, v, 0.8, 0.35))
+    assert np.array_equal(oracle_mod.diff(q1, k1, q2, k2, v, 0.8, 0.35, W=5 * N),
+                          oracle_mod.diff(q1, k1, q2, k2, v, 0.8, 0.35))
+    with pytest.raises(ValueError):
+        oracle_mod.diff(q1, k1, q2, k2, v, 0.8, 0.35, W=-1)
+
+
 # ---------------------------------------------------------------------------------------------
 # GQA mapping, row subsets, bf16 inputs
 # ---------------------------------------------------------------------------------------------
