@@ -189,7 +189,7 @@ def sample_flops(w: swa_inputs.Workload, rows: np.ndarray) -> float:
         lo = np.maximum(0, i - w.W + 1)
         per = np.minimum(i + 1, w.W) + np.minimum(lo, w.stride)
         return 4.0 * w.d * float(per.sum()) * w.B * w.Hq
-    return 8.0 * w.d * float((i + 1).sum()) * w.B * w.Hq
+    return 8.0 * w.d * float(np.minimum(i + 1, w.W).sum()) * w.B * w.Hq
 
 
 def run_oracle_rows(w, inp, rows):
@@ -197,7 +197,7 @@ def run_oracle_rows(w, inp, rows):
 
     if w.kind == "diff":
         return oracle.diff(inp["q1"], inp["k1"], inp["q2"], inp["k2"], inp["v"], w.lam, w.scale,
-                           rows=rows)
+                           rows=rows, W=w.W)
     kind = {"swa": "window", "strided": "strided", "global": "global"}[w.kind]
     return oracle.attn(inp["q"], inp["k"], inp["v"], w.W, w.scale, kind=kind, stride=w.stride,
                        rows=rows)
@@ -305,7 +305,7 @@ def workload_config(w, fl, flush=False):
         cfg["n_global"] = w.stride
     if w.kind == "diff":
         cfg["lambda"] = w.lam
-        cfg["flop_convention"] = "8 d per causal pair (two attention maps)"
+        cfg["flop_convention"] = "8 d per (row, key) pair in the window (two attention maps)"
     return cfg
 
 
@@ -345,6 +345,9 @@ def launch(pkg, w, t, out, stream):
     elif w.kind == "global":
         pkg.global_attn_fwd(t["q"], t["k"], t["v"], out, w.B, w.Hq, w.Hkv, w.N, w.d, w.W,
                             w.stride, w.scale, stream)
+    elif w.W < w.N:
+        pkg.diff_swa_attn_fwd(t["q1"], t["k1"], t["q2"], t["k2"], t["v"], w.lam, None, out, w.B,
+                              w.Hq, w.Hkv, w.N, w.d, w.W, w.scale, stream)
     else:
         pkg.diff_attn_fwd(t["q1"], t["k1"], t["q2"], t["k2"], t["v"], w.lam, out, w.B, w.Hq,
                           w.Hkv, w.N, w.d, w.scale, stream)

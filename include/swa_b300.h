@@ -124,6 +124,19 @@ int diff_attn_fwd_heads(const void* q1, const void* k1, const void* q2, const vo
                         int N, int d, float scale, void* stream);
 
 /*
+ * A differential head inside an SWA layer ([AV] opening list: the variants coexist, most
+ * layers SWA with a few differential heads; [AVpt] "Atenção Diferencial" for the form):
+ * both maps take the window mask of width W,
+ *   out_i = sum_j (a1_ij - lambda_h a2_ij) v_j,  a_ij = softmax over max(0, i-W+1) <= j <= i.
+ * W >= 1 (W >= N is diff_attn_fwd / diff_attn_fwd_heads; W < 1 returns SWA_ERR_SHAPE).
+ * lambda_heads: float32 [Hq] DEVICE array, 4-byte aligned, or NULL to use the scalar lambda
+ * for every head.  Layouts, ownership and errors as diff_attn_fwd.
+ */
+int diff_swa_attn_fwd(const void* q1, const void* k1, const void* q2, const void* k2,
+                      const void* v, float lambda, const float* lambda_heads, void* out, int B,
+                      int Hq, int Hkv, int N, int d, int W, float scale, void* stream);
+
+/*
  * strided_attn_fwd without any device allocation.  The pages have no counterpart to
  * this call; it exists for callers that cannot call cudaMalloc, for example code that
  * runs under an external memory manager or an allocator that forbids foreign device

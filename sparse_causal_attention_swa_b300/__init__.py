@@ -7,8 +7,8 @@ module is a thin ctypes binding with the same names as the C ABI declared in
 and streams.  There is no CPU fallback: if the library is missing, every call raises.
 
 Low-level calls (pointers or tensors, explicit sizes, asynchronous on ``stream``):
-    swa_attn_fwd, strided_attn_fwd, diff_attn_fwd, diff_attn_fwd_heads, strided_attn_fwd_noalloc,
-    swa_attn_fwd_lse, strided_attn_fwd_lse, global_attn_fwd,
+    swa_attn_fwd, strided_attn_fwd, diff_attn_fwd, diff_attn_fwd_heads, diff_swa_attn_fwd,
+    strided_attn_fwd_noalloc, swa_attn_fwd_lse, strided_attn_fwd_lse, global_attn_fwd,
     swa_decode_workspace_bytes, swa_decode_fwd, swa_cache_append, swa_chunk_fwd,
     swa_cache_gather,
     swa_status_string, swa_device_status, swa_watchdog_selftest
@@ -61,6 +61,8 @@ def load():
         lib.diff_attn_fwd.restype = I
         lib.diff_attn_fwd_heads.argtypes = [P, P, P, P, P, P, P, I, I, I, I, I, F, P]
         lib.diff_attn_fwd_heads.restype = I
+        lib.diff_swa_attn_fwd.argtypes = [P, P, P, P, P, F, P, P, I, I, I, I, I, I, F, P]
+        lib.diff_swa_attn_fwd.restype = I
         SZ = ctypes.c_size_t
         lib.swa_decode_workspace_bytes.argtypes = [I, I, I, I]
         lib.swa_decode_workspace_bytes.restype = SZ
@@ -189,6 +191,16 @@ def diff_attn_fwd_heads(q1, k1, q2, k2, v, lam, out, B, Hq, Hkv, N, d, scale, st
            "diff_attn_fwd_heads")
 
 
+def diff_swa_attn_fwd(q1, k1, q2, k2, v, lam, lam_heads, out, B, Hq, Hkv, N, d, W, scale,
+                      stream=None):
+    """Differential attention with both maps under the window W; ``lam_heads`` is a float32
+    [Hq] device tensor or None (then the scalar ``lam`` serves every head)."""
+    _check(load().diff_swa_attn_fwd(_ptr(q1), _ptr(k1), _ptr(q2), _ptr(k2), _ptr(v), float(lam),
+                                    None if lam_heads is None else _ptr(lam_heads), _ptr(out), B,
+                                    Hq, Hkv, N, d, int(W), float(scale), _stream(stream)),
+           "diff_swa_attn_fwd")
+
+
 def swa_device_status(stream=None) -> int:
     return int(load().swa_device_status(_stream(stream)))
 
@@ -243,15 +255,20 @@ def strided_attention(q, k, v, window: int, stride: int, scale: float | None = N
     return _finish(o, q)
 
 
-def diff_attention(q1, k1, q2, k2, v, lam: float, scale: float | None = None, out=None):
-    """(softmax_causal(Q1 K1^T s) - lam softmax_causal(Q2 K2^T s)) V."""
+def diff_attention(q1, k1, q2, k2, v, lam: float, scale: float | None = None, out=None,
+                   window: int | None = None):
+    """(softmax(Q1 K1^T s + M) - lam softmax(Q2 K2^T s + M)) V, M causal, or the sliding
+    window of width ``window`` when one is given."""
     import torch
 
     (a, b_, c, e, f), dev = _prepare(q1, k1, q2, k2, v)
     B, Hq, N, d = a.shape
     o = out if out is not None else torch.empty_like(a)
-    diff_attn_fwd(a, b_, c, e, f, lam, o, B, Hq, b_.shape[1], N, d,
-                  scale if scale is not None else 1.0 / math.sqrt(d))
+    sc = scale if scale is not None else 1.0 / math.sqrt(d)
+    if window is None:
+        diff_attn_fwd(a, b_, c, e, f, lam, o, B, Hq, b_.shape[1], N, d, sc)
+    else:
+        diff_swa_attn_fwd(a, b_, c, e, f, lam, None, o, B, Hq, b_.shape[1], N, d, int(window), sc)
     return _finish(o, q1)
 
 

@@ -9,7 +9,9 @@
 //   * "注意力变体——滑动窗口、稀疏、差分", "Build it" step 3: the local + strided mask adds
 //     keys j = 0, s, 2s, ... <= i to the window.
 //   * "Variantes de Atenção", "Atenção Diferencial": out = (A1 - lambda A2) V with two
-//     causal softmax maps from (Q1, K1) and (Q2, K2).
+//     softmax maps from (Q1, K1) and (Q2, K2), both causal (W = N) or both under the
+//     window W (a differential head inside an SWA layer: "注意力变体", opening list, the
+//     variants coexist).
 //
 // CTA organisation (384 threads, one CTA per SM because of TMEM and shared memory):
 //   warps 0-3  softmax warpgroup of slot 0   (thread t owns query row t of the slot)
@@ -103,7 +105,7 @@ template <int D, int MODE>
 struct SmemLayout {
     static constexpr int QBYTES = BM * D * 2;
     static constexpr int EBYTES = BN * D * 2;  // one ring entry: a K or V tile
-    static constexpr int STAGES = (D == 128) ? 4 : 8;
+    static constexpr int STAGES = (D == 128) ? 4 : 10;
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_RING = 2 * QBYTES;
     // epilogue staging: one output tile, 128 rows x D bf16 as D/64 boxes of 64 columns
@@ -231,7 +233,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd_kernel(const __grid_c
             t.list_off = nblk + 1 + p.tiles[wi.block];
             t.n_tiles = p.tiles[wi.block + 1] - p.tiles[wi.block];
         } else {
-            t.kv_lo = (MODE == MODE_DIFF) ? 0 : max(0, wi.R0 + p.q_off - p.W + 1) / BN;
+            t.kv_lo = max(0, wi.R0 + p.q_off - p.W + 1) / BN;
             t.n_tiles = (wi.R1 + p.q_off) / BN - t.kv_lo + 1;
         }
         return t;
@@ -525,7 +527,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd_kernel(const __grid_c
             const TileSeq ts = tile_seq(wi);
             const int row = wi.r0[s] + trow;
             const int rowk = row + p.q_off;  // the query's key position
-            const int lo_i = (MODE == MODE_DIFF) ? 0 : max(0, rowk - p.W + 1);
+            const int lo_i = max(0, rowk - p.W + 1);
             // compact keys of this row: the multiples of the stride before its window start
             // (at most strided_cap of them: the global prefix j < n_g when the stride is 1)
             const int lo_strided =
@@ -656,6 +658,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) attn_fwd_kernel(const __grid_c
             if (MODE != MODE_DIFF && p.lse != nullptr && row < p.N)
                 p.lse[(size_t)(wi.b * p.Hq + wi.h[s]) * p.N + row] =
                     (l > 0.f) ? m * p.scale + logf(l) : -INFINITY;
+            // Differential: slot 0 writes out O1 / l1 - lambda O2 / l2, reading slot 1's O2 and
+            // 1 / l2 (through lsm).  The turn order keeps both intact until then: slot 1's next
+            // P V product (which overwrites O2) is issued after slot 0's, and slot 0 publishes
+            // the P it needs only after this epilogue; slot 1 reaches its next lsm write even
+            // later.
             if (MODE == MODE_DIFF && s == 1) {
                 lsm[trow] = inv_l;
                 mbar_arrive(bar(L::BAR_L));

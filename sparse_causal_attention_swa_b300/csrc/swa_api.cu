@@ -509,11 +509,13 @@ int strided_attn_fwd_noalloc(const void* q, const void* k, const void* v, void* 
 
 namespace {
 int diff_common(const void* q1, const void* k1, const void* q2, const void* k2, const void* v,
-                float lambda, const float* lambda_heads, void* out, int B, int Hq, int Hkv, int N, int d, float scale,
-                  void* stream) {
+                float lambda, const float* lambda_heads, void* out, int B, int Hq, int Hkv,
+                int N, int d, int W, float scale, void* stream) {
     if (!q1 || !k1 || !q2 || !k2 || !v || !out) return SWA_ERR_NULL;
     int rc = check_common(B, Hq, Hkv, N, d, scale);
     if (rc) return rc;
+    if (W < 1) return SWA_ERR_SHAPE;
+    if (W > N) W = N;
     if (!std::isfinite(lambda)) return SWA_ERR_VALUE;
     if (!aligned16(q1) || !aligned16(k1) || !aligned16(q2) || !aligned16(k2) || !aligned16(v) ||
         !aligned16(out))
@@ -523,7 +525,7 @@ int diff_common(const void* q1, const void* k1, const void* q2, const void* k2, 
     if ((rc = current_device_state(&st))) return rc;
     KParams kp;
     std::memset(&kp, 0, sizeof(kp));
-    fill_common(kp, B, Hq, Hkv, N, N, 1, scale, out, *st);
+    fill_common(kp, B, Hq, Hkv, N, W, 1, scale, out, *st);
     kp.lambda = lambda;
     kp.lambda_heads = lambda_heads;
     kp.pair_mode = 1;  // the two slots are the two score streams of the same rows
@@ -541,7 +543,8 @@ int diff_common(const void* q1, const void* k1, const void* q2, const void* k2, 
 int diff_attn_fwd(const void* q1, const void* k1, const void* q2, const void* k2, const void* v,
                   float lambda, void* out, int B, int Hq, int Hkv, int N, int d, float scale,
                   void* stream) {
-    return diff_common(q1, k1, q2, k2, v, lambda, nullptr, out, B, Hq, Hkv, N, d, scale, stream);
+    return diff_common(q1, k1, q2, k2, v, lambda, nullptr, out, B, Hq, Hkv, N, d, N, scale,
+                       stream);
 }
 
 int diff_attn_fwd_heads(const void* q1, const void* k1, const void* q2, const void* k2,
@@ -549,7 +552,16 @@ int diff_attn_fwd_heads(const void* q1, const void* k1, const void* q2, const vo
                         int N, int d, float scale, void* stream) {
     if (!lambda) return SWA_ERR_NULL;
     if ((reinterpret_cast<uintptr_t>(lambda) & 3u) != 0) return SWA_ERR_ALIGN;
-    return diff_common(q1, k1, q2, k2, v, 0.f, lambda, out, B, Hq, Hkv, N, d, scale, stream);
+    return diff_common(q1, k1, q2, k2, v, 0.f, lambda, out, B, Hq, Hkv, N, d, N, scale, stream);
+}
+
+int diff_swa_attn_fwd(const void* q1, const void* k1, const void* q2, const void* k2,
+                      const void* v, float lambda, const float* lambda_heads, void* out, int B,
+                      int Hq, int Hkv, int N, int d, int W, float scale, void* stream) {
+    if (lambda_heads && (reinterpret_cast<uintptr_t>(lambda_heads) & 3u) != 0)
+        return SWA_ERR_ALIGN;
+    return diff_common(q1, k1, q2, k2, v, lambda_heads ? 0.f : lambda, lambda_heads, out, B, Hq,
+                       Hkv, N, d, W, scale, stream);
 }
 
 int swa_device_status(void* stream) {

@@ -55,8 +55,8 @@ def useful_flops(kind: str, B: int, Hq: int, N: int, d: int, W: int, stride: int
     if kind == "global":  # stride carries the number of global prefix tokens
         p = pairs_global(N, W, stride)
         return 4.0 * d * p * B * Hq
-    if kind == "diff":
-        p = pairs_causal(N)
+    if kind == "diff":  # both maps under the window W (W >= N: causal)
+        p = pairs_window(N, W)
         return 8.0 * d * p * B * Hq
     raise ValueError(kind)
 

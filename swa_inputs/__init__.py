@@ -51,7 +51,7 @@ class Workload:
         return dataclasses.replace(self, **kw)
 
 
-# The five workloads of the headline measurement.  Index = the seed offset.
+# The workloads of the measurements (and the full-size parity cases).  Index = the seed offset.
 WORKLOADS = {
     # small causal SWA case: B=1, H=2, N=512, d=64, W=64
     "swa_small": Workload("swa_small", "swa", 1, 2, 2, 512, 64, 64, seed_index=1),
@@ -65,6 +65,9 @@ WORKLOADS = {
     # differential causal attention with an attention sink on key 0 of K1
     "diff": Workload("diff", "diff", 1, 16, 16, 8192, 64, 8192, lam=0.8, sink_shift=3.0,
                      seed_index=5),
+    # a differential head inside an SWA layer: both maps under a W=1024 window
+    "diff_swa": Workload("diff_swa", "diff", 1, 16, 16, 16384, 64, 1024, lam=0.8, sink_shift=3.0,
+                         seed_index=8),
     # window plus a global prefix (Longformer-style [CLS] / question tokens): W=512, 64 global
     "global": Workload("global", "global", 1, 16, 16, 16384, 64, 512, stride=64, seed_index=7),
     # decode against a W-slot rolling KV cache, Mistral-7B heads: one new query per

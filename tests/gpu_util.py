@@ -41,6 +41,9 @@ def run_gpu(w: swa_inputs.Workload, inp: dict, check_canary: bool = True) -> np.
     elif w.kind == "strided":
         pkg.strided_attn_fwd(d["q"], d["k"], d["v"], out, w.B, w.Hq, w.Hkv, w.N, w.d, w.W,
                              w.stride, w.scale)
+    elif w.W < w.N:
+        pkg.diff_swa_attn_fwd(d["q1"], d["k1"], d["q2"], d["k2"], d["v"], w.lam, None, out, w.B,
+                              w.Hq, w.Hkv, w.N, w.d, w.W, w.scale)
     else:
         pkg.diff_attn_fwd(d["q1"], d["k1"], d["q2"], d["k2"], d["v"], w.lam, out, w.B, w.Hq,
                           w.Hkv, w.N, w.d, w.scale)
@@ -58,7 +61,7 @@ def run_oracle(w: swa_inputs.Workload, inp: dict, rows=None) -> np.ndarray:
         return oracle.attn(inp["q"], inp["k"], inp["v"], w.W, w.scale, kind="strided",
                            stride=w.stride, rows=rows)
     return oracle.diff(inp["q1"], inp["k1"], inp["q2"], inp["k2"], inp["v"], w.lam, w.scale,
-                       rows=rows)
+                       rows=rows, W=w.W if w.W < w.N else 0)
 
 
 def assert_close(w: swa_inputs.Workload, got: np.ndarray, ref: np.ndarray, label: str = ""):

@@ -154,3 +154,13 @@ def test_lse_global_and_per_head_lambda_validation(L):
     assert L.global_attn_fwd(None, P, P, P, 1, 2, 2, 128, 64, 16, 4, 0.125, None) == 1
     assert L.diff_attn_fwd_heads(P, P, P, P, P, None, P, 1, 2, 2, 128, 64, 0.125, None) == 1
     assert L.diff_attn_fwd_heads(P, P, P, P, P, P + 2, P, 1, 2, 2, 128, 64, 0.125, None) == 3
+
+
+def test_diff_window_validation(L):
+    f = L.diff_swa_attn_fwd
+    assert f(P, P, None, P, P, 0.8, None, P, 1, 2, 2, 128, 64, 32, 0.125, None) == 1
+    assert f(P, P, P, P, P, 0.8, None, P, 1, 2, 2, 128, 64, 0, 0.125, None) == 2
+    assert f(P, P, P, P, P, float("nan"), None, P, 1, 2, 2, 128, 64, 32, 0.125, None) == 7
+    assert f(P, P, P, P, P, 0.8, P + 2, P, 1, 2, 2, 128, 64, 32, 0.125, None) == 3
+    assert f(P, P, P, P, P + 8, 0.8, None, P, 1, 2, 2, 128, 64, 32, 0.125, None) == 3
+    assert f(P, P, P, P, P, 0.8, None, P, 1, 2, 2, 128, 96, 32, 0.125, None) == 4

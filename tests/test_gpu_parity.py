@@ -238,6 +238,65 @@ def test_diff_per_head_lambda(heads):
         assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
 
 
+# ------------------------------------------------------ differential head in an SWA layer
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("heads", [(1, 1), (4, 2), (3, 3)])
+def test_diff_window_sweep(d, heads):
+    Hq, Hkv = heads
+    for N in (1, 60, 200, 513):
+        for W in sorted({1, 2, 63, 128, 129, 300, max(1, N - 1)}):
+            if W >= N:
+                continue
+            lam = (0.0, 0.8, 1.0)[(N + W) % 3]
+            check(_w("diff", 1, Hq, Hkv, N, d, W, lam=lam, seed=N * 3 + W),
+                  label=f"diff N={N} W={W} lam={lam} d={d} {heads}")
+
+
+def test_diff_window_full_size_sampled():
+    _full_size("diff_swa")
+
+
+def test_diff_window_per_head_lambda_and_limits():
+    import oracle
+
+    Hq, Hkv, N, d, W = 4, 2, 700, 64, 130
+    w = _w("diff", 2, Hq, Hkv, N, d, W, lam=0.0, seed=77)
+    inp = swa_inputs.make_inputs(w)
+    t = {n: to_dev(a) for n, a in inp.items()}
+    lams = np.array([-0.3, 0.0, 0.6, 1.1], dtype=np.float32)
+    lam_dev = torch.from_numpy(lams).cuda()
+    out, buf = out_like(t["q1"])
+    pkg.diff_swa_attn_fwd(t["q1"], t["k1"], t["q2"], t["k2"], t["v"], 0.0, lam_dev, out, 2, Hq,
+                          Hkv, N, d, W, w.scale)
+    torch.cuda.synchronize()
+    assert pkg.swa_device_status() == 0
+    assert canary_intact(buf, out.numel())
+    ref = oracle.diff_heads(inp["q1"], inp["k1"], inp["q2"], inp["k2"], inp["v"], lams, w.scale,
+                            W=W)
+    assert_close(w, to_f64(out), ref, "windowed diff, per-head lambda")
+    # W >= N is the causal call, bit for bit (per-head and scalar lambda)
+    a, _ = out_like(t["q1"])
+    b, _ = out_like(t["q1"])
+    pkg.diff_swa_attn_fwd(t["q1"], t["k1"], t["q2"], t["k2"], t["v"], 0.0, lam_dev, a, 2, Hq, Hkv,
+                          N, d, N + 5, w.scale)
+    pkg.diff_attn_fwd_heads(t["q1"], t["k1"], t["q2"], t["k2"], t["v"], lam_dev, b, 2, Hq, Hkv, N,
+                            d, w.scale)
+    torch.cuda.synchronize()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    pkg.diff_swa_attn_fwd(t["q1"], t["k1"], t["q2"], t["k2"], t["v"], 0.8, None, a, 2, Hq, Hkv, N,
+                          d, N, w.scale)
+    pkg.diff_attn_fwd(t["q1"], t["k1"], t["q2"], t["k2"], t["v"], 0.8, b, 2, Hq, Hkv, N, d,
+                      w.scale)
+    torch.cuda.synchronize()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    # W = 1: both maps keep only the row's own key, out_i = (1 - lambda) v_i
+    pkg.diff_swa_attn_fwd(t["q1"], t["k1"], t["q2"], t["k2"], t["v"], 0.5, None, a, 2, Hq, Hkv, N,
+                          d, 1, w.scale)
+    torch.cuda.synchronize()
+    v = np.repeat(swa_inputs.bf16_bits_to_f64(inp["v"]), Hq // Hkv, axis=1)
+    assert np.max(np.abs(to_f64(a) - 0.5 * v)) <= 2.0 ** -8 * np.max(np.abs(v))
+
+
 # ------------------------------------------------------------------------- watchdog
 def test_watchdog_reports_timeout_and_clears():
     assert pkg.swa_device_status() == 0
