@@ -51,12 +51,13 @@ FLUSH_BYTES = 256 * 2**20  # written between timed launches when a workload fits
 # + dram__bytes_write.sum), keyed by workload, with the hash of the kernel sources it was
 # taken on.  A changed kernel invalidates the figure (reported as null).
 TRAFFIC = {
-    "mistral_swa": (329.38e6, "afe1deb0fc2a3631"),
-    "gemma_swa": (856.23e6, "afe1deb0fc2a3631"),
-    "strided": (113.29e6, "afe1deb0fc2a3631"),
-    "diff": (95.79e6, "afe1deb0fc2a3631"),
-    "global": (114.97e6, "afe1deb0fc2a3631"),
-    "mistral_decode": (486.66e6, "afe1deb0fc2a3631"),
+    "mistral_swa": (331.90e6, "94d961ac651fde97"),
+    "gemma_swa": (858.72e6, "94d961ac651fde97"),
+    "strided": (113.64e6, "94d961ac651fde97"),
+    "diff": (96.09e6, "94d961ac651fde97"),
+    "diff_swa": (191.63e6, "94d961ac651fde97"),
+    "global": (114.90e6, "94d961ac651fde97"),
+    "mistral_decode": (486.76e6, "94d961ac651fde97"),
 }
 
 
