@@ -93,6 +93,10 @@ def _load():
             lib.oracle_lse.restype = ctypes.c_int
             lib.oracle_lse.argtypes = [ctypes.c_int, _P, _P, _P, _I64, _I64, _I64, _I64, _I64,
                                        _I64, _I64, ctypes.c_double, _P, _I64]
+            lib.oracle_attn_bwd.restype = ctypes.c_int
+            lib.oracle_attn_bwd.argtypes = [ctypes.c_int, _P, _P, _P, _P, _P, _P, _P, _I64,
+                                            _I64, _I64, _I64, _I64, _I64, _I64,
+                                            ctypes.c_double, ctypes.c_int]
             lib.oracle_cache_slot.restype = ctypes.c_int64
             lib.oracle_cache_slot.argtypes = [_I64, _I64]
             lib.oracle_max_threads.restype = ctypes.c_int
@@ -241,6 +245,26 @@ def lse(q, k, W: int, scale: float, kind: str = "window", stride: int = 0, rows=
     if rc != 0:
         raise ValueError(f"oracle_lse rejected its arguments (code {rc})")
     return out
+
+
+def attn_bwd(q, k, v, dout, W: int, scale: float, kind: str = "window", stride: int = 0,
+             nthreads: int = 0):
+    """Gradients (dq, dk, dv) in fp64 of the masked attention forward for an upstream
+    gradient ``dout`` = dL/dout ([B, Hq, N, d]).  dk and dv sum over the query heads that
+    share a KV head."""
+    lib = _load()
+    q64, k64, v64, g64 = _f64(q), _f64(k), _f64(v), _f64(dout)
+    B, Hq, N, d = q64.shape
+    Hkv = k64.shape[1]
+    dq = np.empty_like(q64)
+    dk = np.empty_like(k64)
+    dv = np.empty_like(v64)
+    rc = lib.oracle_attn_bwd(KINDS[kind], _ptr(q64), _ptr(k64), _ptr(v64), _ptr(g64), _ptr(dq),
+                             _ptr(dk), _ptr(dv), B, Hq, Hkv, N, d, int(W), int(stride),
+                             float(scale), int(nthreads))
+    if rc != 0:
+        raise ValueError(f"oracle_attn_bwd rejected its arguments (code {rc})")
+    return dq, dk, dv
 
 
 def cache_slot(j: int, W: int) -> int:

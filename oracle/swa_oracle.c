@@ -38,6 +38,8 @@
  *   W; W >= N is the causal mask of the page's formulas, a smaller W a differential head
  *   inside an SWA layer ([AV] opening list: the variants coexist, most layers SWA and a few
  *   differential heads).
+ *   Backward (oracle_attn_bwd): the gradients of step 4's output with respect to q, k and
+ *   v by the chain rule through the row softmax (written out above that function).
  *   Decode against a rolling cache ([SWA] §4.2): the K, V of absolute position j sit in
  *   cache slot j mod W (the note's 1-indexed slot (i-1) mod W); a query at position t reads
  *   the positions max(0, t-W+1) .. t through their slots, steps 2-4 as above.
@@ -348,6 +350,82 @@ int oracle_lse(int kind, const double* q, const double* k, double* lse, int64_t 
             }
     free(M);
     free(z);
+    return 0;
+}
+
+/*
+ * Gradients of the masked attention forward (the backward pass that training with SWA needs,
+ * [AV] exercises 2-3 train models with SWA layers).  For a loss L with dL/dout = dout, the
+ * chain rule through out_i = sum_j a_ij v_j and the row softmax a_ij = softmax_j(z_ij),
+ * z_ij = scale q_i.k_j + M_ij, gives, row by row:
+ *   dv_j  += a_ij dout_i                               (out is linear in v)
+ *   da_ij  = dout_i . v_j
+ *   dz_ij  = a_ij (da_ij - sum_j' a_ij' da_ij')        (the softmax Jacobian)
+ *   dq_i  += scale sum_j dz_ij k_j,   dk_j += scale dz_ij q_i
+ * Masked pairs have a_ij = 0 and contribute nothing.  A KV head's dk and dv sum the
+ * contributions of all g query heads that read it.  dq: [B, Hq, N, d]; dk, dv: [B, Hkv, N, d].
+ */
+int oracle_attn_bwd(int kind, const double* q, const double* k, const double* v,
+                    const double* dout, double* dq, double* dk, double* dv, int64_t B,
+                    int64_t Hq, int64_t Hkv, int64_t N, int64_t d, int64_t W, int64_t stride,
+                    double scale, int nthreads) {
+    if (check_shape(B, Hq, Hkv, N, d)) return 2;
+    if (kind != MASK_WINDOW && kind != MASK_STRIDED && kind != MASK_CAUSAL && kind != MASK_GLOBAL)
+        return 2;
+    if (kind != MASK_CAUSAL && W < 1) return 2;
+    if (kind == MASK_STRIDED && stride < 1) return 2;
+    if (kind == MASK_GLOBAL && stride < 0) return 2;
+    const int64_t g = Hq / Hkv;
+    memset(dq, 0, sizeof(double) * (size_t)(B * Hq * N * d));
+    memset(dk, 0, sizeof(double) * (size_t)(B * Hkv * N * d));
+    memset(dv, 0, sizeof(double) * (size_t)(B * Hkv * N * d));
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#endif
+    /* one (batch, KV head) per task: its dk and dv are written by that task only */
+#pragma omp parallel
+    {
+        double* M = (double*)malloc(sizeof(double) * (size_t)N);
+        double* z = (double*)malloc(sizeof(double) * (size_t)N);
+        double* a = (double*)malloc(sizeof(double) * (size_t)N);
+        double* da = (double*)malloc(sizeof(double) * (size_t)N);
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t t = 0; t < B * Hkv; ++t) {
+            const int64_t b = t / Hkv, hk = t % Hkv;
+            const size_t koff = (size_t)((b * Hkv + hk) * N * d);
+            for (int64_t h = hk * g; h < (hk + 1) * g; ++h) {
+                for (int64_t i = 0; i < N; ++i) {
+                    const size_t qoff = (size_t)(((b * Hq + h) * N + i) * d);
+                    mask_row(kind, i, W, stride, M);
+                    softmax_row(q + qoff, k + koff, d, i, scale, M, z, a);
+                    double delta = 0.0;
+                    for (int64_t j = 0; j <= i; ++j) {
+                        da[j] = 0.0;
+                        if (M[j] != 0.0) continue;  /* masked */
+                        const double* vj = v + koff + (size_t)(j * d);
+                        double dot = 0.0;
+                        for (int64_t c = 0; c < d; ++c) dot += dout[qoff + c] * vj[c];
+                        da[j] = dot;
+                        delta += a[j] * dot;
+                    }
+                    for (int64_t j = 0; j <= i; ++j) {
+                        if (M[j] != 0.0) continue;
+                        const double dzj = a[j] * (da[j] - delta);
+                        const size_t jo = koff + (size_t)(j * d);
+                        for (int64_t c = 0; c < d; ++c) {
+                            dq[qoff + c] += scale * dzj * k[jo + c];
+                            dk[jo + c] += scale * dzj * q[qoff + c];
+                            dv[jo + c] += a[j] * dout[qoff + c];
+                        }
+                    }
+                }
+            }
+        }
+        free(M);
+        free(z);
+        free(a);
+        free(da);
+    }
     return 0;
 }
 

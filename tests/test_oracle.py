@@ -603,3 +603,60 @@ def test_global_brute_force_and_pair_count(oracle_mod, N):
                                        rtol=0, atol=1e-12)
             assert oracle_mod.pair_count(N, W, "global", ng) == int(allowed.sum())
             assert flops.pairs_global(N, W, ng) == int(allowed.sum())
+
+
+# ------------------------------------------------------------------ backward (gradients)
+def _bwd_inputs(seed, B=1, Hq=4, Hkv=2, N=13, d=5):
+    rng = np.random.default_rng(seed)
+    return (rng.standard_normal((B, Hq, N, d)), rng.standard_normal((B, Hkv, N, d)),
+            rng.standard_normal((B, Hkv, N, d)), rng.standard_normal((B, Hq, N, d)))
+
+
+@pytest.mark.parametrize("kind,W,stride", [("window", 4, 0), ("window", 1, 0), ("causal", 0, 0),
+                                           ("strided", 3, 4), ("global", 3, 2)])
+def test_bwd_matches_central_differences(oracle_mod, kind, W, stride):
+    """Every entry of dq, dk, dv against a central difference of L = sum(dout * out) through
+    the (separately pinned) forward oracle: the definition of a gradient, not its formula."""
+    q, k, v, g = _bwd_inputs(90 + W + stride)
+    scale, h = 0.45, 1e-5
+    dq, dk, dv = oracle_mod.attn_bwd(q, k, v, g, W, scale, kind=kind, stride=stride)
+
+    def loss(q_, k_, v_):
+        return float(np.sum(g * oracle_mod.attn(q_, k_, v_, W, scale, kind=kind, stride=stride)))
+
+    for name, x, grad in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+        fd = np.empty_like(x)
+        for idx in np.ndindex(x.shape):
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += h
+            xm[idx] -= h
+            args_p = {"q": q, "k": k, "v": v}
+            args_m = dict(args_p)
+            args_p[name], args_m[name] = xp, xm
+            fd[idx] = (loss(**{n + "_": a for n, a in args_p.items()}) -
+                       loss(**{n + "_": a for n, a in args_m.items()})) / (2 * h)
+        assert np.max(np.abs(fd - grad)) < 1e-7 * max(1.0, np.max(np.abs(grad))), name
+
+
+def test_bwd_w1_closed_form(oracle_mod):
+    # a row that keeps only its own key has a constant softmax: no gradient to q or k, and
+    # dv_j is the sum of dout_j over the query heads that read KV head j
+    q, k, v, g = _bwd_inputs(95, B=2, Hq=6, Hkv=2, N=9, d=4)
+    dq, dk, dv = oracle_mod.attn_bwd(q, k, v, g, 1, 0.7)
+    assert np.all(dq == 0.0) and np.all(dk == 0.0)
+    expect = g.reshape(2, 2, 3, 9, 4).sum(axis=2)
+    np.testing.assert_allclose(dv, expect, rtol=0, atol=1e-14)
+
+
+def test_bwd_gqa_equals_repeated_kv_and_w_ge_n_is_causal(oracle_mod):
+    q, k, v, g = _bwd_inputs(96, Hq=4, Hkv=1, N=11, d=3)
+    dq, dk, dv = oracle_mod.attn_bwd(q, k, v, g, 5, 0.6)
+    dq_r, dk_r, dv_r = oracle_mod.attn_bwd(q, np.repeat(k, 4, axis=1), np.repeat(v, 4, axis=1),
+                                           g, 5, 0.6)
+    np.testing.assert_allclose(dq, dq_r, rtol=0, atol=1e-14)
+    np.testing.assert_allclose(dk, dk_r.sum(axis=1, keepdims=True), rtol=0, atol=1e-13)
+    np.testing.assert_allclose(dv, dv_r.sum(axis=1, keepdims=True), rtol=0, atol=1e-13)
+    causal = oracle_mod.attn_bwd(q, k, v, g, 0, 0.6, kind="causal")
+    for W in (11, 30):
+        for a, b in zip(oracle_mod.attn_bwd(q, k, v, g, W, 0.6), causal):
+            assert np.array_equal(a, b)
