@@ -185,6 +185,32 @@ int strided_attn_fwd_noalloc(const void* q, const void* k, const void* v, void* 
  * SWA_ERR_TOO_LARGE if workspace_bytes is too small.
  */
 size_t swa_decode_workspace_bytes(int B, int Hq, int W, int d);
+
+/*
+ * Backward pass of causal sliding-window attention (the forward of [SWA] §3.1; training
+ * with SWA layers is [AV] exercises 2-3).  With dout = dL/dout and a_ij the forward's
+ * softmax weights over the window max(0, i-W+1) <= j <= i:
+ *   dv_j = sum_i a_ij dout_i
+ *   ds_ij = a_ij (dout_i . v_j - delta_i),   delta_i = dout_i . out_i
+ *   dq_i = scale sum_j ds_ij k_j,            dk_j = scale sum_i ds_ij q_i
+ * dk and dv of a KV head sum over the Hq / Hkv query heads that read it.
+ *   q, out, dout, dq:  bf16 [B, Hq, N, d] device, contiguous, 16-byte aligned
+ *   k, v, dk, dv:      bf16 [B, Hkv, N, d] device, contiguous, 16-byte aligned
+ *   lse:               fp32 [B, Hq, N] device, the row log-sum-exp that swa_attn_fwd_lse
+ *                      wrote with the same q, k, W and scale (a_ij = exp(scale q_i.k_j - lse_i))
+ *   out:               the forward output of that call
+ *   workspace:         device scratch of at least swa_attn_bwd_workspace_bytes(B, Hq, N)
+ *                      bytes, 16-byte aligned, owned by the caller (it receives delta)
+ * dq, dk and dv are overwritten (not accumulated into).  Three kernels run on `stream`: delta,
+ * then dk / dv (one CTA per 128-key tile), then dq (one CTA per 128-row tile); the result is
+ * deterministic.  W >= 1 (W > N is N); B * Hq <= 65535; d 64 or 128.  Errors as for
+ * swa_attn_fwd; SWA_ERR_TOO_LARGE if workspace_bytes is too small.
+ */
+size_t swa_attn_bwd_workspace_bytes(int B, int Hq, int N);
+int swa_attn_bwd(const void* q, const void* k, const void* v, const void* out, const float* lse,
+                 const void* dout, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int N,
+                 int d, int W, float scale, void* workspace, size_t workspace_bytes,
+                 void* stream);
 int swa_decode_fwd(const void* q, const void* k_cache, const void* v_cache, const int* pos,
                    void* out, int B, int Hq, int Hkv, int W, int d, float scale, void* workspace,
                    size_t workspace_bytes, void* stream);

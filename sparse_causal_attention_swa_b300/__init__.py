@@ -9,6 +9,7 @@ and streams.  There is no CPU fallback: if the library is missing, every call ra
 Low-level calls (pointers or tensors, explicit sizes, asynchronous on ``stream``):
     swa_attn_fwd, strided_attn_fwd, diff_attn_fwd, diff_attn_fwd_heads, diff_swa_attn_fwd,
     strided_attn_fwd_noalloc, swa_attn_fwd_lse, strided_attn_fwd_lse, global_attn_fwd,
+    swa_attn_bwd_workspace_bytes, swa_attn_bwd,
     swa_decode_workspace_bytes, swa_decode_fwd, swa_cache_append, swa_chunk_fwd,
     swa_cache_gather,
     swa_status_string, swa_device_status, swa_watchdog_selftest
@@ -63,6 +64,11 @@ def load():
         lib.diff_attn_fwd_heads.restype = I
         lib.diff_swa_attn_fwd.argtypes = [P, P, P, P, P, F, P, P, I, I, I, I, I, I, F, P]
         lib.diff_swa_attn_fwd.restype = I
+        lib.swa_attn_bwd_workspace_bytes.argtypes = [I, I, I]
+        lib.swa_attn_bwd_workspace_bytes.restype = ctypes.c_size_t
+        lib.swa_attn_bwd.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, P,
+                                     ctypes.c_size_t, P]
+        lib.swa_attn_bwd.restype = I
         SZ = ctypes.c_size_t
         lib.swa_decode_workspace_bytes.argtypes = [I, I, I, I]
         lib.swa_decode_workspace_bytes.restype = SZ
@@ -199,6 +205,20 @@ def diff_swa_attn_fwd(q1, k1, q2, k2, v, lam, lam_heads, out, B, Hq, Hkv, N, d, 
                                     None if lam_heads is None else _ptr(lam_heads), _ptr(out), B,
                                     Hq, Hkv, N, d, int(W), float(scale), _stream(stream)),
            "diff_swa_attn_fwd")
+
+
+def swa_attn_bwd_workspace_bytes(B, Hq, N) -> int:
+    return int(load().swa_attn_bwd_workspace_bytes(B, Hq, N))
+
+
+def swa_attn_bwd(q, k, v, out, lse, dout, dq, dk, dv, B, Hq, Hkv, N, d, W, scale, workspace,
+                 workspace_bytes, stream=None):
+    """Gradients dq, dk, dv of causal SWA for the upstream gradient ``dout``; ``out`` and
+    ``lse`` come from swa_attn_fwd_lse with the same arguments."""
+    _check(load().swa_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout),
+                               _ptr(dq), _ptr(dk), _ptr(dv), B, Hq, Hkv, N, d, int(W),
+                               float(scale), _ptr(workspace), int(workspace_bytes),
+                               _stream(stream)), "swa_attn_bwd")
 
 
 def swa_device_status(stream=None) -> int:

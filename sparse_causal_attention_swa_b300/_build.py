@@ -10,7 +10,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 LIB = os.path.join(PKG, "libswa_b300.so")
 SOURCES = [os.path.join(CSRC, "swa_api.cu")]
-DEPS = SOURCES + [os.path.join(CSRC, f) for f in ("attn_fwd.cuh", "decode.cuh", "ptx.cuh")] + [
+DEPS = SOURCES + [os.path.join(CSRC, f) for f in ("attn_fwd.cuh", "attn_bwd.cuh", "decode.cuh", "ptx.cuh")] + [
     os.path.join(ROOT, "include", "swa_b300.h")]
 
 NVCC_FLAGS = [

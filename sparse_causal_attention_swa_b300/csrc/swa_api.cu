@@ -14,6 +14,7 @@
 #include <vector>
 
 #include "attn_fwd.cuh"
+#include "attn_bwd.cuh"
 #include "decode.cuh"
 #include "swa_b300.h"
 
@@ -36,6 +37,7 @@ struct DeviceState {
     int num_sms = 0;
     bool attr_set[2][3] = {};
     bool dec_attr_set[2][5] = {};
+    bool bwd_attr_set[2][2] = {};
     // strided tile lists, keyed by (N, W, stride, rows per block, compact-key cap)
     std::map<std::tuple<int, int, int, int, int>, int*> tile_lists;
 };
@@ -317,6 +319,46 @@ int dispatch_decode(int g, const swa::DecParams& dp, int B, int Hkv, cudaStream_
     return launch_decode<D, 16>(dp, B, Hkv, stream, st, 4);
 }
 
+}  // namespace
+
+namespace {
+size_t bwd_workspace_bytes(int B, int Hq, int N) {
+    return ((size_t)B * Hq * N * sizeof(float) + 255) / 256 * 256;
+}
+
+template <int D, int KIND>
+int launch_bwd(const swa::BwdParams& bp, int n_tiles, int n_mats, cudaStream_t stream,
+               DeviceState& st) {
+    using L = swa::BwdLayout<D>;
+    auto kern = swa::attn_bwd_kernel<D, KIND>;
+    bool& set = st.bwd_attr_set[D == 128 ? 1 : 0][KIND];
+    if (!set) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::BYTES) !=
+            cudaSuccess)
+            return SWA_ERR_CUDA;
+        set = true;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)n_tiles, (unsigned)n_mats, 1);
+    cfg.blockDim = dim3(swa::BWD_THREADS, 1, 1);
+    cfg.dynamicSmemBytes = L::BYTES;
+    cfg.stream = stream;
+    return cudaLaunchKernelEx(&cfg, kern, bp) == cudaSuccess ? SWA_OK : SWA_ERR_CUDA;
+}
+
+template <int D>
+int run_bwd(const swa::BwdParams& bp, const void* out, const void* dout, float* delta,
+            cudaStream_t stream, DeviceState& st) {
+    const long long rows = (long long)bp.B * bp.Hq * bp.N;
+    const int n_tiles = (bp.N + swa::BM - 1) / swa::BM;
+    swa::bwd_delta_kernel<D><<<(unsigned)((rows + 255) / 256), 256, 0, stream>>>(
+        static_cast<const __nv_bfloat16*>(out), static_cast<const __nv_bfloat16*>(dout), delta,
+        rows);
+    if (cudaPeekAtLastError() != cudaSuccess) return SWA_ERR_CUDA;
+    int rc = launch_bwd<D, 0>(bp, n_tiles, bp.B * bp.Hkv, stream, st);
+    if (rc) return rc;
+    return launch_bwd<D, 1>(bp, n_tiles, bp.B * bp.Hq, stream, st);
+}
 }  // namespace
 
 extern "C" {
@@ -641,6 +683,58 @@ int swa_decode_fwd(const void* q, const void* k_cache, const void* v_cache, cons
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (d == 128) return dispatch_decode<128>(Hq / Hkv, dp, B, Hkv, s, *st);
     return dispatch_decode<64>(Hq / Hkv, dp, B, Hkv, s, *st);
+}
+
+
+size_t swa_attn_bwd_workspace_bytes(int B, int Hq, int N) {
+    if (B < 1 || Hq < 1 || N < 1) return 0;
+    return bwd_workspace_bytes(B, Hq, N);
+}
+
+int swa_attn_bwd(const void* q, const void* k, const void* v, const void* out, const float* lse,
+                 const void* dout, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int N,
+                 int d, int W, float scale, void* workspace, size_t workspace_bytes,
+                 void* stream) {
+    if (!q || !k || !v || !out || !lse || !dout || !dq || !dk || !dv || !workspace)
+        return SWA_ERR_NULL;
+    int rc = check_common(B, Hq, Hkv, N, d, scale);
+    if (rc) return rc;
+    if (W < 1) return SWA_ERR_SHAPE;
+    if (W > N) W = N;
+    // grid: (row tiles, heads); the second grid dimension is at most 65535
+    if ((long long)B * Hq > 65535 || (long long)B * Hq * N > (1ll << 38)) return SWA_ERR_SHAPE;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(dout) ||
+        !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(workspace) ||
+        (reinterpret_cast<uintptr_t>(lse) & 3u) != 0)
+        return SWA_ERR_ALIGN;
+    if (workspace_bytes < bwd_workspace_bytes(B, Hq, N)) return SWA_ERR_TOO_LARGE;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceState* st = nullptr;
+    if ((rc = current_device_state(&st))) return rc;
+    swa::BwdParams bp;
+    std::memset(&bp, 0, sizeof(bp));
+    if ((rc = make_map(&bp.tm_q, q, d, N, d, (long long)B * Hq, (long long)N * d))) return rc;
+    if ((rc = make_map(&bp.tm_do, dout, d, N, d, (long long)B * Hq, (long long)N * d))) return rc;
+    if ((rc = make_map(&bp.tm_k, k, d, N, d, (long long)B * Hkv, (long long)N * d))) return rc;
+    if ((rc = make_map(&bp.tm_v, v, d, N, d, (long long)B * Hkv, (long long)N * d))) return rc;
+    bp.lse = lse;
+    bp.delta = static_cast<const float*>(workspace);
+    bp.dq = static_cast<__nv_bfloat16*>(dq);
+    bp.dk = static_cast<__nv_bfloat16*>(dk);
+    bp.dv = static_cast<__nv_bfloat16*>(dv);
+    bp.status = st->status;
+    bp.wait_limit_ns = kWaitLimitNs;
+    bp.B = B;
+    bp.Hq = Hq;
+    bp.Hkv = Hkv;
+    bp.N = N;
+    bp.W = W;
+    bp.scale = scale;
+    bp.scale_log2 = scale * 1.4426950408889634f;
+    float* delta = static_cast<float*>(workspace);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (d == 128) return run_bwd<128>(bp, out, dout, delta, s, *st);
+    return run_bwd<64>(bp, out, dout, delta, s, *st);
 }
 
 int swa_cache_append(const void* k_new, const void* v_new, void* k_cache, void* v_cache,

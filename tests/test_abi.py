@@ -164,3 +164,31 @@ def test_diff_window_validation(L):
     assert f(P, P, P, P, P, 0.8, P + 2, P, 1, 2, 2, 128, 64, 32, 0.125, None) == 3
     assert f(P, P, P, P, P + 8, 0.8, None, P, 1, 2, 2, 128, 64, 32, 0.125, None) == 3
     assert f(P, P, P, P, P, 0.8, None, P, 1, 2, 2, 128, 96, 32, 0.125, None) == 4
+
+
+def test_bwd_validation(L):
+    f = L.swa_attn_bwd
+    n = L.swa_attn_bwd_workspace_bytes(2, 4, 300)
+    assert n >= 2 * 4 * 300 * 4 and n % 256 == 0
+    assert L.swa_attn_bwd_workspace_bytes(0, 4, 300) == 0
+    ok = dict(q=P, k=P, v=P, out=P, lse=P, g=P, dq=P, dk=P, dv=P, B=2, Hq=4, Hkv=2, N=300, d=64,
+              W=50, scale=0.125, ws=P, nb=n)
+
+    def call(**kw):
+        a = {**ok, **kw}
+        return f(a["q"], a["k"], a["v"], a["out"], a["lse"], a["g"], a["dq"], a["dk"], a["dv"],
+                 a["B"], a["Hq"], a["Hkv"], a["N"], a["d"], a["W"], a["scale"], a["ws"], a["nb"],
+                 None)
+
+    assert call(lse=None) == 1
+    assert call(dv=None) == 1
+    assert call(ws=None) == 1
+    assert call(W=0) == 2
+    assert call(Hq=4, Hkv=3) == 2
+    assert call(B=1, Hq=65536, Hkv=1) == 2
+    assert call(d=96) == 4
+    assert call(scale=float("inf")) == 7
+    assert call(dk=P + 8) == 3
+    assert call(lse=P + 2) == 3
+    assert call(ws=P + 4) == 3
+    assert call(nb=n - 1) == 8
