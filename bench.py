@@ -39,31 +39,39 @@ from sparse_causal_attention_swa_b300 import flops as flopcount  # noqa: E402
 
 METRIC = "causal SWA fwd band-only TFLOP/s (Mistral shape, 1 B300) and % of BF16 peak"
 DEFAULT_WORKLOAD = "mistral_swa"
-KERNEL_SOURCES = ["sparse_causal_attention_swa_b300/csrc/attn_fwd.cuh",
-                  "sparse_causal_attention_swa_b300/csrc/decode.cuh",
-                  "sparse_causal_attention_swa_b300/csrc/ptx.cuh",
-                  "sparse_causal_attention_swa_b300/csrc/swa_api.cu"]
+_CSRC = "sparse_causal_attention_swa_b300/csrc/"
+# device sources of each kernel family (a traffic figure is valid while they are unchanged)
+KERNEL_SOURCES = {
+    "attn_fwd": [_CSRC + "attn_fwd.cuh", _CSRC + "ptx.cuh"],
+    "decode": [_CSRC + "decode.cuh", _CSRC + "ptx.cuh"],
+    "attn_bwd": [_CSRC + "attn_bwd.cuh", _CSRC + "attn_fwd.cuh", _CSRC + "ptx.cuh"],
+}
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 L2_BYTES = 126 * 2**20
 FLUSH_BYTES = 256 * 2**20  # written between timed launches when a workload fits in twice L2
 
 # DRAM traffic per launch of the dominant kernel, from one ncu capture (dram__bytes_read.sum
-# + dram__bytes_write.sum), keyed by workload, with the hash of the kernel sources it was
-# taken on.  A changed kernel invalidates the figure (reported as null).
+# + dram__bytes_write.sum), keyed by workload, with the hash of that kernel's device sources
+# (KERNEL_SOURCES of its family) when it was taken.  A changed kernel invalidates the figure
+# (reported as null).
 TRAFFIC = {
-    "mistral_swa": (331.90e6, "94d961ac651fde97"),
-    "gemma_swa": (858.72e6, "94d961ac651fde97"),
-    "strided": (113.64e6, "94d961ac651fde97"),
-    "diff": (96.09e6, "94d961ac651fde97"),
-    "diff_swa": (191.63e6, "94d961ac651fde97"),
-    "global": (114.90e6, "94d961ac651fde97"),
-    "mistral_decode": (486.76e6, "94d961ac651fde97"),
+    "mistral_swa": (331.90e6, "fcec546b72b2890d"),
+    "gemma_swa": (858.72e6, "fcec546b72b2890d"),
+    "strided": (113.64e6, "fcec546b72b2890d"),
+    "diff": (96.09e6, "fcec546b72b2890d"),
+    "diff_swa": (191.63e6, "fcec546b72b2890d"),
+    "global": (114.90e6, "fcec546b72b2890d"),
+    "mistral_decode": (486.76e6, "86fc03c18c809f41"),
 }
 
 
-def kernel_hash() -> str:
+def kernel_family(w: swa_inputs.Workload) -> str:
+    return {"decode": "decode", "bwd": "attn_bwd"}.get(w.kind, "attn_fwd")
+
+
+def kernel_hash(family: str = "attn_fwd") -> str:
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES:
+    for f in KERNEL_SOURCES[family]:
         with open(os.path.join(ROOT, f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -227,12 +235,57 @@ def cpu_baseline_decode(w, inp, budget_s: float = 15.0):
                       f"{dt:.1f} s, fp64, one thread)"}
 
 
+def bwd_prefix(w, inp, n_rows: int):
+    """The backward restricted to the first n_rows positions of the first batch entry (all
+    heads): with causal windows those rows and keys form a complete problem of their own."""
+    return {n: np.ascontiguousarray(a[:1, :, :n_rows]) for n, a in inp.items()}
+
+
+def run_oracle_bwd(w, inp, n_rows: int) -> float:
+    """Run the oracle's gradients on a prefix sub-problem; returns its useful FLOPs."""
+    import oracle
+
+    sub = bwd_prefix(w, inp, n_rows)
+    oracle.attn_bwd(sub["q"], sub["k"], sub["v"], sub["dout"], w.W, w.scale)
+    return flopcount.useful_flops("bwd", 1, w.Hq, n_rows, w.d, w.W)
+
+
+def bwd_sample_rows(w, inp, budget_s: float) -> int:
+    """Prefix length whose oracle backward takes about budget_s seconds."""
+    n = min(w.N, 256)
+    t0 = time.perf_counter()
+    run_oracle_bwd(w, inp, n)
+    dt = max(time.perf_counter() - t0, 1e-3)
+    # cost grows with the pairs: linearly in n once n exceeds W
+    per_pair = dt / flopcount.pairs_window(n, w.W)
+    while n < w.N and flopcount.pairs_window(min(w.N, 2 * n), w.W) * per_pair < budget_s:
+        n = min(w.N, 2 * n)
+    return n
+
+
+def cpu_baseline_bwd(w, inp, budget_s: float = 15.0):
+    import oracle
+
+    oracle.build()
+    inp = oracle_inputs_f64(inp)
+    n = bwd_sample_rows(w, inp, budget_s)
+    t0 = time.perf_counter()
+    fl = run_oracle_bwd(w, inp, n)
+    dt = time.perf_counter() - t0
+    return {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": min(oracle.max_threads(), w.Hkv),
+            "kind": "oracle",
+            "sample": f"the first {n} positions of all {w.Hq} heads of {w.name} ({fl:.3e} useful "
+                      f"FLOPs, {dt:.1f} s, fp64, one thread per KV head)"}
+
+
 def cpu_baseline(w, inp, budget_s: float = 15.0):
     """Time the oracle as it stands on the host cores over a bounded row sample."""
     import oracle
 
     if w.kind == "decode":
         return cpu_baseline_decode(w, inp, budget_s)
+    if w.kind == "bwd":
+        return cpu_baseline_bwd(w, inp, budget_s)
     oracle.build()
     inp = oracle_inputs_f64(inp)
     probe = oracle_sample_rows(w, 4, seed=w.seed)
@@ -260,6 +313,9 @@ def reference_arm(args, w, ws, rank):
     oracle.build()
     inp = oracle_inputs_f64(swa_inputs.make_inputs(w))
     fl_full, _ = workload_units(w)
+    if w.kind == "bwd":
+        reference_arm_bwd(args, w, ws, inp, fl_full)
+        return
     # size every step so warmup + steps stay within about two minutes
     probe = oracle_sample_rows(w, 4, seed=w.seed)
     t0 = time.perf_counter()
@@ -294,6 +350,34 @@ def reference_arm(args, w, ws, rank):
     print(json.dumps(line), flush=True)
 
 
+def reference_arm_bwd(args, w, ws, inp, fl_full):
+    import oracle
+
+    n = bwd_sample_rows(w, inp, 120.0 / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        run_oracle_bwd(w, inp, n)
+    fl = 0.0
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        fl += run_oracle_bwd(w, inp, n)
+    dt = time.perf_counter() - t0
+    value = fl / dt / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(w, fl_full),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s",
+                         "cores": min(oracle.max_threads(), w.Hkv), "kind": "oracle",
+                         "sample": f"the first {n} positions of all {w.Hq} heads per step "
+                                   f"(one thread per KV head)"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
 def workload_config(w, fl, flush=False):
     cfg = {"workload": w.name, "kind": w.kind, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "N": w.N,
            "d": w.d, "W": w.W, "scale": w.scale, "useful_flops_per_step": fl,
@@ -304,6 +388,9 @@ def workload_config(w, fl, flush=False):
         cfg["stride"] = w.stride
     if w.kind == "global":
         cfg["n_global"] = w.stride
+    if w.kind == "bwd":
+        cfg["flop_convention"] = ("10 d per (row, key) pair in the window: the products S, dP, "
+                                  "dV, dK, dQ (2.5 x the forward)")
     if w.kind == "diff":
         cfg["lambda"] = w.lam
         cfg["flop_convention"] = "8 d per (row, key) pair in the window (two attention maps)"
@@ -346,12 +433,32 @@ def launch(pkg, w, t, out, stream):
     elif w.kind == "global":
         pkg.global_attn_fwd(t["q"], t["k"], t["v"], out, w.B, w.Hq, w.Hkv, w.N, w.d, w.W,
                             w.stride, w.scale, stream)
+    elif w.kind == "bwd":  # out receives dq
+        pkg.swa_attn_bwd(t["q"], t["k"], t["v"], t["out_fwd"], t["lse"], t["dout"], out, t["dk"],
+                         t["dv"], w.B, w.Hq, w.Hkv, w.N, w.d, w.W, w.scale, t["ws"],
+                         t["ws"].numel(), stream)
     elif w.W < w.N:
         pkg.diff_swa_attn_fwd(t["q1"], t["k1"], t["q2"], t["k2"], t["v"], w.lam, None, out, w.B,
                               w.Hq, w.Hkv, w.N, w.d, w.W, w.scale, stream)
     else:
         pkg.diff_attn_fwd(t["q1"], t["k1"], t["q2"], t["k2"], t["v"], w.lam, out, w.B, w.Hq,
                           w.Hkv, w.N, w.d, w.scale, stream)
+
+
+def bwd_buffers(pkg, w, t, stream):
+    """Device buffers of a backward step besides q, k, v, dout: the forward's output and row
+    log-sum-exp (computed here, once, by the forward call), the delta workspace and dk, dv."""
+    import torch
+
+    q = t["q"]
+    t["out_fwd"] = torch.empty_like(q)
+    t["lse"] = torch.empty((w.B, w.Hq, w.N), dtype=torch.float32, device=q.device)
+    pkg.swa_attn_fwd_lse(q, t["k"], t["v"], t["out_fwd"], t["lse"], w.B, w.Hq, w.Hkv, w.N, w.d,
+                         w.W, w.scale, stream)
+    nb = pkg.swa_attn_bwd_workspace_bytes(w.B, w.Hq, w.N)
+    t["ws"] = torch.empty(nb, dtype=torch.uint8, device=q.device)
+    t["dk"] = torch.empty_like(t["k"])
+    t["dv"] = torch.empty_like(t["v"])
 
 
 def bench_workload(args, w, ws, rank, dev, want_cpu, want_e2e):
@@ -366,6 +473,8 @@ def bench_workload(args, w, ws, rank, dev, want_cpu, want_e2e):
     out = torch.empty_like(first)
     stream = torch.cuda.current_stream(dev)
     sh = stream.cuda_stream
+    if w.kind == "bwd":
+        bwd_buffers(pkg, w, t, sh)
     fl, algo_bytes = workload_units(w)
 
     for _ in range(args.warmup):
@@ -418,13 +527,15 @@ def bench_workload(args, w, ws, rank, dev, want_cpu, want_e2e):
     hbm_peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     achieved_tf = fl / (launch_ms * 1e-3) / 1e12
     tkey = TRAFFIC.get(w.name)
-    traffic = tkey[0] if (tkey and tkey[1] == kernel_hash()) else None
+    traffic = tkey[0] if (tkey and tkey[1] == kernel_hash(kernel_family(w))) else None
     tensor_bound = w.name not in ("swa_small",) and w.kind != "decode"
     if tensor_bound:
         roofline = {"bound": "tensor", "achieved": achieved_tf, "peak": bf16_peak,
                     "unit": "TFLOP/s", "frac": achieved_tf / bf16_peak, "traffic": traffic,
                     "peak_source": f"{peak_src} bf16_tflops (burst, kernel timed alone)",
-                    "kernel": f"attn_fwd_kernel<{w.d},{ {'swa': 0, 'strided': 1, 'global': 1, 'diff': 2}[w.kind]}>",
+                    "kernel": (f"bwd_delta_kernel<{w.d}> + attn_bwd_kernel<{w.d},0> (dk, dv) + "
+                               f"attn_bwd_kernel<{w.d},1> (dq), one call" if w.kind == "bwd" else
+                               f"attn_fwd_kernel<{w.d},{ {'swa': 0, 'strided': 1, 'global': 1, 'diff': 2}[w.kind]}>"),
                     "algorithmic_flops_per_launch": fl,
                     "hbm_gbs_algorithmic": algo_bytes / (launch_ms * 1e-3) / 1e9}
     else:
@@ -442,7 +553,8 @@ def bench_workload(args, w, ws, rank, dev, want_cpu, want_e2e):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic", "config": workload_config(w, fl, flush),
         "pct_of_bf16_peak": 100.0 * achieved_tf / bf16_peak,
-        "roofline": roofline, "gpu_launches": args.steps * (2 if w.kind == "decode" else 1),
+        "roofline": roofline,
+        "gpu_launches": args.steps * {"decode": 2, "bwd": 3}.get(w.kind, 1),
         "clocks": clk,
     }
     if ws > 1:
@@ -465,18 +577,30 @@ def e2e_measure(args, w, inp, pkg, dev, ws):
     dev_t = {n: torch.empty_like(h, device=dev) for n, h in host.items()}
     first = dev_t["q1"] if w.kind == "diff" else dev_t["q"]
     out = torch.empty_like(first)
-    out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     stream = torch.cuda.current_stream(dev)
     sh = stream.cuda_stream
-    h2d = sum(h.numel() * 2 for h in host.values())
-    d2h = out.numel() * 2
+    results = [out]
+    if w.kind == "bwd":
+        # the forward's output and log-sum-exp are inputs of the backward: made once on the
+        # device, then copied from pinned host buffers every step like q, k, v and dout
+        for n in host:
+            dev_t[n].copy_(host[n])
+        bwd_buffers(pkg, w, dev_t, sh)
+        torch.cuda.synchronize(dev)
+        for n in ("out_fwd", "lse"):
+            host[n] = dev_t[n].cpu().pin_memory()
+        results = [out, dev_t["dk"], dev_t["dv"]]
+    res_host = [torch.empty(r.shape, dtype=r.dtype).pin_memory() for r in results]
+    h2d = sum(h.numel() * h.element_size() for h in host.values())
+    d2h = sum(r.numel() * r.element_size() for r in results)
     steps = max(3, min(args.steps, 20))
 
     def step():
         for n in host:
             dev_t[n].copy_(host[n], non_blocking=True)
         launch(pkg, w, dev_t, out, sh)
-        out_host.copy_(out, non_blocking=True)
+        for r, rh in zip(results, res_host):
+            rh.copy_(r, non_blocking=True)
 
     for _ in range(2):
         step()

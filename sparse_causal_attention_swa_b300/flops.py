@@ -55,6 +55,9 @@ def useful_flops(kind: str, B: int, Hq: int, N: int, d: int, W: int, stride: int
     if kind == "global":  # stride carries the number of global prefix tokens
         p = pairs_global(N, W, stride)
         return 4.0 * d * p * B * Hq
+    if kind == "bwd":  # S, dP, dV, dK, dQ: five products of 2 d per pair (2.5 x forward)
+        p = pairs_window(N, W)
+        return 10.0 * d * p * B * Hq
     if kind == "diff":  # both maps under the window W (W >= N: causal)
         p = pairs_window(N, W)
         return 8.0 * d * p * B * Hq
@@ -86,4 +89,6 @@ def algorithmic_bytes(kind: str, B: int, Hq: int, Hkv: int, N: int, d: int) -> i
     kv = B * Hkv * N * d * 2
     if kind == "diff":
         return 2 * q + 3 * kv + q  # q1, q2, k1, k2, v, out
+    if kind == "bwd":  # q, out, dout, lse (fp32), k, v read; dq, dk, dv written
+        return 4 * q + 4 * kv + B * Hq * N * 4
     return q + 2 * kv + q  # q, k, v, out

@@ -68,6 +68,9 @@ WORKLOADS = {
     # a differential head inside an SWA layer: both maps under a W=1024 window
     "diff_swa": Workload("diff_swa", "diff", 1, 16, 16, 16384, 64, 1024, lam=0.8, sink_shift=3.0,
                          seed_index=8),
+    # backward pass of the Mistral-shaped SWA layer: q, k, v as the forward, plus dL/dout
+    "mistral_swa_bwd": Workload("mistral_swa_bwd", "bwd", 1, 32, 8, 16384, 128, 4096,
+                                seed_index=9),
     # window plus a global prefix (Longformer-style [CLS] / question tokens): W=512, 64 global
     "global": Workload("global", "global", 1, 16, 16, 16384, 64, 512, stride=64, seed_index=7),
     # decode against a W-slot rolling KV cache, Mistral-7B heads: one new query per
@@ -132,6 +135,13 @@ def make_inputs(w: Workload, seed: int | None = None) -> dict[str, np.ndarray]:
             "q2": _normal_bf16(rng, qs),
             "k2": _normal_bf16(rng, ks),
             "v": _normal_bf16(rng, ks),
+        }
+    if w.kind == "bwd":  # the forward's inputs, then the upstream gradient dL/dout
+        return {
+            "q": _normal_bf16(rng, qs),
+            "k": _normal_bf16(rng, ks),
+            "v": _normal_bf16(rng, ks),
+            "dout": _normal_bf16(rng, qs),
         }
     return {
         "q": _normal_bf16(rng, qs),
