@@ -252,7 +252,7 @@ def run_oracle_bwd(w, inp, n_rows: int) -> float:
 
 def bwd_sample_rows(w, inp, budget_s: float) -> int:
     """Prefix length whose oracle backward takes about budget_s seconds."""
-    n = min(w.N, 256)
+    n = min(w.N, 1024)  # large enough that thread start-up does not dominate the probe
     t0 = time.perf_counter()
     run_oracle_bwd(w, inp, n)
     dt = max(time.perf_counter() - t0, 1e-3)
