@@ -95,6 +95,13 @@ def test_tensor_wrapper_host_roundtrip():
     assert_close(w, out.float().numpy().astype(np.float64), run_oracle(w, inp), "wrapper")
 
 
+def _full_size_all_rows(name):
+    """Every output element of the workload against the oracle (all rows of all heads)."""
+    w = swa_inputs.WORKLOADS[name]
+    err = check(w, label=name)
+    print(f"{name}: all {w.N} rows x {w.B * w.Hq} heads checked, max err {err:.3e}")
+
+
 def _full_size(name, n_random=200, boundary_step=1):
     w = swa_inputs.WORKLOADS[name]
     rows = swa_inputs.sample_rows(w.N, n_random, seed=w.seed, tile=128)
@@ -107,7 +114,7 @@ def _full_size(name, n_random=200, boundary_step=1):
 
 
 def test_mistral_full_size_sampled():
-    _full_size("mistral_swa")
+    _full_size_all_rows("mistral_swa")
 
 
 def test_gemma_swa_full_size_sampled():
@@ -168,7 +175,7 @@ def test_strided_sweep(d, heads):
 
 
 def test_strided_full_size_sampled():
-    _full_size("strided")
+    _full_size_all_rows("strided")
 
 
 # ------------------------------------------------------------------------- global prefix
@@ -204,7 +211,7 @@ def test_diff_sweep(d, heads):
 
 
 def test_diff_full_size_sampled():
-    _full_size("diff")
+    _full_size_all_rows("diff")
 
 
 @pytest.mark.parametrize("heads", [(4, 2), (3, 3)])
@@ -253,7 +260,7 @@ def test_diff_window_sweep(d, heads):
 
 
 def test_diff_window_full_size_sampled():
-    _full_size("diff_swa")
+    _full_size_all_rows("diff_swa")
 
 
 def test_diff_window_per_head_lambda_and_limits():
