@@ -17,6 +17,11 @@ barrier and device synchronisation, and the time is the maximum over ranks.
 
 ``--impl reference`` times the fp64 CPU oracle (the only reference this method has) on
 the host cores over bounded row samples of the same workload.
+
+Other workloads (``--workload``, or ``--all`` for one line each): the Gemma-3-shaped layers,
+local + strided, window plus a global prefix, the differential forms, decode against a
+rolling cache, and ``mistral_swa_bwd``, where one step is one backward call (dq, dk, dv) of
+the Mistral-shaped layer with the forward's output and log-sum-exp computed once beforehand.
 """
 from __future__ import annotations
 
@@ -201,15 +206,15 @@ def sample_flops(w: swa_inputs.Workload, rows: np.ndarray) -> float:
     return 8.0 * w.d * float(np.minimum(i + 1, w.W).sum()) * w.B * w.Hq
 
 
-def run_oracle_rows(w, inp, rows):
+def run_oracle_rows(w, inp, rows, nthreads: int = 0):
     import oracle
 
     if w.kind == "diff":
         return oracle.diff(inp["q1"], inp["k1"], inp["q2"], inp["k2"], inp["v"], w.lam, w.scale,
-                           rows=rows, W=w.W)
+                           rows=rows, W=w.W, nthreads=nthreads)
     kind = {"swa": "window", "strided": "strided", "global": "global"}[w.kind]
     return oracle.attn(inp["q"], inp["k"], inp["v"], w.W, w.scale, kind=kind, stride=w.stride,
-                       rows=rows)
+                       rows=rows, nthreads=nthreads)
 
 
 def oracle_inputs_f64(inp):
@@ -298,10 +303,20 @@ def cpu_baseline(w, inp, budget_s: float = 15.0):
     run_oracle_rows(w, inp, rows)
     dt = time.perf_counter() - t0
     fl = sample_flops(w, rows)
-    return {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.max_threads(),
-            "kind": "oracle",
-            "sample": f"{rows.size} seeded random query rows x all {w.B * w.Hq} heads of "
-                      f"{w.name} ({fl:.3e} useful FLOPs, {dt:.1f} s, fp64)"}
+    res = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": oracle.max_threads(),
+           "kind": "oracle",
+           "sample": f"{rows.size} seeded random query rows x all {w.B * w.Hq} heads of "
+                     f"{w.name} ({fl:.3e} useful FLOPs, {dt:.1f} s, fp64)"}
+    if w.N * w.Hq * w.B <= 4096:  # the small workload: the whole of it on one core as well
+        every = np.arange(w.N, dtype=np.int64)
+        nt = oracle.max_threads()
+        t0 = time.perf_counter()
+        run_oracle_rows(w, inp, every, nthreads=1)
+        dt1 = time.perf_counter() - t0
+        run_oracle_rows(w, inp, every[:1], nthreads=nt)  # OpenMP keeps the last thread count
+        res["one_core"] = {"value": sample_flops(w, every) / dt1 / 1e12, "unit": "TFLOP/s",
+                           "seconds": dt1, "sample": "every row, one thread"}
+    return res
 
 
 def reference_arm(args, w, ws, rank):

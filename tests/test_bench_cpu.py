@@ -60,3 +60,13 @@ def test_bwd_cpu_baseline_and_reference_arm():
     line = json.loads(buf.getvalue().strip().splitlines()[-1])
     assert line["impl"] == "reference" and line["value"] > 0 and line["dtype"] == "f64"
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["config"]["kind"] == "bwd"
+
+
+def test_small_workload_cpu_baseline_has_one_core_time():
+    import oracle
+
+    w = swa_inputs.WORKLOADS["swa_small"]
+    nt = oracle.max_threads()
+    cb = bench.cpu_baseline(w, swa_inputs.make_inputs(w), budget_s=0.5)
+    assert cb["value"] > 0 and cb["one_core"]["value"] > 0
+    assert oracle.max_threads() == nt  # the thread count is restored
