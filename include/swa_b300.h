@@ -1,6 +1,7 @@
 /*
  * swa_b300.h -- C ABI of the B300 (sm_103a) sliding-window / sparse / differential
- * causal attention forward library (libswa_b300.so).
+ * causal attention library (libswa_b300.so): the forward calls, decode and chunked prefill
+ * against a rolling KV cache, and the backward pass of causal SWA.
  *
  * Sources, cited by page title and section:
  *   [SWA]  "SWA：滑动窗口注意力与跨层信息传递" (lizn-zn.github.io): §1 (the window W
@@ -10,7 +11,8 @@
  *          §4.1 (skip the work outside the window).
  *   [AV]   "注意力变体——滑动窗口、稀疏、差分" (ai-engineering.com.cn), "Build it"
  *          step 2 (sliding-window causal mask), step 3 (local + strided mask),
- *          step 4 (differential attention).
+ *          step 4 (differential attention); exercises 2-4 (training with SWA layers,
+ *          a learnable lambda per head).
  *   [AVpt] "Variantes de Atenção — Janela Deslizante, Esparsa, Diferencial"
  *          (ai-engineering.academy), "Atenção Diferencial": A1 = softmax(Q1 K1^T / sqrt d),
  *          A2 = softmax(Q2 K2^T / sqrt d), DiffAttn = (A1 - lambda A2) V.
@@ -53,7 +55,7 @@ typedef enum swa_status {
     SWA_ERR_CUDA = 5,        /* a CUDA runtime / driver call failed (launch, attribute, map) */
     SWA_ERR_TIMEOUT = 6,     /* a kernel-side bounded wait ran out (read by swa_device_status) */
     SWA_ERR_VALUE = 7,       /* scale not finite and > 0, or lambda not finite */
-    SWA_ERR_TOO_LARGE = 8    /* a fixed capacity (the no-alloc tile list, a decode workspace) is too small */
+    SWA_ERR_TOO_LARGE = 8    /* a fixed capacity (the no-alloc tile list, a decode or backward workspace) is too small */
 } swa_status;
 
 /* Capacity, in int entries (256 KiB), of the fixed device array that
