@@ -16,6 +16,8 @@ Low-level calls (pointers or tensors, explicit sizes, asynchronous on ``stream``
 Convenience wrappers on [B, H, N, d] bf16 tensors (allocate ``out``; CPU inputs are
 copied to the current CUDA device and the result copied back):
     swa_attention, strided_attention, diff_attention, swa_decode
+For training, swa_attention_trainable (CUDA tensors) records the forward for autograd and
+runs swa_attn_bwd in the backward.
 """
 from __future__ import annotations
 
@@ -290,6 +292,57 @@ def diff_attention(q1, k1, q2, k2, v, lam: float, scale: float | None = None, ou
     else:
         diff_swa_attn_fwd(a, b_, c, e, f, lam, None, o, B, Hq, b_.shape[1], N, d, int(window), sc)
     return _finish(o, q1)
+
+
+_SWA_AUTOGRAD = None
+
+
+def _swa_autograd_fn():
+    """torch.autograd.Function whose forward is swa_attn_fwd_lse and whose backward is
+    swa_attn_bwd (built on first use, so importing this module does not import torch)."""
+    global _SWA_AUTOGRAD
+    if _SWA_AUTOGRAD is None:
+        import torch
+
+        class SwaAttention(torch.autograd.Function):
+            @staticmethod
+            def forward(ctx, q, k, v, window, scale):
+                B, Hq, N, d = q.shape
+                out = torch.empty_like(q)
+                lse = torch.empty((B, Hq, N), dtype=torch.float32, device=q.device)
+                swa_attn_fwd_lse(q, k, v, out, lse, B, Hq, k.shape[1], N, d, window, scale)
+                ctx.save_for_backward(q, k, v, out, lse)
+                ctx.window, ctx.scale = window, scale
+                return out
+
+            @staticmethod
+            def backward(ctx, dout):
+                q, k, v, out, lse = ctx.saved_tensors
+                B, Hq, N, d = q.shape
+                g = dout.to(torch.bfloat16).contiguous()
+                dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+                nb = swa_attn_bwd_workspace_bytes(B, Hq, N)
+                ws = torch.empty(nb, dtype=torch.uint8, device=q.device)
+                swa_attn_bwd(q, k, v, out, lse, g, dq, dk, dv, B, Hq, k.shape[1], N, d,
+                             ctx.window, ctx.scale, ws, nb)
+                return dq, dk, dv, None, None
+
+        _SWA_AUTOGRAD = SwaAttention
+    return _SWA_AUTOGRAD
+
+
+def swa_attention_trainable(q, k, v, window: int, scale: float | None = None):
+    """Causal sliding-window attention that records itself for autograd: the forward is
+    swa_attn_fwd_lse, the backward swa_attn_bwd (dq, dk, dv, all bf16).  q, k, v: bf16 CUDA
+    tensors [B, H, N, d]."""
+    import torch
+
+    for t in (q, k, v):
+        if t.dtype != torch.bfloat16 or t.dim() != 4 or not t.is_cuda:
+            raise ValueError("expected bf16 CUDA tensors of shape [B, H, N, d]")
+    sc = scale if scale is not None else 1.0 / math.sqrt(q.shape[-1])
+    return _swa_autograd_fn().apply(q.contiguous(), k.contiguous(), v.contiguous(), int(window),
+                                    float(sc))
 
 
 def swa_decode(q, k_cache, v_cache, pos, scale: float | None = None, out=None, workspace=None):
