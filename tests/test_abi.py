@@ -192,3 +192,22 @@ def test_bwd_validation(L):
     assert call(lse=P + 2) == 3
     assert call(ws=P + 4) == 3
     assert call(nb=n - 1) == 8
+
+
+def test_header_compiles_and_library_links_from_c(tmp_path):
+    """The header is valid C and the library links and answers from a C program."""
+    import shutil
+    import subprocess
+
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    lib_dir = os.path.dirname(pkg.LIBRARY_PATH)
+    exe = str(tmp_path / "abi_from_c")
+    src = os.path.join(ROOT, "tests", "abi_c", "abi_from_c.c")
+    r = subprocess.run([cc, "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"),
+                        src, "-o", exe, "-L", lib_dir, "-lswa_b300", f"-Wl,-rpath,{lib_dir}"],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0 and "ok" in r.stdout, r.stdout + r.stderr
