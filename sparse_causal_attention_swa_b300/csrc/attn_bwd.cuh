@@ -12,12 +12,13 @@
 //
 // Three kernels, launched in order on one stream:
 //   bwd_delta_kernel      delta_i = dout_i . out_i (bf16 in, fp32 out), one row per thread
-//   attn_bwd_dkdv_kernel  one CTA per (batch, KV head, 128-key tile): walks the query tiles
-//                         of the group's heads that see the tile; S^T = K Q^T and
+//   attn_bwd_kernel<D, 0> (dk, dv) one CTA per (batch, KV head, 128-key tile): walks the
+//                         query tiles of the group's heads that see the tile; S^T = K Q^T and
 //                         dP^T = V dO^T on tcgen05, P^T and dS^T from them, then
 //                         dV += P^T dO and dK += dS^T Q accumulate in tensor memory
-//   attn_bwd_dq_kernel    one CTA per (batch, query head, 128-row tile): walks the KV tiles
-//                         of the row tile's window; S = Q K^T, dP = dO V^T, dS, dQ += dS K
+//   attn_bwd_kernel<D, 1> (dq) one CTA per (batch, query head, 128-row tile): walks the KV
+//                         tiles of the row tile's window; S = Q K^T, dP = dO V^T, dS,
+//                         dQ += dS K
 // The dq kernel recomputes S and dP instead of having the dk/dv kernel scatter dq with
 // atomics: dq stays deterministic and no fp32 dq buffer is needed.
 //
