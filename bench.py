@@ -18,7 +18,8 @@ barrier and device synchronisation, and the time is the maximum over ranks.
 ``--impl reference`` times the fp64 CPU oracle (the only reference this method has) on
 the host cores over bounded row samples of the same workload.
 
-Other workloads (``--workload``, or ``--all`` for one line each): the Gemma-3-shaped layers,
+Other workloads (``--workload``, or ``--all`` for one line each): the Gemma-3-shaped layers
+and ``gemma_group`` (one step = the 5:1 group: five W=1024 layers and one full-causal layer),
 local + strided, window plus a global prefix, the differential forms, decode against a
 rolling cache, and ``mistral_swa_bwd``, where one step is one backward call (dq, dk, dv) of
 the Mistral-shaped layer with the forward's output and log-sum-exp computed once beforehand.
@@ -54,6 +55,7 @@ KERNEL_SOURCES = {
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 L2_BYTES = 126 * 2**20
 FLUSH_BYTES = 256 * 2**20  # written between timed launches when a workload fits in twice L2
+PREFILL_CYCLES = 20e6  # about 10 ms of device spin ahead of the timed launches (see below)
 
 # DRAM traffic per launch of the dominant kernel, from one ncu capture (dram__bytes_read.sum
 # + dram__bytes_write.sum), keyed by workload, with the hash of that kernel's device sources
@@ -98,8 +100,14 @@ def workload_units(w: swa_inputs.Workload):
         return (flopcount.decode_flops(pos, w.Hq, w.d, w.W),
                 flopcount.decode_bytes(pos, w.Hq, w.Hkv, w.d, w.W))
     fl = flopcount.useful_flops(w.kind, w.B, w.Hq, w.N, w.d, w.W, w.stride)
-    by = flopcount.algorithmic_bytes(w.kind, w.B, w.Hq, w.Hkv, w.N, w.d)
+    by = flopcount.algorithmic_bytes(w.kind, w.B, w.Hq, w.Hkv, w.N, w.d,
+                                     layers=w.stride + 1 if w.kind == "group" else 1)
     return fl, by
+
+
+def group_layers(w: swa_inputs.Workload):
+    """The layers of a "group" step: `stride` W-window layers and one full-causal layer."""
+    return [w.replace(kind="swa")] * w.stride + [w.replace(kind="swa", W=w.N)]
 
 
 # ------------------------------------------------------------------------------ distributed
@@ -192,6 +200,8 @@ def oracle_sample_rows(w: swa_inputs.Workload, n_rows: int, seed: int) -> np.nda
 
 def sample_flops(w: swa_inputs.Workload, rows: np.ndarray) -> float:
     i = rows.astype(np.int64)
+    if w.kind == "group":
+        return sum(sample_flops(lw, rows) for lw in group_layers(w))
     if w.kind == "swa":
         per = np.minimum(i + 1, w.W)
         return 4.0 * w.d * float(per.sum()) * w.B * w.Hq
@@ -209,6 +219,11 @@ def sample_flops(w: swa_inputs.Workload, rows: np.ndarray) -> float:
 def run_oracle_rows(w, inp, rows, nthreads: int = 0):
     import oracle
 
+    if w.kind == "group":  # every layer of the group, each one really computed
+        out = None
+        for lw in group_layers(w):
+            out = run_oracle_rows(lw, inp, rows, nthreads)
+        return out
     if w.kind == "diff":
         return oracle.diff(inp["q1"], inp["k1"], inp["q2"], inp["k2"], inp["v"], w.lam, w.scale,
                            rows=rows, W=w.W, nthreads=nthreads)
@@ -403,6 +418,10 @@ def workload_config(w, fl, flush=False):
         cfg["stride"] = w.stride
     if w.kind == "global":
         cfg["n_global"] = w.stride
+    if w.kind == "group":
+        cfg["layers"] = (f"{w.stride} causal SWA layers with W={w.W} and one full-causal layer "
+                         f"(W=N), each a swa_attn_fwd call on the same inputs")
+        cfg["flop_convention"] = "4 d per allowed (row, key) pair, summed over the group's layers"
     if w.kind == "bwd":
         cfg["flop_convention"] = ("10 d per (row, key) pair in the window: the products S, dP, "
                                   "dV, dK, dQ (2.5 x the forward)")
@@ -442,6 +461,10 @@ def launch(pkg, w, t, out, stream):
     elif w.kind == "swa":
         pkg.swa_attn_fwd(t["q"], t["k"], t["v"], out, w.B, w.Hq, w.Hkv, w.N, w.d, w.W, w.scale,
                          stream)
+    elif w.kind == "group":  # the window layers, then the full-causal layer
+        for lw in group_layers(w):
+            pkg.swa_attn_fwd(t["q"], t["k"], t["v"], out, lw.B, lw.Hq, lw.Hkv, lw.N, lw.d, lw.W,
+                             lw.scale, stream)
     elif w.kind == "strided":
         pkg.strided_attn_fwd(t["q"], t["k"], t["v"], out, w.B, w.Hq, w.Hkv, w.N, w.d, w.W,
                              w.stride, w.scale, stream)
@@ -515,6 +538,9 @@ def bench_workload(args, w, ws, rank, dev, want_cpu, want_e2e):
     torch.cuda.synchronize(dev)
     flush = algo_bytes < 2 * L2_BYTES
     scratch = torch.empty(FLUSH_BYTES // 4, dtype=torch.int32, device=dev) if flush else None
+    # keep host time out of the events: a device-side spin of a few ms holds the stream while
+    # the host enqueues every timed launch, so no launch waits for its host-side call
+    torch.cuda._sleep(int(PREFILL_CYCLES))
     t_begin.record(stream)
     for s in range(args.steps):
         if flush:
@@ -543,24 +569,35 @@ def bench_workload(args, w, ws, rank, dev, want_cpu, want_e2e):
     achieved_tf = fl / (launch_ms * 1e-3) / 1e12
     tkey = TRAFFIC.get(w.name)
     traffic = tkey[0] if (tkey and tkey[1] == kernel_hash(kernel_family(w))) else None
-    tensor_bound = w.name not in ("swa_small",) and w.kind != "decode"
-    if tensor_bound:
+    # the bound is whichever floor is higher: the tensor time of the useful FLOPs or the
+    # HBM time of the algorithmic bytes (below the ridge, e.g. local + strided, it is HBM)
+    t_tensor = fl / (bf16_peak * 1e12)
+    t_hbm = algo_bytes / (hbm_peak * 1e9)
+    mode = {"swa": 0, "group": 0, "strided": 1, "global": 1, "diff": 2}.get(w.kind)
+    if w.kind == "bwd":
+        kname = (f"bwd_delta_kernel<{w.d}> + attn_bwd_kernel<{w.d},0> (dk, dv) + "
+                 f"attn_bwd_kernel<{w.d},1> (dq), one call")
+    elif w.kind == "decode":
+        kname = "decode_split_kernel + decode_combine_kernel"
+    elif w.kind == "group":
+        kname = (f"attn_fwd_kernel<{w.d},0>, {w.stride} launches with W={w.W} and one with "
+                 f"W=N per step")
+    else:
+        kname = f"attn_fwd_kernel<{w.d},{mode}>"
+    gbs = algo_bytes / (launch_ms * 1e-3) / 1e9
+    if t_tensor >= t_hbm:
         roofline = {"bound": "tensor", "achieved": achieved_tf, "peak": bf16_peak,
                     "unit": "TFLOP/s", "frac": achieved_tf / bf16_peak, "traffic": traffic,
                     "peak_source": f"{peak_src} bf16_tflops (burst, kernel timed alone)",
-                    "kernel": (f"bwd_delta_kernel<{w.d}> + attn_bwd_kernel<{w.d},0> (dk, dv) + "
-                               f"attn_bwd_kernel<{w.d},1> (dq), one call" if w.kind == "bwd" else
-                               f"attn_fwd_kernel<{w.d},{ {'swa': 0, 'strided': 1, 'global': 1, 'diff': 2}[w.kind]}>"),
-                    "algorithmic_flops_per_launch": fl,
-                    "hbm_gbs_algorithmic": algo_bytes / (launch_ms * 1e-3) / 1e9}
+                    "kernel": kname, "algorithmic_flops_per_launch": fl,
+                    "hbm_gbs_algorithmic": gbs}
     else:
-        gbs = algo_bytes / (launch_ms * 1e-3) / 1e9
         roofline = {"bound": "hbm", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
                     "frac": gbs / hbm_peak, "traffic": traffic,
                     "peak_source": f"{peak_src} hbm_gbs",
-                    "kernel": ("decode_split_kernel + decode_combine_kernel" if w.kind == "decode"
-                               else f"attn_fwd_kernel<{w.d},0>"),
-                    "algorithmic_bytes_per_launch": algo_bytes}
+                    "kernel": kname, "algorithmic_bytes_per_launch": algo_bytes,
+                    "tflops_useful": achieved_tf,
+                    "tensor_frac": achieved_tf / bf16_peak}
 
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws,
@@ -569,7 +606,7 @@ def bench_workload(args, w, ws, rank, dev, want_cpu, want_e2e):
         "data": "synthetic", "config": workload_config(w, fl, flush),
         "pct_of_bf16_peak": 100.0 * achieved_tf / bf16_peak,
         "roofline": roofline,
-        "gpu_launches": args.steps * {"decode": 2, "bwd": 3}.get(w.kind, 1),
+        "gpu_launches": args.steps * {"decode": 2, "bwd": 3, "group": w.stride + 1}.get(w.kind, 1),
         "clocks": clk,
     }
     if ws > 1:

@@ -97,6 +97,10 @@ def _load():
             lib.oracle_attn_bwd.argtypes = [ctypes.c_int, _P, _P, _P, _P, _P, _P, _P, _I64,
                                             _I64, _I64, _I64, _I64, _I64, _I64,
                                             ctypes.c_double, ctypes.c_int]
+            lib.oracle_attn_bwd_rows.restype = ctypes.c_int
+            lib.oracle_attn_bwd_rows.argtypes = [ctypes.c_int, _P, _P, _P, _P, _P, _P, _P, _I64,
+                                                 _I64, _I64, _I64, _I64, _I64, _I64,
+                                                 ctypes.c_double, _P, _I64, ctypes.c_int]
             lib.oracle_cache_slot.restype = ctypes.c_int64
             lib.oracle_cache_slot.argtypes = [_I64, _I64]
             lib.oracle_max_threads.restype = ctypes.c_int
@@ -248,10 +252,14 @@ def lse(q, k, W: int, scale: float, kind: str = "window", stride: int = 0, rows=
 
 
 def attn_bwd(q, k, v, dout, W: int, scale: float, kind: str = "window", stride: int = 0,
-             nthreads: int = 0):
+             nthreads: int = 0, rows=None):
     """Gradients (dq, dk, dv) in fp64 of the masked attention forward for an upstream
     gradient ``dout`` = dL/dout ([B, Hq, N, d]).  dk and dv sum over the query heads that
-    share a KV head."""
+    share a KV head.
+
+    ``rows`` (optional): only the terms of these query rows are taken; dq is zero on the
+    other rows and dk, dv are sums over these rows only (complete for every key whose
+    readers all lie in the subset)."""
     lib = _load()
     q64, k64, v64, g64 = _f64(q), _f64(k), _f64(v), _f64(dout)
     B, Hq, N, d = q64.shape
@@ -259,9 +267,11 @@ def attn_bwd(q, k, v, dout, W: int, scale: float, kind: str = "window", stride: 
     dq = np.empty_like(q64)
     dk = np.empty_like(k64)
     dv = np.empty_like(v64)
-    rc = lib.oracle_attn_bwd(KINDS[kind], _ptr(q64), _ptr(k64), _ptr(v64), _ptr(g64), _ptr(dq),
-                             _ptr(dk), _ptr(dv), B, Hq, Hkv, N, d, int(W), int(stride),
-                             float(scale), int(nthreads))
+    r, nrows = _rows_arg(rows, N)
+    rc = lib.oracle_attn_bwd_rows(KINDS[kind], _ptr(q64), _ptr(k64), _ptr(v64), _ptr(g64),
+                                  _ptr(dq), _ptr(dk), _ptr(dv), B, Hq, Hkv, N, d, int(W),
+                                  int(stride), float(scale), None if r is None else _ptr(r),
+                                  nrows, int(nthreads))
     if rc != 0:
         raise ValueError(f"oracle_attn_bwd rejected its arguments (code {rc})")
     return dq, dk, dv

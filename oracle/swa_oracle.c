@@ -365,11 +365,40 @@ int oracle_lse(int kind, const double* q, const double* k, double* lse, int64_t 
  * Masked pairs have a_ij = 0 and contribute nothing.  A KV head's dk and dv sum the
  * contributions of all g query heads that read it.  dq: [B, Hq, N, d]; dk, dv: [B, Hkv, N, d].
  */
+/*
+ * The same gradients restricted to the terms of a subset of query rows (the nrows entries
+ * of rows, each in [0, N); rows = NULL means every row): dq holds the rows of the subset
+ * (0 elsewhere) and dk, dv hold the sums over the subset's rows only.  Summing the results
+ * of a partition of the rows gives the full gradients; a key's dk and dv are complete as
+ * soon as the subset holds every row that reads the key.
+ */
+int oracle_attn_bwd_rows(int kind, const double* q, const double* k, const double* v,
+                         const double* dout, double* dq, double* dk, double* dv, int64_t B,
+                         int64_t Hq, int64_t Hkv, int64_t N, int64_t d, int64_t W,
+                         int64_t stride, double scale, const int64_t* rows, int64_t nrows,
+                         int nthreads);
+
 int oracle_attn_bwd(int kind, const double* q, const double* k, const double* v,
                     const double* dout, double* dq, double* dk, double* dv, int64_t B,
                     int64_t Hq, int64_t Hkv, int64_t N, int64_t d, int64_t W, int64_t stride,
                     double scale, int nthreads) {
+    return oracle_attn_bwd_rows(kind, q, k, v, dout, dq, dk, dv, B, Hq, Hkv, N, d, W, stride,
+                                scale, NULL, N, nthreads);
+}
+
+int oracle_attn_bwd_rows(int kind, const double* q, const double* k, const double* v,
+                         const double* dout, double* dq, double* dk, double* dv, int64_t B,
+                         int64_t Hq, int64_t Hkv, int64_t N, int64_t d, int64_t W,
+                         int64_t stride, double scale, const int64_t* rows, int64_t nrows,
+                         int nthreads) {
     if (check_shape(B, Hq, Hkv, N, d)) return 2;
+    if (rows) {
+        if (nrows < 0) return 2;
+        for (int64_t r = 0; r < nrows; ++r)
+            if (rows[r] < 0 || rows[r] >= N) return 2;
+    } else if (nrows != N) {
+        return 2;
+    }
     if (kind != MASK_WINDOW && kind != MASK_STRIDED && kind != MASK_CAUSAL && kind != MASK_GLOBAL)
         return 2;
     if (kind != MASK_CAUSAL && W < 1) return 2;
@@ -394,7 +423,8 @@ int oracle_attn_bwd(int kind, const double* q, const double* k, const double* v,
             const int64_t b = t / Hkv, hk = t % Hkv;
             const size_t koff = (size_t)((b * Hkv + hk) * N * d);
             for (int64_t h = hk * g; h < (hk + 1) * g; ++h) {
-                for (int64_t i = 0; i < N; ++i) {
+                for (int64_t r = 0; r < nrows; ++r) {
+                    const int64_t i = rows ? rows[r] : r;
                     const size_t qoff = (size_t)(((b * Hq + h) * N + i) * d);
                     mask_row(kind, i, W, stride, M);
                     softmax_row(q + qoff, k + koff, d, i, scale, M, z, a);

@@ -306,45 +306,50 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(const __grid_constant
 
 // Write n new K and V rows per (sequence, KV head) into the rolling caches: row r holds
 // position pos + r and goes to slot (pos + r) mod W; of a block longer than W only the last
-// W rows are written (the others would be overwritten at once).  grid (B*Hkv, rows),
-// D/8 threads (16-byte units).
+// W rows are written (the others would be overwritten at once).  grid (rows, up to 65535
+// (sequence, KV head) pairs walked with a stride of gridDim.y), D/8 threads (16-byte units).
+// The slot is formed in 64-bit arithmetic: pos + r may exceed the int range.
 template <int D>
 __global__ void __launch_bounds__(D / 8) cache_append_kernel(const __nv_bfloat16* k_new,
                                                              const __nv_bfloat16* v_new,
                                                              __nv_bfloat16* k_cache,
                                                              __nv_bfloat16* v_cache,
-                                                             const int* pos, int Hkv, int W,
-                                                             int n) {
-    const int bh = blockIdx.x;  // b * Hkv + hk
-    const int r = n - min(n, W) + (int)blockIdx.y;
-    const int posb = pos[bh / Hkv];
-    if (posb < 0) return;
-    const size_t slot = (size_t)((posb + r) % W);
+                                                             const int* pos, int n_bh, int Hkv,
+                                                             int W, int n) {
+    const int r = n - min(n, W) + (int)blockIdx.x;
     const int u = threadIdx.x;
-    const size_t src = ((size_t)bh * n + r) * D;
-    reinterpret_cast<uint4*>(k_cache + ((size_t)bh * W + slot) * D)[u] =
-        reinterpret_cast<const uint4*>(k_new + src)[u];
-    reinterpret_cast<uint4*>(v_cache + ((size_t)bh * W + slot) * D)[u] =
-        reinterpret_cast<const uint4*>(v_new + src)[u];
+    for (int bh = (int)blockIdx.y; bh < n_bh; bh += (int)gridDim.y) {  // b * Hkv + hk
+        const int posb = pos[bh / Hkv];
+        if (posb < 0) continue;
+        const size_t slot = (size_t)(((long long)posb + r) % W);
+        const size_t src = ((size_t)bh * n + r) * D;
+        reinterpret_cast<uint4*>(k_cache + ((size_t)bh * W + slot) * D)[u] =
+            reinterpret_cast<const uint4*>(k_new + src)[u];
+        reinterpret_cast<uint4*>(v_cache + ((size_t)bh * W + slot) * D)[u] =
+            reinterpret_cast<const uint4*>(v_new + src)[u];
+    }
 }
 
 // Copy the nctx positions pos0 - nctx .. pos0 - 1 out of the rolling caches, in time order,
-// into rows 0 .. nctx-1 of contiguous context buffers [B*Hkv][ctx_rows][D].
+// into rows 0 .. nctx-1 of contiguous context buffers [B*Hkv][ctx_rows][D].  grid (rows,
+// up to 65535 (sequence, KV head) pairs walked with a stride of gridDim.y).
 template <int D>
 __global__ void __launch_bounds__(D / 8) cache_gather_kernel(const __nv_bfloat16* k_cache,
                                                              const __nv_bfloat16* v_cache,
                                                              __nv_bfloat16* k_ctx,
-                                                             __nv_bfloat16* v_ctx, int W,
-                                                             int pos0, int nctx, int ctx_rows) {
-    const int bh = blockIdx.x;
-    const int r = blockIdx.y;
-    const size_t slot = (size_t)((pos0 - nctx + r) % W);
+                                                             __nv_bfloat16* v_ctx, int n_bh,
+                                                             int W, int pos0, int nctx,
+                                                             int ctx_rows) {
+    const int r = blockIdx.x;
+    const size_t slot = (size_t)(((long long)pos0 - nctx + r) % W);
     const int u = threadIdx.x;
-    const size_t dst = ((size_t)bh * ctx_rows + r) * D;
-    reinterpret_cast<uint4*>(k_ctx + dst)[u] =
-        reinterpret_cast<const uint4*>(k_cache + ((size_t)bh * W + slot) * D)[u];
-    reinterpret_cast<uint4*>(v_ctx + dst)[u] =
-        reinterpret_cast<const uint4*>(v_cache + ((size_t)bh * W + slot) * D)[u];
+    for (int bh = (int)blockIdx.y; bh < n_bh; bh += (int)gridDim.y) {
+        const size_t dst = ((size_t)bh * ctx_rows + r) * D;
+        reinterpret_cast<uint4*>(k_ctx + dst)[u] =
+            reinterpret_cast<const uint4*>(k_cache + ((size_t)bh * W + slot) * D)[u];
+        reinterpret_cast<uint4*>(v_ctx + dst)[u] =
+            reinterpret_cast<const uint4*>(v_cache + ((size_t)bh * W + slot) * D)[u];
+    }
 }
 
 }  // namespace swa

@@ -11,6 +11,7 @@
 #include <map>
 #include <mutex>
 #include <tuple>
+#include <utility>
 #include <vector>
 
 #include "attn_fwd.cuh"
@@ -81,11 +82,36 @@ int current_device_state(DeviceState** out) {
     return SWA_OK;
 }
 
+// Process-lifetime cache of encoded tensor maps.  A map is a pure function of the values it
+// encodes (base address, extents, strides, box), so a cached entry is bit for bit what a new
+// encoding would produce and never goes stale: a buffer freed and re-allocated at the same
+// address with the same shape is described by the same map.  A repeated call therefore
+// encodes nothing.  Guarded by g_mutex (every caller of make_map holds it); bounded by
+// dropping the whole cache when it reaches kMapCacheMax entries.
+struct MapKey {
+    uintptr_t base;
+    long long rows, row_stride, nmat, mat_stride;
+    int d, box_rows;
+    bool operator<(const MapKey& o) const {
+        return std::tie(base, rows, row_stride, nmat, mat_stride, d, box_rows) <
+               std::tie(o.base, o.rows, o.row_stride, o.nmat, o.mat_stride, o.d, o.box_rows);
+    }
+};
+constexpr size_t kMapCacheMax = 4096;
+std::map<MapKey, CUtensorMap> g_map_cache;
+
 // 3-D view [nmat][rows][d] of a bf16 tensor; consecutive rows are `row_stride` elements
 // apart and consecutive matrices (heads) `mat_stride` elements apart.  The box is
 // 64 columns (128 bytes, one swizzle span) x box_rows rows x 1 matrix, 128-byte swizzled.
 int make_map(CUtensorMap* m, const void* base, int d, long long rows, long long row_stride,
              long long nmat, long long mat_stride, int box_rows = 128) {
+    const MapKey key{reinterpret_cast<uintptr_t>(base), rows, row_stride, nmat, mat_stride, d,
+                     box_rows};
+    auto it = g_map_cache.find(key);
+    if (it != g_map_cache.end()) {
+        *m = it->second;
+        return SWA_OK;
+    }
     cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)rows, (cuuint64_t)nmat};
     cuuint64_t strides[2] = {(cuuint64_t)row_stride * 2, (cuuint64_t)mat_stride * 2};
     cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
@@ -94,7 +120,10 @@ int make_map(CUtensorMap* m, const void* base, int d, long long rows, long long 
                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? SWA_OK : SWA_ERR_CUDA;
+    if (r != CUDA_SUCCESS) return SWA_ERR_CUDA;
+    if (g_map_cache.size() >= kMapCacheMax) g_map_cache.clear();
+    g_map_cache.emplace(key, *m);
+    return SWA_OK;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -520,16 +549,8 @@ int strided_attn_fwd_noalloc(const void* q, const void* k, const void* v, void* 
         na.tiles = static_cast<int*>(ptr);
         na.ready = true;
     }
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    {
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(1, 1, 1);
-        cfg.blockDim = dim3(256, 1, 1);
-        cfg.stream = s;
-        if (cudaLaunchKernelEx(&cfg, noalloc_build_tiles_kernel, na.tiles, N, Wc, sc, rpb) !=
-            cudaSuccess)
-            return SWA_ERR_CUDA;
-    }
+    // every tensor map is encoded before anything is launched: a call that fails here
+    // leaves the shared tile array as the previous call left it
     KParams kp;
     std::memset(&kp, 0, sizeof(kp));
     fill_common(kp, B, Hq, Hkv, N, Wc, sc, scale, out, *st);
@@ -546,6 +567,16 @@ int strided_attn_fwd_noalloc(const void* q, const void* k, const void* v, void* 
     if ((rc = make_map(&kp.tm_v2, v, d, ns, (long long)sc * d, (long long)B * Hkv,
                        (long long)N * d)))
         return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(1, 1, 1);
+        cfg.blockDim = dim3(256, 1, 1);
+        cfg.stream = s;
+        if (cudaLaunchKernelEx(&cfg, noalloc_build_tiles_kernel, na.tiles, N, Wc, sc, rpb) !=
+            cudaSuccess)
+            return SWA_ERR_CUDA;
+    }
     return dispatch<swa::MODE_STRIDED>(d, kp, n_items_for(kp), s, *st);
 }
 
@@ -749,8 +780,11 @@ int swa_cache_append(const void* k_new, const void* v_new, void* k_cache, void* 
     DeviceState* st = nullptr;
     int rc = current_device_state(&st);
     if (rc) return rc;
+    // rows on gridDim.x (up to 2^31 - 1), (sequence, KV head) pairs on gridDim.y (at most
+    // 65535 blocks, the kernel strides over the rest)
+    const int n_bh = B * Hkv;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(B * Hkv), (unsigned)std::min(n, W), 1);
+    cfg.gridDim = dim3((unsigned)std::min(n, W), (unsigned)std::min(n_bh, 65535), 1);
     cfg.blockDim = dim3((unsigned)(d / 8), 1, 1);
     cfg.stream = static_cast<cudaStream_t>(stream);
     const auto* kn = static_cast<const __nv_bfloat16*>(k_new);
@@ -758,8 +792,8 @@ int swa_cache_append(const void* k_new, const void* v_new, void* k_cache, void* 
     auto* kc = static_cast<__nv_bfloat16*>(k_cache);
     auto* vc = static_cast<__nv_bfloat16*>(v_cache);
     cudaError_t e = (d == 128)
-        ? cudaLaunchKernelEx(&cfg, swa::cache_append_kernel<128>, kn, vn, kc, vc, pos, Hkv, W, n)
-        : cudaLaunchKernelEx(&cfg, swa::cache_append_kernel<64>, kn, vn, kc, vc, pos, Hkv, W, n);
+        ? cudaLaunchKernelEx(&cfg, swa::cache_append_kernel<128>, kn, vn, kc, vc, pos, n_bh, Hkv, W, n)
+        : cudaLaunchKernelEx(&cfg, swa::cache_append_kernel<64>, kn, vn, kc, vc, pos, n_bh, Hkv, W, n);
     return e == cudaSuccess ? SWA_OK : SWA_ERR_CUDA;
 }
 
@@ -777,8 +811,9 @@ int swa_cache_gather(const void* k_cache, const void* v_cache, void* k_ctx, void
     DeviceState* st = nullptr;
     int rc = current_device_state(&st);
     if (rc) return rc;
+    const int n_bh = B * Hkv;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(B * Hkv), (unsigned)nctx, 1);
+    cfg.gridDim = dim3((unsigned)nctx, (unsigned)std::min(n_bh, 65535), 1);
     cfg.blockDim = dim3((unsigned)(d / 8), 1, 1);
     cfg.stream = static_cast<cudaStream_t>(stream);
     const auto* kc = static_cast<const __nv_bfloat16*>(k_cache);
@@ -786,8 +821,8 @@ int swa_cache_gather(const void* k_cache, const void* v_cache, void* k_ctx, void
     auto* kx = static_cast<__nv_bfloat16*>(k_ctx);
     auto* vx = static_cast<__nv_bfloat16*>(v_ctx);
     cudaError_t e = (d == 128)
-        ? cudaLaunchKernelEx(&cfg, swa::cache_gather_kernel<128>, kc, vc, kx, vx, W, pos0, nctx, ctx_rows)
-        : cudaLaunchKernelEx(&cfg, swa::cache_gather_kernel<64>, kc, vc, kx, vx, W, pos0, nctx, ctx_rows);
+        ? cudaLaunchKernelEx(&cfg, swa::cache_gather_kernel<128>, kc, vc, kx, vx, n_bh, W, pos0, nctx, ctx_rows)
+        : cudaLaunchKernelEx(&cfg, swa::cache_gather_kernel<64>, kc, vc, kx, vx, n_bh, W, pos0, nctx, ctx_rows);
     return e == cudaSuccess ? SWA_OK : SWA_ERR_CUDA;
 }
 

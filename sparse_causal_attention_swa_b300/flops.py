@@ -55,6 +55,8 @@ def useful_flops(kind: str, B: int, Hq: int, N: int, d: int, W: int, stride: int
     if kind == "global":  # stride carries the number of global prefix tokens
         p = pairs_global(N, W, stride)
         return 4.0 * d * p * B * Hq
+    if kind == "group":  # `stride` window-W layers plus one full-causal layer
+        return 4.0 * d * (stride * pairs_window(N, W) + pairs_causal(N)) * B * Hq
     if kind == "bwd":  # S, dP, dV, dK, dQ: five products of 2 d per pair (2.5 x forward)
         p = pairs_window(N, W)
         return 10.0 * d * p * B * Hq
@@ -83,10 +85,14 @@ def decode_bytes(pos, Hq: int, Hkv: int, d: int, W: int) -> int:
     return 2 * Hkv * d * 2 * decode_keys(pos, W) + 2 * B * Hq * d * 2
 
 
-def algorithmic_bytes(kind: str, B: int, Hq: int, Hkv: int, N: int, d: int) -> int:
-    """HBM bytes that every correct implementation must move: inputs read once, output written once (bf16)."""
+def algorithmic_bytes(kind: str, B: int, Hq: int, Hkv: int, N: int, d: int,
+                      layers: int = 1) -> int:
+    """HBM bytes that every correct implementation must move: inputs read once, output written
+    once (bf16); a "group" of `layers` calls moves them once per call."""
     q = B * Hq * N * d * 2
     kv = B * Hkv * N * d * 2
+    if kind == "group":
+        return layers * (q + 2 * kv + q)
     if kind == "diff":
         return 2 * q + 3 * kv + q  # q1, q2, k1, k2, v, out
     if kind == "bwd":  # q, out, dout, lse (fp32), k, v read; dq, dk, dv written

@@ -25,9 +25,9 @@ class Workload:
     """One synthetic workload: the sizes of one call of the hot path."""
 
     name: str
-    kind: str  # "swa" | "strided" | "diff" | "decode" | "global"
+    kind: str  # "swa" | "strided" | "diff" | "decode" | "global" | "group" | "bwd"
     # (for "strided" the stride field is the stride; for "global" it is the number of global
-    # prefix tokens)
+    # prefix tokens; for "group" it is the number of W-window layers per full-causal layer)
     B: int
     Hq: int
     Hkv: int
@@ -60,6 +60,9 @@ WORKLOADS = {
     # Gemma-3-shaped pair: W=1024 layer and a global (full causal, W=N) layer
     "gemma_swa": Workload("gemma_swa", "swa", 2, 16, 8, 32768, 128, 1024, seed_index=3),
     "gemma_global": Workload("gemma_global", "swa", 2, 16, 8, 32768, 128, 32768, seed_index=3),
+    # the Gemma-3 5:1 group: five W=1024 layers and one full-causal layer on the same inputs
+    "gemma_group": Workload("gemma_group", "group", 2, 16, 8, 32768, 128, 1024, stride=5,
+                            seed_index=3),
     # local + strided sparse causal attention
     "strided": Workload("strided", "strided", 1, 16, 16, 16384, 64, 256, stride=128, seed_index=4),
     # differential causal attention with an attention sink on key 0 of K1

@@ -131,3 +131,45 @@ def test_workspace_too_small_is_rejected_and_deterministic():
         torch.cuda.synchronize()
         outs.append(out.clone())
     assert torch.equal(outs[0], outs[1])
+
+
+def test_cache_append_slot_near_int_max_and_long_blocks():
+    """Slots come from 64-bit arithmetic: rows at positions past 2^31 - 1 land in the slot
+    the oracle's slot map gives.  Blocks and contexts longer than 65535 rows (more rows than a
+    grid's y extent) are copied whole."""
+    B, Hkv, d = 2, 3, 64
+    W, n = 7, 4
+    rng = np.random.default_rng(11)
+    kn = f32_to_bf16_bits(rng.standard_normal((B, Hkv, n, d), dtype=np.float32))
+    vn = f32_to_bf16_bits(rng.standard_normal((B, Hkv, n, d), dtype=np.float32))
+    pos = np.array([2**31 - 2, 5], dtype=np.int32)
+    kc = torch.zeros((B, Hkv, W, d), dtype=torch.bfloat16, device="cuda")
+    vc = torch.zeros_like(kc)
+    tp = torch.as_tensor(pos, device="cuda")
+    pkg.swa_cache_append(to_dev(kn), to_dev(vn), kc, vc, tp, B, Hkv, W, d, n)
+    torch.cuda.synchronize()
+    kcb = kc.view(torch.int16).cpu().numpy().view(np.uint16)
+    vcb = vc.view(torch.int16).cpu().numpy().view(np.uint16)
+    for b in range(B):
+        for r in range(n):
+            slot = oracle.cache_slot(int(pos[b]) + r, W)
+            assert np.array_equal(kcb[b, :, slot], kn[b, :, r])
+            assert np.array_equal(vcb[b, :, slot], vn[b, :, r])
+
+    # a block of 70000 rows into a cache of the same length, then gathered back
+    B, Hkv, W = 1, 2, 70000
+    n = W
+    kn = f32_to_bf16_bits(rng.standard_normal((B, Hkv, n, d), dtype=np.float32))
+    vn = f32_to_bf16_bits(rng.standard_normal((B, Hkv, n, d), dtype=np.float32))
+    kc = torch.zeros((B, Hkv, W, d), dtype=torch.bfloat16, device="cuda")
+    vc = torch.zeros_like(kc)
+    p0 = 123
+    tp = torch.tensor([p0], dtype=torch.int32, device="cuda")
+    pkg.swa_cache_append(to_dev(kn), to_dev(vn), kc, vc, tp, B, Hkv, W, d, n)
+    kx = torch.zeros((B, Hkv, n, d), dtype=torch.bfloat16, device="cuda")
+    vx = torch.zeros_like(kx)
+    pkg.swa_cache_gather(kc, vc, kx, vx, B, Hkv, W, d, p0 + n, n, n)
+    torch.cuda.synchronize()
+    assert pkg.swa_device_status() == 0
+    assert np.array_equal(kx.view(torch.int16).cpu().numpy().view(np.uint16), kn)
+    assert np.array_equal(vx.view(torch.int16).cpu().numpy().view(np.uint16), vn)

@@ -660,3 +660,29 @@ def test_bwd_gqa_equals_repeated_kv_and_w_ge_n_is_causal(oracle_mod):
     for W in (11, 30):
         for a, b in zip(oracle_mod.attn_bwd(q, k, v, g, W, 0.6), causal):
             assert np.array_equal(a, b)
+
+
+def test_bwd_row_subsets_partition_the_gradients(oracle_mod):
+    """The row-subset form: every row listed is the full form bit for bit; dq of a subset is
+    the full dq on its rows and zero elsewhere; the dk, dv of a partition of the rows add up to
+    the full dk, dv; a key read only by rows of a subset gets its full gradient from it."""
+    q, k, v, g = _bwd_inputs(97, B=2, Hq=4, Hkv=2, N=23, d=6)
+    W, sc = 5, 0.4
+    full = oracle_mod.attn_bwd(q, k, v, g, W, sc)
+    every = oracle_mod.attn_bwd(q, k, v, g, W, sc, rows=np.arange(23))
+    for a, b in zip(full, every):
+        assert np.array_equal(a, b)
+    part_a = np.array([0, 3, 4, 5, 9, 10, 11, 12, 13, 21])
+    part_b = np.setdiff1d(np.arange(23), part_a)
+    ra = oracle_mod.attn_bwd(q, k, v, g, W, sc, rows=part_a)
+    rb = oracle_mod.attn_bwd(q, k, v, g, W, sc, rows=part_b)
+    np.testing.assert_array_equal(ra[0][:, :, part_a], full[0][:, :, part_a])
+    assert np.all(ra[0][:, :, part_b] == 0.0)
+    for x, y, f in zip(ra[1:], rb[1:], full[1:]):
+        np.testing.assert_allclose(x + y, f, rtol=0, atol=1e-13)
+    # keys 9..13 are read by rows 9..17 only (W = 5): the contiguous subset 9..17 covers them
+    sub = oracle_mod.attn_bwd(q, k, v, g, W, sc, rows=np.arange(9, 18))
+    for x, f in zip(sub[1:], full[1:]):
+        np.testing.assert_allclose(x[:, :, 9:14], f[:, :, 9:14], rtol=0, atol=1e-13)
+    with pytest.raises(ValueError):
+        oracle_mod.attn_bwd(q, k, v, g, W, sc, rows=np.array([0, 23]))
