@@ -22,9 +22,14 @@
 // The dq kernel recomputes S and dP instead of having the dk/dv kernel scatter dq with
 // atomics: dq stays deterministic and no fp32 dq buffer is needed.
 //
-// CTA organisation (192 threads): warps 0-3 compute (thread t owns TMEM lane t: a query row
-// in the dq kernel, a key row in the dk/dv kernel), warp 4 lane 0 loads tiles with TMA,
-// warp 5 owns TMEM and issues the MMAs (converged warp, one elected lane per operation).
+// CTA organisation (320 threads): warps 0-7 compute; warps w and w + 4 share TMEM lanes
+// 32 (w % 4) .. 32 (w % 4) + 31 (a query row each in the dq kernel, a key row each in the
+// dk/dv kernel) and split the 128 columns of a step, 64 each, so two warps per lane quarter
+// overlap their exponentials; warp 8 lane 0 loads tiles with TMA, warp 9 owns TMEM and
+// issues the MMAs (converged warp, one elected lane per operation).  P^T and dS^T (or dS)
+// are packed to bf16 pairs over the first 32 of each half's 64 columns, i.e. TMEM columns
+// [0, 32) and [64, 96) of the S and dP regions; a warp overwrites only columns it has read.
+// A 32-column chunk that no lane of a warp may read is neither loaded nor exponentiated.
 // Every MMA form here is one the forward kernel uses: S-type products with both operands
 // K-major from shared memory, and accumulating products whose A operand (P or dS, bf16
 // packed in pairs) is read from tensor memory and whose B operand is a K-major tile read as
@@ -52,9 +57,10 @@ struct BwdParams {
     float scale, scale_log2;
 };
 
-constexpr int BWD_THREADS = 192;
-constexpr int BWD_PRODUCER_WARP = 4;
-constexpr int BWD_MMA_WARP = 5;
+constexpr int BWD_THREADS = 320;
+constexpr int BWD_COMPUTE_WARPS = 8;
+constexpr int BWD_PRODUCER_WARP = 8;
+constexpr int BWD_MMA_WARP = 9;
 constexpr float LOG2E_F = 1.4426950408889634f;
 
 template <int D>
@@ -88,12 +94,14 @@ __device__ __forceinline__ void bwd_load_tile(uint32_t dst, const CUtensorMap* m
     for (int c = 0; c < D / 64; ++c) tma_load_3d(dst + c * (BM * 128), m, bar, c * 64, row, mat);
 }
 
-// D columns of fp32 from TMEM lane (the calling thread's), times `mul`, to one bf16 row.
+// Columns [32 c0, 32 c0 + D/2) of fp32 from TMEM lane (the calling thread's), times `mul`,
+// to the same columns of one bf16 row (the two warps of a lane quarter store one half each).
 template <int D>
-__device__ __forceinline__ void bwd_store_row(uint32_t taddr, float mul, __nv_bfloat16* dst,
-                                              bool valid) {
+__device__ __forceinline__ void bwd_store_half_row(uint32_t taddr, float mul,
+                                                   __nv_bfloat16* dst, bool valid, int c0) {
 #pragma unroll
-    for (int c = 0; c < D / 32; ++c) {
+    for (int cc = 0; cc < D / 64; ++cc) {
+        const int c = c0 + cc;
         uint32_t rr[32];
         tmem_ld32(taddr + c * 32, rr);
         if (valid) {
@@ -189,7 +197,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) attn_bwd_kernel(const __grid_c
             mbar_init(bar(L::BAR_EMPTY + s), 1);
         }
         mbar_init(bar(L::BAR_SP), 1);
-        mbar_init(bar(L::BAR_DS), 4);
+        mbar_init(bar(L::BAR_DS), BWD_COMPUTE_WARPS);
         mbar_init(bar(L::BAR_FIN), 1);
         *abort_flag = 0;
         fence_barrier_init();
@@ -293,11 +301,13 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) attn_bwd_kernel(const __grid_c
             for (int k = 0; k < BN / 16; ++k) {
                 const uint64_t koff = (uint64_t)((k * 2048) >> 4);
                 const uint32_t acc = (s > 0 || k > 0) ? 1u : 0u;
+                // packed pairs of k-step k: columns (k / 4) 64 + (k % 4) 8 of S / dP
+                const uint32_t pc = (uint32_t)((k >> 2) * 64 + (k & 3) * 8);
                 if (DKDV) {
-                    mma_ts_elect(tA1, tS + (uint32_t)(k * 8), m1 + koff, ID_O, acc);   // dV += P^T dO
-                    mma_ts_elect(tA2, tDP + (uint32_t)(k * 8), m0 + koff, ID_O, acc);  // dK += dS^T Q
+                    mma_ts_elect(tA1, tS + pc, m1 + koff, ID_O, acc);   // dV += P^T dO
+                    mma_ts_elect(tA2, tDP + pc, m0 + koff, ID_O, acc);  // dK += dS^T Q
                 } else {
-                    mma_ts_elect(tA1, tS + (uint32_t)(k * 8), m0 + koff, ID_O, acc);   // dQ += dS K
+                    mma_ts_elect(tA1, tS + pc, m0 + koff, ID_O, acc);   // dQ += dS K
                 }
             }
             mma_commit_elect(bar(L::BAR_EMPTY + st));
@@ -309,9 +319,10 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) attn_bwd_kernel(const __grid_c
         (void)mbar_wait_bounded(bar(L::BAR_FIN), 0u, &never, lim);
         __syncwarp();
     } else {
-        // ===================================== compute warpgroup (warps 0-3)
-        const int t = (int)threadIdx.x;  // TMEM lane
-        const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+        // ===================================== compute warps (0-7)
+        const int quarter = (int)(warp & 3), half = (int)(warp >> 2);
+        const int t = quarter * 32 + (int)lane;  // TMEM lane
+        const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         const uint32_t tS = tmem_base + lane_off;
         const uint32_t tDP = tS + 128u;
         const uint32_t tA1 = tS + 256u;
@@ -326,17 +337,17 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) attn_bwd_kernel(const __grid_c
         }
         bool ok = true;
         for (int s = 0; s < n_steps && ok; ++s) {
-            // per-column values of the step's query tile (dk/dv): lane l of chunk c holds
-            // query column 32 c + l, handed to the other lanes by shuffles
-            float lse2_c[BN / 32], delta_c[BN / 32];
+            // per-column values of the step's query tile (dk/dv): lane l of this warp's chunk
+            // cc holds query column 32 (2 half + cc) + l, handed to the other lanes by shuffles
+            float lse2_c[2], delta_c[2];
             const int ct = step_tile(s);
             if (DKDV) {
                 const size_t base = (size_t)step_qmat(s) * p.N;
 #pragma unroll
-                for (int c = 0; c < BN / 32; ++c) {
-                    const int qc = ct * BM + c * 32 + (int)lane;
-                    lse2_c[c] = (qc < p.N) ? __ldg(p.lse + base + qc) * LOG2E_F : 0.f;
-                    delta_c[c] = (qc < p.N) ? __ldg(p.delta + base + qc) : 0.f;
+                for (int cc = 0; cc < 2; ++cc) {
+                    const int qc = ct * BM + (2 * half + cc) * 32 + (int)lane;
+                    lse2_c[cc] = (qc < p.N) ? __ldg(p.lse + base + qc) * LOG2E_F : 0.f;
+                    delta_c[cc] = (qc < p.N) ? __ldg(p.delta + base + qc) : 0.f;
                 }
             }
             ok = mbar_wait_bounded(bar(L::BAR_SP), (uint32_t)s & 1u, abort_flag, lim);
@@ -358,39 +369,56 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) attn_bwd_kernel(const __grid_c
                 bnd = my - k0;
                 if (!valid) bnd = -1;
             }
+            // the warp's allowed columns lie in [wa, wb]
+            int la = max(a, 0), lb = min(bnd, BN - 1);
+            if (la > lb) {
+                la = BN;
+                lb = -1;
+            }
+            const int wa = __reduce_min_sync(0xffffffffu, la);
+            const int wb = __reduce_max_sync(0xffffffffu, lb);
 #pragma unroll
-            for (int c = 0; c < BN / 32; ++c) {
-                uint32_t sr[32], dr[32];
-                tmem_ld32(tS + c * 32, sr);
-                tmem_ld32(tDP + c * 32, dr);
+            for (int cc = 0; cc < 2; ++cc) {
+                const int c = 2 * half + cc;
                 uint32_t pk[16], dk16[16];
+                if (c * 32 <= wb && c * 32 + 31 >= wa) {  // warp-uniform
+                    uint32_t sr[32], dr[32];
+                    tmem_ld32(tS + c * 32, sr);
+                    tmem_ld32(tDP + c * 32, dr);
 #pragma unroll
-                for (int u = 0; u < 16; ++u) {
-                    float pv[2], dsv[2];
+                    for (int u = 0; u < 16; ++u) {
+                        float pv[2], dsv[2];
 #pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int col = c * 32 + 2 * u + e;
-                        float l2, dl;
-                        if (DKDV) {
-                            l2 = __shfl_sync(0xffffffffu, lse2_c[c], 2 * u + e);
-                            dl = __shfl_sync(0xffffffffu, delta_c[c], 2 * u + e);
-                        } else {
-                            l2 = lse2_row;
-                            dl = delta_row;
+                        for (int e = 0; e < 2; ++e) {
+                            const int col = c * 32 + 2 * u + e;
+                            float l2, dl;
+                            if (DKDV) {
+                                l2 = __shfl_sync(0xffffffffu, lse2_c[cc], 2 * u + e);
+                                dl = __shfl_sync(0xffffffffu, delta_c[cc], 2 * u + e);
+                            } else {
+                                l2 = lse2_row;
+                                dl = delta_row;
+                            }
+                            const bool in = (col >= a) && (col <= bnd);
+                            pv[e] = in ? fast_exp2(fmaf(__uint_as_float(sr[2 * u + e]), sl2, -l2))
+                                       : 0.f;
+                            dsv[e] = pv[e] * (__uint_as_float(dr[2 * u + e]) - dl);
                         }
-                        const bool in = (col >= a) && (col <= bnd);
-                        pv[e] = in ? fast_exp2(fmaf(__uint_as_float(sr[2 * u + e]), sl2, -l2)) : 0.f;
-                        dsv[e] = pv[e] * (__uint_as_float(dr[2 * u + e]) - dl);
+                        pk[u] = pack_bf16x2(pv[0], pv[1]);
+                        dk16[u] = pack_bf16x2(dsv[0], dsv[1]);
                     }
-                    pk[u] = pack_bf16x2(pv[0], pv[1]);
-                    dk16[u] = pack_bf16x2(dsv[0], dsv[1]);
-                }
-                // packed columns [16c, 16c+16) lie in columns this thread has already loaded
-                if (DKDV) {
-                    tmem_st16(tS + c * 16, pk);     // P^T over S^T
-                    tmem_st16(tDP + c * 16, dk16);  // dS^T over dP^T
                 } else {
-                    tmem_st16(tS + c * 16, dk16);   // dS over S
+#pragma unroll
+                    for (int u = 0; u < 16; ++u) pk[u] = dk16[u] = 0u;
+                }
+                // packed columns: 64 half + 16 cc .. + 16, inside the half's first chunk, which
+                // this warp has already read
+                const uint32_t pc = (uint32_t)(half * 64 + cc * 16);
+                if (DKDV) {
+                    tmem_st16(tS + pc, pk);     // P^T over S^T
+                    tmem_st16(tDP + pc, dk16);  // dS^T over dP^T
+                } else {
+                    tmem_st16(tS + pc, dk16);   // dS over S
                 }
             }
             tmem_wait_st();
@@ -404,13 +432,13 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) attn_bwd_kernel(const __grid_c
         }
         if (ok) {
             tc_fence_after();
+            const size_t row = (size_t)bz * p.N + (size_t)(valid ? my : 0);
+            const int c0 = half * (D / 64);
             if (DKDV) {
-                const size_t row = (size_t)bz * p.N + (size_t)(valid ? my : 0);
-                bwd_store_row<D>(tA1, 1.f, p.dv + row * D, valid);
-                bwd_store_row<D>(tA2, p.scale, p.dk + row * D, valid);
+                bwd_store_half_row<D>(tA1, 1.f, p.dv + row * D, valid, c0);
+                bwd_store_half_row<D>(tA2, p.scale, p.dk + row * D, valid, c0);
             } else {
-                const size_t row = (size_t)bz * p.N + (size_t)(valid ? my : 0);
-                bwd_store_row<D>(tA1, p.scale, p.dq + row * D, valid);
+                bwd_store_half_row<D>(tA1, p.scale, p.dq + row * D, valid, c0);
             }
         }
     }
