@@ -63,19 +63,35 @@ constexpr int BWD_PRODUCER_WARP = 8;
 constexpr int BWD_MMA_WARP = 9;
 constexpr float LOG2E_F = 1.4426950408889634f;
 
-template <int D>
+template <int D, int KIND>
 struct BwdLayout {
     static constexpr int TB = BM * D * 2;    // one 128-row bf16 tile (D/64 boxes of 16 KiB)
-    static constexpr int OFF_FIX = 0;        // the two tiles the CTA keeps (Q, dO or K, V)
-    static constexpr int OFF_RING = 2 * TB;  // two stages, each two tiles
-    static constexpr int OFF_BAR = OFF_RING + 4 * TB;
+    // The moving tiles come through two rings, so each is freed as soon as its last product
+    // is done.  Ring A holds the B operand of S (dk/dv: Q, read again by dK at the end of the
+    // step; dq: K, read again by dQ); ring B that of dP (dk/dv: dO, read again by dV in mid
+    // step; dq: V).  The dq kernel's ring A has three entries, so K(s+1) is in place when S(s+1)
+    // is issued at the start of step s.
+    static constexpr int NA = (KIND == 0) ? 2 : 3;
+    static constexpr int NB = 2;
+    static constexpr int OFF_FIX = 0;        // the two tiles the CTA keeps (K, V or Q, dO)
+    static constexpr int OFF_RA = 2 * TB;
+    static constexpr int OFF_RB = OFF_RA + NA * TB;
+    static constexpr int OFF_DS = OFF_RB + NB * TB;  // dk/dv: dS^T, 128 keys x 128 queries
+    static constexpr int DS_BYTES = (KIND == 0) ? BM * BN * 2 : 0;
+    static constexpr int OFF_BAR = OFF_DS + DS_BYTES;
     static constexpr int BAR_FIX = 0;
-    static constexpr int BAR_FULL = 1;   // two
-    static constexpr int BAR_EMPTY = 3;  // two
-    static constexpr int BAR_SP = 5;     // S and dP products of a step are in TMEM
-    static constexpr int BAR_DS = 6;     // the step's P / dS are in TMEM (one arrival per warp)
-    static constexpr int BAR_FIN = 7;    // every MMA of the CTA has completed
-    static constexpr int NBARS = 8;
+    static constexpr int BAR_AFULL = 1;    // three (ring A entries)
+    static constexpr int BAR_AEMPTY = 4;   // three
+    static constexpr int BAR_BFULL = 7;    // two (ring B entries)
+    static constexpr int BAR_BEMPTY = 9;   // two
+    static constexpr int BAR_SREADY = 11;  // S (dq: per region, two) is in TMEM
+    static constexpr int BAR_DPREADY = 13; // dP is in TMEM
+    static constexpr int BAR_P = 14;       // dk/dv: P^T is in TMEM (one arrival per warp)
+    static constexpr int BAR_DPL = 15;     // dP has been read (one arrival per warp)
+    static constexpr int BAR_DS = 16;      // dS^T in smem / dS in TMEM (dq: per region, two)
+    static constexpr int BAR_DSFREE = 18;  // dk/dv: the dS^T tile may be rewritten
+    static constexpr int BAR_FIN = 19;     // every MMA of the CTA has completed
+    static constexpr int NBARS = 20;
     static constexpr int OFF_TMEM = OFF_BAR + NBARS * 8;
     static constexpr int OFF_ABORT = OFF_TMEM + 4;
     static constexpr int END = OFF_ABORT + 4;
@@ -83,7 +99,7 @@ struct BwdLayout {
     static constexpr int MIN_BYTES = 116 * 1024;
     static constexpr int BYTES = (END + 1024 > MIN_BYTES) ? END + 1024 : MIN_BYTES;
     static_assert(BYTES <= 232448, "shared memory budget");
-    static_assert(TB % 1024 == 0, "1024-byte tile alignment");
+    static_assert(TB % 1024 == 0 && OFF_DS % 1024 == 0, "1024-byte tile alignment");
 };
 
 // One 128-row tile of a [mat][N][D] tensor (rows past N are zero-filled by TMA).
@@ -143,10 +159,23 @@ __global__ void bwd_delta_kernel(const __nv_bfloat16* __restrict__ out,
     delta[r] = acc;
 }
 
-// The two kernels share their skeleton; KIND 0 is the dk/dv kernel, KIND 1 the dq kernel.
+// The two kernels share their set-up; KIND 0 is the dk/dv kernel, KIND 1 the dq kernel.
+//
+// Pipelining.  A step's products are issued so that the tensor core works on one step while
+// the compute warps work on another, and each ring entry is released by its last product.
+//   dk/dv: per step s the issuer waits for P^T(s) (packed over S^T in TMEM) and issues
+//          dV += P^T(s) dO(s), then S^T(s+1) (after dV(s) in issue order, so it cannot
+//          overwrite P^T(s) too early); once the compute warps have read dP^T(s) it issues
+//          dP^T(s+1); once dS^T(s) is in shared memory it issues dK += dS^T(s) Q(s).  The
+//          compute warps form dS^T(s) while dV(s), S^T(s+1) and dP^T(s+1) run.
+//   dq:    S has two TMEM regions, so S(s+1) is issued at the start of step s; dP(s+1)
+//          once dP(s) has been read; dQ += dS(s) K(s) once dS(s) (packed over S(s)) is in.
+// Every barrier completes at most one phase ahead of its waiters: each next phase needs an
+// event that follows the waiter's previous wait (the per-region barriers of the dq kernel
+// exist for exactly this).
 template <int D, int KIND>
 __global__ void __launch_bounds__(BWD_THREADS, 1) attn_bwd_kernel(const __grid_constant__ BwdParams p) {
-    using L = BwdLayout<D>;
+    using L = BwdLayout<D, KIND>;
     constexpr bool DKDV = (KIND == 0);
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -192,12 +221,20 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) attn_bwd_kernel(const __grid_c
     }
     if (threadIdx.x == 0) {
         mbar_init(bar(L::BAR_FIX), 1);
-        for (int s = 0; s < 2; ++s) {
-            mbar_init(bar(L::BAR_FULL + s), 1);
-            mbar_init(bar(L::BAR_EMPTY + s), 1);
+        for (int i = 0; i < 3; ++i) {
+            mbar_init(bar(L::BAR_AFULL + i), 1);
+            mbar_init(bar(L::BAR_AEMPTY + i), 1);
         }
-        mbar_init(bar(L::BAR_SP), 1);
-        mbar_init(bar(L::BAR_DS), BWD_COMPUTE_WARPS);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar(L::BAR_BFULL + i), 1);
+            mbar_init(bar(L::BAR_BEMPTY + i), 1);
+            mbar_init(bar(L::BAR_SREADY + i), 1);
+            mbar_init(bar(L::BAR_DS + i), BWD_COMPUTE_WARPS);
+        }
+        mbar_init(bar(L::BAR_DPREADY), 1);
+        mbar_init(bar(L::BAR_P), BWD_COMPUTE_WARPS);
+        mbar_init(bar(L::BAR_DPL), BWD_COMPUTE_WARPS);
+        mbar_init(bar(L::BAR_DSFREE), 1);
         mbar_init(bar(L::BAR_FIN), 1);
         *abort_flag = 0;
         fence_barrier_init();
@@ -225,31 +262,58 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) attn_bwd_kernel(const __grid_c
                 bwd_load_tile<D>(sbase + L::OFF_FIX, &p.tm_q, bar(L::BAR_FIX), t0, bz);
                 bwd_load_tile<D>(sbase + L::OFF_FIX + L::TB, &p.tm_do, bar(L::BAR_FIX), t0, bz);
             }
-            int issued = 0;
+            // per step: the tile of each ring, the one whose entry frees first (dk/dv: dO;
+            // dq: K) first
+            auto load_a = [&](int s) -> bool {
+                const int e = s % L::NA, use = s / L::NA;
+                if (use > 0 && !mbar_wait_bounded(bar(L::BAR_AEMPTY + e), (uint32_t)(use - 1) & 1u,
+                                                  abort_flag, lim))
+                    return false;
+                mbar_arrive_expect_tx(bar(L::BAR_AFULL + e), L::TB);
+                const uint32_t dst = sbase + L::OFF_RA + (uint32_t)e * L::TB;
+                if (DKDV)
+                    bwd_load_tile<D>(dst, &p.tm_q, bar(L::BAR_AFULL + e), step_tile(s) * BM,
+                                     step_qmat(s));
+                else
+                    bwd_load_tile<D>(dst, &p.tm_k, bar(L::BAR_AFULL + e), step_tile(s) * BN, kvmat);
+                return true;
+            };
+            auto load_b = [&](int s) -> bool {
+                const int e = s % L::NB, use = s / L::NB;
+                if (use > 0 && !mbar_wait_bounded(bar(L::BAR_BEMPTY + e), (uint32_t)(use - 1) & 1u,
+                                                  abort_flag, lim))
+                    return false;
+                mbar_arrive_expect_tx(bar(L::BAR_BFULL + e), L::TB);
+                const uint32_t dst = sbase + L::OFF_RB + (uint32_t)e * L::TB;
+                if (DKDV)
+                    bwd_load_tile<D>(dst, &p.tm_do, bar(L::BAR_BFULL + e), step_tile(s) * BM,
+                                     step_qmat(s));
+                else
+                    bwd_load_tile<D>(dst, &p.tm_v, bar(L::BAR_BFULL + e), step_tile(s) * BN, kvmat);
+                return true;
+            };
+            int issued_a = 0, issued_b = 0;
             for (int s = 0; s < n_steps && ok; ++s) {
-                const int st = s & 1, use = s >> 1;
-                if (use > 0)
-                    ok = mbar_wait_bounded(bar(L::BAR_EMPTY + st), (uint32_t)(use - 1) & 1u,
-                                           abort_flag, lim);
-                if (!ok) break;
-                mbar_arrive_expect_tx(bar(L::BAR_FULL + st), 2 * L::TB);
-                const uint32_t dst = sbase + L::OFF_RING + (uint32_t)st * 2u * L::TB;
-                const int row = step_tile(s) * BM;
                 if (DKDV) {
-                    const int qm = step_qmat(s);
-                    bwd_load_tile<D>(dst, &p.tm_q, bar(L::BAR_FULL + st), row, qm);
-                    bwd_load_tile<D>(dst + L::TB, &p.tm_do, bar(L::BAR_FULL + st), row, qm);
+                    ok = load_b(s);
+                    if (ok) issued_b = s + 1;
+                    if (ok) ok = load_a(s);
+                    if (ok) issued_a = s + 1;
                 } else {
-                    bwd_load_tile<D>(dst, &p.tm_k, bar(L::BAR_FULL + st), row, kvmat);
-                    bwd_load_tile<D>(dst + L::TB, &p.tm_v, bar(L::BAR_FULL + st), row, kvmat);
+                    ok = load_a(s);
+                    if (ok) issued_a = s + 1;
+                    if (ok) ok = load_b(s);
+                    if (ok) issued_b = s + 1;
                 }
-                issued = s + 1;
             }
             // drain: every issued copy must have landed before the CTA may exit
             volatile int never = 0;
             (void)mbar_wait_bounded(bar(L::BAR_FIX), 0u, &never, lim);
-            for (int s = max(0, issued - 2); s < issued; ++s)
-                (void)mbar_wait_bounded(bar(L::BAR_FULL + (s & 1)), (uint32_t)(s >> 1) & 1u,
+            for (int s = max(0, issued_a - L::NA); s < issued_a; ++s)
+                (void)mbar_wait_bounded(bar(L::BAR_AFULL + s % L::NA), (uint32_t)(s / L::NA) & 1u,
+                                        &never, lim);
+            for (int s = max(0, issued_b - L::NB); s < issued_b; ++s)
+                (void)mbar_wait_bounded(bar(L::BAR_BFULL + s % L::NB), (uint32_t)(s / L::NB) & 1u,
                                         &never, lim);
         }
         __syncwarp();
@@ -257,10 +321,11 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) attn_bwd_kernel(const __grid_c
         // ===================================== MMA issuer (converged warp)
         constexpr uint32_t ID_S = idesc_bf16_f32(BM, BN, 0);
         constexpr uint32_t ID_O = idesc_bf16_f32(BM, D, 1);
-        const uint32_t tS = tmem_base;          // S (then P over its first 64 columns)
-        const uint32_t tDP = tmem_base + 128u;  // dP (then dS over its first 64 columns)
-        const uint32_t tA1 = tmem_base + 256u;  // dk/dv: dV;  dq: dQ
-        const uint32_t tA2 = tmem_base + 256u + (uint32_t)D;  // dk/dv: dK
+        // TMEM.  dk/dv: S^T [0,128) (P^T packed over it), dP^T [128,256), dV, dK.
+        //        dq:    S regions [0,128) and [128,256) (dS packed over them), dP [256,384), dQ.
+        const uint32_t tDP = tmem_base + (DKDV ? 128u : 256u);
+        const uint32_t tA1 = tmem_base + (DKDV ? 256u : 384u);  // dk/dv: dV;  dq: dQ
+        const uint32_t tA2 = tmem_base + 256u + (uint32_t)D;    // dk/dv: dK
         // fixed operands: A of the two S-type products
         const uint64_t fa0 = smem_desc_sw128(sbase + L::OFF_FIX, 16, 1024);
         const uint64_t fa1 = smem_desc_sw128(sbase + L::OFF_FIX + L::TB, 16, 1024);
@@ -268,49 +333,97 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) attn_bwd_kernel(const __grid_c
             const bool r = mbar_wait_bounded(bb, parity, abort_flag, lim);
             return __all_sync(0xffffffffu, r);
         };
+        auto ring_a = [&](int s) -> uint32_t { return sbase + L::OFF_RA + (uint32_t)(s % L::NA) * L::TB; };
+        auto ring_b = [&](int s) -> uint32_t { return sbase + L::OFF_RB + (uint32_t)(s % L::NB) * L::TB; };
+        auto wait_a = [&](int s) { return wait(bar(L::BAR_AFULL + s % L::NA), (uint32_t)(s / L::NA) & 1u); };
+        auto wait_b = [&](int s) { return wait(bar(L::BAR_BFULL + s % L::NB), (uint32_t)(s / L::NB) & 1u); };
+        // an S-type product: D(tmem) = fixed tile (A, K-major) times ring tile (B, K-major)
+        auto issue_sprod = [&](uint32_t dst, uint64_t fa, uint32_t tile) {
+            const uint64_t bd = smem_desc_sw128(tile, 16, 1024);
+#pragma unroll
+            for (int k = 0; k < D / 16; ++k) {
+                const uint32_t off = ((k >> 2) * (BM * 128) + (k & 3) * 32) >> 4;
+                mma_ss_elect(dst, fa + off, bd + off, ID_S, k > 0 ? 1u : 0u);
+            }
+        };
+        // a ring tile as the MN-major B operand (N = d, K = the tile's 128 rows) of k-step k
+        auto mn_b = [&](uint32_t tile, int k) -> uint64_t {
+            return smem_desc_sw128(tile, BN * 128, 1024) + (uint64_t)((k * 2048) >> 4);
+        };
+        // packed pairs of k-step k of P^T / dS / dS^T in TMEM: columns (k / 4) 64 + (k % 4) 8
+        auto pcol = [](int k) -> uint32_t { return (uint32_t)((k >> 2) * 64 + (k & 3) * 8); };
         bool ok = wait(bar(L::BAR_FIX), 0u);
+        if (ok && n_steps > 0) ok = wait_a(0);
+        if (ok && n_steps > 0) {
+            tc_fence_after();
+            issue_sprod(tmem_base, fa0, ring_a(0));  // S(0) (dq: region 0)
+            mma_commit_elect(bar(L::BAR_SREADY));
+            ok = wait_b(0);
+            if (ok) {
+                tc_fence_after();
+                issue_sprod(tDP, fa1, ring_b(0));  // dP(0)
+                mma_commit_elect(bar(L::BAR_DPREADY));
+                if (!DKDV) mma_commit_elect(bar(L::BAR_BEMPTY));  // dq: V(0) read
+            }
+        }
         for (int s = 0; s < n_steps && ok; ++s) {
-            const int st = s & 1;
-            ok = wait(bar(L::BAR_FULL + st), (uint32_t)(s >> 1) & 1u);
-            if (!ok) break;
-            tc_fence_after();
-            const uint32_t r0 = sbase + L::OFF_RING + (uint32_t)st * 2u * L::TB;  // Q | K tile
-            const uint32_t r1 = r0 + L::TB;                                        // dO | V tile
-            const uint64_t b0 = smem_desc_sw128(r0, 16, 1024);
-            const uint64_t b1 = smem_desc_sw128(r1, 16, 1024);
-            // dk/dv: S^T = K Q^T, dP^T = V dO^T.   dq: S = Q K^T, dP = dO V^T.
+            const bool more = s + 1 < n_steps;
+            if (DKDV) {
+                ok = wait(bar(L::BAR_P), (uint32_t)s & 1u);
+                if (!ok) break;
+                tc_fence_after();
 #pragma unroll
-            for (int k = 0; k < D / 16; ++k) {
-                const uint32_t off = ((k >> 2) * (BM * 128) + (k & 3) * 32) >> 4;
-                mma_ss_elect(tS, fa0 + off, b0 + off, ID_S, k > 0 ? 1u : 0u);
-            }
-#pragma unroll
-            for (int k = 0; k < D / 16; ++k) {
-                const uint32_t off = ((k >> 2) * (BM * 128) + (k & 3) * 32) >> 4;
-                mma_ss_elect(tDP, fa1 + off, b1 + off, ID_S, k > 0 ? 1u : 0u);
-            }
-            mma_commit_elect(bar(L::BAR_SP));
-            ok = wait(bar(L::BAR_DS), (uint32_t)s & 1u);
-            if (!ok) break;
-            tc_fence_after();
-            // accumulating products: the ring tiles as MN-major B operands (N = d, K = the
-            // tile's 128 rows), P / dS from TMEM as A
-            const uint64_t m0 = smem_desc_sw128(r0, BN * 128, 1024);
-            const uint64_t m1 = smem_desc_sw128(r1, BN * 128, 1024);
-#pragma unroll
-            for (int k = 0; k < BN / 16; ++k) {
-                const uint64_t koff = (uint64_t)((k * 2048) >> 4);
-                const uint32_t acc = (s > 0 || k > 0) ? 1u : 0u;
-                // packed pairs of k-step k: columns (k / 4) 64 + (k % 4) 8 of S / dP
-                const uint32_t pc = (uint32_t)((k >> 2) * 64 + (k & 3) * 8);
-                if (DKDV) {
-                    mma_ts_elect(tA1, tS + pc, m1 + koff, ID_O, acc);   // dV += P^T dO
-                    mma_ts_elect(tA2, tDP + pc, m0 + koff, ID_O, acc);  // dK += dS^T Q
-                } else {
-                    mma_ts_elect(tA1, tS + pc, m0 + koff, ID_O, acc);   // dQ += dS K
+                for (int k = 0; k < BN / 16; ++k)  // dV += P^T dO
+                    mma_ts_elect(tA1, tmem_base + pcol(k), mn_b(ring_b(s), k), ID_O,
+                                 (s > 0 || k > 0) ? 1u : 0u);
+                mma_commit_elect(bar(L::BAR_BEMPTY + s % L::NB));  // dO(s) read
+                if (more) {
+                    // S^T(s+1), after dV(s) in issue order (it overwrites P^T(s))
+                    ok = wait_a(s + 1);
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_sprod(tmem_base, fa0, ring_a(s + 1));
+                    mma_commit_elect(bar(L::BAR_SREADY));
                 }
+            } else if (more) {
+                // dq: S(s+1) into the other region (its last reader, dQ(s-1), went before)
+                ok = wait_a(s + 1);
+                if (!ok) break;
+                tc_fence_after();
+                issue_sprod(tmem_base + 128u * (uint32_t)((s + 1) & 1), fa0, ring_a(s + 1));
+                mma_commit_elect(bar(L::BAR_SREADY + ((s + 1) & 1)));
             }
-            mma_commit_elect(bar(L::BAR_EMPTY + st));
+            ok = wait(bar(L::BAR_DPL), (uint32_t)s & 1u);  // dP(s) has been read
+            if (ok && more) ok = wait_b(s + 1);
+            if (!ok) break;
+            if (more) {
+                tc_fence_after();
+                issue_sprod(tDP, fa1, ring_b(s + 1));
+                mma_commit_elect(bar(L::BAR_DPREADY));
+                if (!DKDV) mma_commit_elect(bar(L::BAR_BEMPTY + (s + 1) % L::NB));  // V(s+1) read
+            }
+            const int rd = DKDV ? 0 : (s & 1);
+            ok = wait(bar(L::BAR_DS + rd), DKDV ? ((uint32_t)s & 1u) : ((uint32_t)(s >> 1) & 1u));
+            if (!ok) break;
+            tc_fence_after();
+            if (DKDV) {
+                // dK += dS^T Q, dS^T from shared memory (K-major, two 64-column boxes)
+                const uint64_t ads = smem_desc_sw128(sbase + L::OFF_DS, 16, 1024);
+#pragma unroll
+                for (int k = 0; k < BN / 16; ++k) {
+                    const uint32_t offa = ((k >> 2) * (BM * 128) + (k & 3) * 32) >> 4;
+                    mma_ss_elect(tA2, ads + offa, mn_b(ring_a(s), k), ID_O,
+                                 (s > 0 || k > 0) ? 1u : 0u);
+                }
+                mma_commit_elect(bar(L::BAR_DSFREE));
+                mma_commit_elect(bar(L::BAR_AEMPTY + s % L::NA));  // Q(s) read
+            } else {
+#pragma unroll
+                for (int k = 0; k < BN / 16; ++k)  // dQ += dS K
+                    mma_ts_elect(tA1, tmem_base + 128u * (uint32_t)rd + pcol(k), mn_b(ring_a(s), k),
+                                 ID_O, (s > 0 || k > 0) ? 1u : 0u);
+                mma_commit_elect(bar(L::BAR_AEMPTY + s % L::NA));  // K(s) read
+            }
         }
         // all issued MMAs complete: the compute warps read the accumulators, TMEM may go
         __syncwarp();
@@ -323,10 +436,10 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) attn_bwd_kernel(const __grid_c
         const int quarter = (int)(warp & 3), half = (int)(warp >> 2);
         const int t = quarter * 32 + (int)lane;  // TMEM lane
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-        const uint32_t tS = tmem_base + lane_off;
-        const uint32_t tDP = tS + 128u;
-        const uint32_t tA1 = tS + 256u;
-        const uint32_t tA2 = tS + 256u + (uint32_t)D;
+        const uint32_t tL = tmem_base + lane_off;
+        const uint32_t tDP = tL + (DKDV ? 128u : 256u);
+        const uint32_t tA1 = tL + (DKDV ? 256u : 384u);
+        const uint32_t tA2 = tL + 256u + (uint32_t)D;
         const int my = t0 + t;  // dk/dv: this thread's key;  dq: its query row
         const bool valid = my < p.N;
         const float sl2 = p.scale_log2;
@@ -335,6 +448,10 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) attn_bwd_kernel(const __grid_c
             lse2_row = __ldg(p.lse + (size_t)bz * p.N + my) * LOG2E_F;
             delta_row = __ldg(p.delta + (size_t)bz * p.N + my);
         }
+        auto wait = [&](uint32_t bb, uint32_t parity) -> bool {
+            const bool r = mbar_wait_bounded(bb, parity, abort_flag, lim);
+            return __all_sync(0xffffffffu, r);
+        };
         bool ok = true;
         for (int s = 0; s < n_steps && ok; ++s) {
             // per-column values of the step's query tile (dk/dv): lane l of this warp's chunk
@@ -350,10 +467,6 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) attn_bwd_kernel(const __grid_c
                     delta_c[cc] = (qc < p.N) ? __ldg(p.delta + base + qc) : 0.f;
                 }
             }
-            ok = mbar_wait_bounded(bar(L::BAR_SP), (uint32_t)s & 1u, abort_flag, lim);
-            ok = __all_sync(0xffffffffu, ok);
-            if (!ok) break;
-            tc_fence_after();
             // allowed pairs: key j and query i with i - W < j <= i, both < N
             //   dk/dv: this thread's key j = my, column = query ct*128 + col
             //   dq:    this thread's query i = my, column = key ct*128 + col
@@ -362,74 +475,102 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) attn_bwd_kernel(const __grid_c
                 const int q0 = ct * BM;
                 a = my - q0;                                   // i >= j
                 bnd = min(my + p.W - 1, p.N - 1) - q0;         // i <= j + W - 1, i < N
-                if (!valid) bnd = -1;
             } else {
                 const int k0 = ct * BN;
                 a = max(0, my - p.W + 1) - k0;
                 bnd = my - k0;
-                if (!valid) bnd = -1;
             }
-            // the warp's allowed columns lie in [wa, wb]
-            int la = max(a, 0), lb = min(bnd, BN - 1);
-            if (la > lb) {
-                la = BN;
-                lb = -1;
-            }
-            const int wa = __reduce_min_sync(0xffffffffu, la);
-            const int wb = __reduce_max_sync(0xffffffffu, lb);
+            if (!valid) bnd = -1;
+            const int rg = DKDV ? 0 : (s & 1);  // S region of the step
+            const uint32_t tS = tL + 128u * (uint32_t)rg;
+            ok = wait(bar(L::BAR_SREADY + rg), DKDV ? ((uint32_t)s & 1u) : ((uint32_t)(s >> 1) & 1u));
+            if (!ok) break;
+            tc_fence_after();
+            // the weights of this warp's 64 columns
+            float pv[64];
 #pragma unroll
             for (int cc = 0; cc < 2; ++cc) {
-                const int c = 2 * half + cc;
-                uint32_t pk[16], dk16[16];
-                if (c * 32 <= wb && c * 32 + 31 >= wa) {  // warp-uniform
-                    uint32_t sr[32], dr[32];
-                    tmem_ld32(tS + c * 32, sr);
-                    tmem_ld32(tDP + c * 32, dr);
+                uint32_t sr[32];
+                tmem_ld32(tS + (uint32_t)(half * 64 + cc * 32), sr);
 #pragma unroll
-                    for (int u = 0; u < 16; ++u) {
-                        float pv[2], dsv[2];
-#pragma unroll
-                        for (int e = 0; e < 2; ++e) {
-                            const int col = c * 32 + 2 * u + e;
-                            float l2, dl;
-                            if (DKDV) {
-                                l2 = __shfl_sync(0xffffffffu, lse2_c[cc], 2 * u + e);
-                                dl = __shfl_sync(0xffffffffu, delta_c[cc], 2 * u + e);
-                            } else {
-                                l2 = lse2_row;
-                                dl = delta_row;
-                            }
-                            const bool in = (col >= a) && (col <= bnd);
-                            pv[e] = in ? fast_exp2(fmaf(__uint_as_float(sr[2 * u + e]), sl2, -l2))
-                                       : 0.f;
-                            dsv[e] = pv[e] * (__uint_as_float(dr[2 * u + e]) - dl);
-                        }
-                        pk[u] = pack_bf16x2(pv[0], pv[1]);
-                        dk16[u] = pack_bf16x2(dsv[0], dsv[1]);
-                    }
-                } else {
-#pragma unroll
-                    for (int u = 0; u < 16; ++u) pk[u] = dk16[u] = 0u;
-                }
-                // packed columns: 64 half + 16 cc .. + 16, inside the half's first chunk, which
-                // this warp has already read
-                const uint32_t pc = (uint32_t)(half * 64 + cc * 16);
-                if (DKDV) {
-                    tmem_st16(tS + pc, pk);     // P^T over S^T
-                    tmem_st16(tDP + pc, dk16);  // dS^T over dP^T
-                } else {
-                    tmem_st16(tS + pc, dk16);   // dS over S
+                for (int u = 0; u < 32; ++u) {
+                    const int col = (2 * half + cc) * 32 + u;
+                    const float l2 = DKDV ? __shfl_sync(0xffffffffu, lse2_c[cc], u) : lse2_row;
+                    const bool in = (col >= a) && (col <= bnd);
+                    pv[cc * 32 + u] = in ? fast_exp2(fmaf(__uint_as_float(sr[u]), sl2, -l2)) : 0.f;
                 }
             }
-            tmem_wait_st();
+            if (DKDV) {
+                // P^T, packed over the first 32 of this warp's columns (already read)
+                uint32_t pk[16];
+#pragma unroll
+                for (int cc = 0; cc < 2; ++cc) {
+#pragma unroll
+                    for (int u = 0; u < 16; ++u)
+                        pk[u] = pack_bf16x2(pv[cc * 32 + 2 * u], pv[cc * 32 + 2 * u + 1]);
+                    tmem_st16(tS + (uint32_t)(half * 64 + cc * 16), pk);
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(L::BAR_P));
+            }
+            // dS = P (dP - delta)
+            ok = wait(bar(L::BAR_DPREADY), (uint32_t)s & 1u);
+            if (!ok) break;
+            tc_fence_after();
+            uint32_t dsw[32];
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) {
+                uint32_t dr[32];
+                tmem_ld32(tDP + (uint32_t)(half * 64 + cc * 32), dr);
+#pragma unroll
+                for (int u = 0; u < 16; ++u) {
+                    float dsv[2];
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const float dl =
+                            DKDV ? __shfl_sync(0xffffffffu, delta_c[cc], 2 * u + e) : delta_row;
+                        dsv[e] = pv[cc * 32 + 2 * u + e] * (__uint_as_float(dr[2 * u + e]) - dl);
+                    }
+                    dsw[cc * 16 + u] = pack_bf16x2(dsv[0], dsv[1]);
+                }
+            }
+            // dP has been read: the issuer may overwrite it with the next step's
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(L::BAR_DS));
+            if (lane == 0) mbar_arrive(bar(L::BAR_DPL));
+            if (DKDV) {
+                // dS^T into shared memory: this thread's key row, this warp's 64 query columns
+                // (box `half`), 16-byte unit u of the row at u ^ (row & 7)
+                if (s > 0) {
+                    ok = wait(bar(L::BAR_DSFREE), (uint32_t)(s - 1) & 1u);
+                    if (!ok) break;
+                }
+                const uint32_t rowa = sbase + L::OFF_DS + (uint32_t)half * (BM * 128) + (uint32_t)t * 128u;
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    st_shared_v4(rowa + (((uint32_t)u ^ (uint32_t)(t & 7)) << 4), dsw[4 * u],
+                                 dsw[4 * u + 1], dsw[4 * u + 2], dsw[4 * u + 3]);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(L::BAR_DS));
+            } else {
+                // dS packed over the step's S region (columns this warp has read)
+#pragma unroll
+                for (int cc = 0; cc < 2; ++cc) {
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int u = 0; u < 16; ++u) pk[u] = dsw[cc * 16 + u];
+                    tmem_st16(tS + (uint32_t)(half * 64 + cc * 16), pk);
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(L::BAR_DS + rg));
+            }
         }
-        if (ok) {
-            ok = mbar_wait_bounded(bar(L::BAR_FIN), 0u, abort_flag, lim);
-            ok = __all_sync(0xffffffffu, ok);
-        }
+        if (ok) ok = wait(bar(L::BAR_FIN), 0u);
         if (ok) {
             tc_fence_after();
             const size_t row = (size_t)bz * p.N + (size_t)(valid ? my : 0);

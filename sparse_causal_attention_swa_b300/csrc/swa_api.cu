@@ -358,7 +358,7 @@ size_t bwd_workspace_bytes(int B, int Hq, int N) {
 template <int D, int KIND>
 int launch_bwd(const swa::BwdParams& bp, int n_tiles, int n_mats, cudaStream_t stream,
                DeviceState& st) {
-    using L = swa::BwdLayout<D>;
+    using L = swa::BwdLayout<D, KIND>;
     auto kern = swa::attn_bwd_kernel<D, KIND>;
     bool& set = st.bwd_attr_set[D == 128 ? 1 : 0][KIND];
     if (!set) {
