@@ -26,15 +26,16 @@
 // 32 (w % 4) .. 32 (w % 4) + 31 (a query row each in the dq kernel, a key row each in the
 // dk/dv kernel) and split the 128 columns of a step, 64 each, so two warps per lane quarter
 // overlap their exponentials; warp 8 lane 0 loads tiles with TMA, warp 9 owns TMEM and
-// issues the MMAs (converged warp, one elected lane per operation).  P^T and dS^T (or dS)
-// are packed to bf16 pairs over the first 32 of each half's 64 columns, i.e. TMEM columns
-// [0, 32) and [64, 96) of the S and dP regions; a warp overwrites only columns it has read.
-// A 32-column chunk that no lane of a warp may read is neither loaded nor exponentiated.
+// issues the MMAs (converged warp, one elected lane per operation).  P^T (dk/dv) and dS
+// (dq) are packed to bf16 pairs over the first 32 of each half's 64 columns of their S
+// region, i.e. its TMEM columns [0, 32) and [64, 96); a warp overwrites only columns it has
+// read.  dS^T (dk/dv) goes to a 128 x 128 shared-memory tile in the 128-byte-swizzled
+// K-major layout, the A operand of dK += dS^T Q.
 // Every MMA form here is one the forward kernel uses: S-type products with both operands
-// K-major from shared memory, and accumulating products whose A operand (P or dS, bf16
-// packed in pairs) is read from tensor memory and whose B operand is a K-major tile read as
-// MN-major.  Every wait is bounded; a timeout raises the CTA's abort flag, every role
-// leaves its loop, and the status word reports SWA_ERR_TIMEOUT.
+// K-major from shared memory, accumulating products whose A operand (P^T or dS, bf16 packed
+// in pairs) is read from tensor memory or (dS^T) from shared memory and whose B operand is a
+// K-major tile read as MN-major.  Every wait is bounded; a timeout raises the CTA's abort
+// flag, every role leaves its loop, and the status word reports SWA_ERR_TIMEOUT.
 #pragma once
 
 #include "attn_fwd.cuh"
