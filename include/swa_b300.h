@@ -213,6 +213,46 @@ int swa_attn_bwd(const void* q, const void* k, const void* v, const void* out, c
                  const void* dout, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int N,
                  int d, int W, float scale, void* workspace, size_t workspace_bytes,
                  void* stream);
+/*
+ * Backward pass of local + strided sparse causal attention ([AV] step 3; the same chain rule
+ * as swa_attn_bwd): row i reads its window max(0, i-W+1) <= j <= i and the keys
+ * j = 0, stride, 2*stride, ... before the window; a_ij is the forward's weight over that set
+ * (lse from strided_attn_fwd_lse with the same q, k, W, stride and scale).  Arguments, layouts,
+ * ownership and errors as swa_attn_bwd, with
+ *   workspace: at least strided_attn_bwd_workspace_bytes(B, Hq, Hkv, N, d, W, stride) bytes;
+ *              it receives delta and fp32 partial sums of the keys j = 0, stride, ... .
+ * Four kernels run on `stream`: delta, the dk / dv of the strided keys (their readers are every
+ * row past their window, walked in chunks), the window dk / dv (which adds those partial sums
+ * before rounding), then dq (each row tile's strided keys, then its window).  Deterministic.
+ */
+size_t strided_attn_bwd_workspace_bytes(int B, int Hq, int Hkv, int N, int d, int W,
+                                        int stride);
+int strided_attn_bwd(const void* q, const void* k, const void* v, const void* out,
+                     const float* lse, const void* dout, void* dq, void* dk, void* dv, int B,
+                     int Hq, int Hkv, int N, int d, int W, int stride, float scale,
+                     void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * global_attn_fwd that also writes each row's log-sum-exp over its mask (as swa_attn_fwd_lse).
+ */
+int global_attn_fwd_lse(const void* q, const void* k, const void* v, void* out, float* lse,
+                        int B, int Hq, int Hkv, int N, int d, int W, int n_global, float scale,
+                        void* stream);
+
+/*
+ * Backward pass of the window plus a global prefix ([AV] "稀疏 / 块注意力", the mask of
+ * global_attn_fwd): row i reads its window and every key j < n_global with j <= i.  lse from
+ * global_attn_fwd_lse with the same arguments.  As strided_attn_bwd with the prefix in place
+ * of the strided keys; workspace: at least global_attn_bwd_workspace_bytes(B, Hq, Hkv, N, d, W,
+ * n_global) bytes.  n_global >= 0 (0 is swa_attn_bwd; n_global >= N is full causal).
+ */
+size_t global_attn_bwd_workspace_bytes(int B, int Hq, int Hkv, int N, int d, int W,
+                                       int n_global);
+int global_attn_bwd(const void* q, const void* k, const void* v, const void* out,
+                    const float* lse, const void* dout, void* dq, void* dk, void* dv, int B,
+                    int Hq, int Hkv, int N, int d, int W, int n_global, float scale,
+                    void* workspace, size_t workspace_bytes, void* stream);
+
 int swa_decode_fwd(const void* q, const void* k_cache, const void* v_cache, const int* pos,
                    void* out, int B, int Hq, int Hkv, int W, int d, float scale, void* workspace,
                    size_t workspace_bytes, void* stream);

@@ -9,7 +9,9 @@ and streams.  There is no CPU fallback: if the library is missing, every call ra
 Low-level calls (pointers or tensors, explicit sizes, asynchronous on ``stream``):
     swa_attn_fwd, strided_attn_fwd, diff_attn_fwd, diff_attn_fwd_heads, diff_swa_attn_fwd,
     strided_attn_fwd_noalloc, swa_attn_fwd_lse, strided_attn_fwd_lse, global_attn_fwd,
-    swa_attn_bwd_workspace_bytes, swa_attn_bwd,
+    global_attn_fwd_lse, swa_attn_bwd_workspace_bytes, swa_attn_bwd,
+    strided_attn_bwd_workspace_bytes, strided_attn_bwd, global_attn_bwd_workspace_bytes,
+    global_attn_bwd,
     swa_decode_workspace_bytes, swa_decode_fwd, swa_cache_append, swa_chunk_fwd,
     swa_cache_gather,
     swa_status_string, swa_device_status, swa_watchdog_selftest
@@ -71,6 +73,18 @@ def load():
         lib.swa_attn_bwd.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, F, P,
                                      ctypes.c_size_t, P]
         lib.swa_attn_bwd.restype = I
+        lib.strided_attn_bwd_workspace_bytes.argtypes = [I, I, I, I, I, I, I]
+        lib.strided_attn_bwd_workspace_bytes.restype = ctypes.c_size_t
+        lib.strided_attn_bwd.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, P,
+                                         ctypes.c_size_t, P]
+        lib.strided_attn_bwd.restype = I
+        lib.global_attn_bwd_workspace_bytes.argtypes = [I, I, I, I, I, I, I]
+        lib.global_attn_bwd_workspace_bytes.restype = ctypes.c_size_t
+        lib.global_attn_bwd.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, P,
+                                        ctypes.c_size_t, P]
+        lib.global_attn_bwd.restype = I
+        lib.global_attn_fwd_lse.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, F, P]
+        lib.global_attn_fwd_lse.restype = I
         SZ = ctypes.c_size_t
         lib.swa_decode_workspace_bytes.argtypes = [I, I, I, I]
         lib.swa_decode_workspace_bytes.restype = SZ
@@ -221,6 +235,40 @@ def swa_attn_bwd(q, k, v, out, lse, dout, dq, dk, dv, B, Hq, Hkv, N, d, W, scale
                                _ptr(dq), _ptr(dk), _ptr(dv), B, Hq, Hkv, N, d, int(W),
                                float(scale), _ptr(workspace), int(workspace_bytes),
                                _stream(stream)), "swa_attn_bwd")
+
+
+def strided_attn_bwd_workspace_bytes(B, Hq, Hkv, N, d, W, stride) -> int:
+    return int(load().strided_attn_bwd_workspace_bytes(B, Hq, Hkv, N, d, W, stride))
+
+
+def strided_attn_bwd(q, k, v, out, lse, dout, dq, dk, dv, B, Hq, Hkv, N, d, W, stride, scale,
+                     workspace, workspace_bytes, stream=None):
+    """Gradients of local + strided attention; ``out`` and ``lse`` come from
+    strided_attn_fwd_lse with the same arguments."""
+    _check(load().strided_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout),
+                                   _ptr(dq), _ptr(dk), _ptr(dv), B, Hq, Hkv, N, d, int(W),
+                                   int(stride), float(scale), _ptr(workspace),
+                                   int(workspace_bytes), _stream(stream)), "strided_attn_bwd")
+
+
+def global_attn_fwd_lse(q, k, v, out, lse, B, Hq, Hkv, N, d, W, n_global, scale, stream=None):
+    _check(load().global_attn_fwd_lse(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq,
+                                      Hkv, N, d, int(W), int(n_global), float(scale),
+                                      _stream(stream)), "global_attn_fwd_lse")
+
+
+def global_attn_bwd_workspace_bytes(B, Hq, Hkv, N, d, W, n_global) -> int:
+    return int(load().global_attn_bwd_workspace_bytes(B, Hq, Hkv, N, d, W, n_global))
+
+
+def global_attn_bwd(q, k, v, out, lse, dout, dq, dk, dv, B, Hq, Hkv, N, d, W, n_global, scale,
+                    workspace, workspace_bytes, stream=None):
+    """Gradients of the window plus a global prefix; ``out`` and ``lse`` come from
+    global_attn_fwd_lse with the same arguments."""
+    _check(load().global_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(dout),
+                                  _ptr(dq), _ptr(dk), _ptr(dv), B, Hq, Hkv, N, d, int(W),
+                                  int(n_global), float(scale), _ptr(workspace),
+                                  int(workspace_bytes), _stream(stream)), "global_attn_bwd")
 
 
 def swa_device_status(stream=None) -> int:

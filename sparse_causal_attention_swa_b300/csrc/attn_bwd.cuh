@@ -47,14 +47,24 @@ struct BwdParams {
     CUtensorMap tm_k;   // [B*Hkv][N][d]
     CUtensorMap tm_v;
     CUtensorMap tm_do;  // [B*Hq][N][d]
+    CUtensorMap tm_k2;  // strided / global prefix: compact keys, row r = key r * stride
+    CUtensorMap tm_v2;  // the same rows of V
     const float* lse;   // [B, Hq, N] natural-log row log-sum-exp of the forward
     const float* delta; // [B, Hq, N] dout . out
     __nv_bfloat16* dq;  // [B, Hq, N, d]
     __nv_bfloat16* dk;  // [B, Hkv, N, d]
     __nv_bfloat16* dv;  // [B, Hkv, N, d]
+    float* cpart;       // compact keys: [2][cchunks][B*Hkv][ncomp_pad][d] fp32 partial dK, dV
     int* status;
     unsigned long long wait_limit_ns;
     int B, Hq, Hkv, N, W;
+    // local + strided and window + global prefix: row i also reads the compact keys r * stride
+    // with r < ncomp(i) = min(ceil(lo(i) / stride), cap), lo(i) = max(0, i - W + 1) (the keys
+    // before its window); cap = 0 is the plain window
+    int stride, cap;
+    int ncomp;          // compact keys any row reads: ncomp(N - 1)
+    int ncomp_pad;      // ncomp rounded up to a whole 128-row tile
+    int cchunks;        // query-tile chunks of the compact dk/dv pass
     float scale, scale_log2;
 };
 
@@ -113,14 +123,24 @@ __device__ __forceinline__ void bwd_load_tile(uint32_t dst, const CUtensorMap* m
 
 // Columns [32 c0, 32 c0 + D/2) of fp32 from TMEM lane (the calling thread's), times `mul`,
 // to the same columns of one bf16 row (the two warps of a lane quarter store one half each).
+// `extra` (or null): n fp32 rows, `stride` floats apart, added to the columns before `mul`.
 template <int D>
 __device__ __forceinline__ void bwd_store_half_row(uint32_t taddr, float mul,
-                                                   __nv_bfloat16* dst, bool valid, int c0) {
+                                                   __nv_bfloat16* dst, bool valid, int c0,
+                                                   const float* extra = nullptr, int n = 0,
+                                                   size_t stride = 0) {
 #pragma unroll
     for (int cc = 0; cc < D / 64; ++cc) {
         const int c = c0 + cc;
         uint32_t rr[32];
         tmem_ld32(taddr + c * 32, rr);
+        if (valid && extra != nullptr) {
+            for (int i = 0; i < n; ++i) {
+                const float* x = extra + (size_t)i * stride + c * 32;
+#pragma unroll
+                for (int e = 0; e < 32; ++e) rr[e] = __float_as_uint(__uint_as_float(rr[e]) + x[e]);
+            }
+        }
         if (valid) {
             uint4* o = reinterpret_cast<uint4*>(dst + c * 32);
 #pragma unroll
@@ -134,6 +154,35 @@ __device__ __forceinline__ void bwd_store_half_row(uint32_t taddr, float mul,
             }
         }
     }
+}
+
+// Columns [32 c0, 32 c0 + D/2) of fp32 from TMEM lane to the same columns of an fp32 row
+// (zeros when `have` is false: no product wrote the accumulator).
+template <int D>
+__device__ __forceinline__ void bwd_store_half_row_f32(uint32_t taddr, float* dst, bool have,
+                                                       int c0) {
+#pragma unroll
+    for (int cc = 0; cc < D / 64; ++cc) {
+        const int c = c0 + cc;
+        uint32_t rr[32];
+        if (have) {
+            tmem_ld32(taddr + c * 32, rr);
+        } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) rr[e] = 0u;
+        }
+        float4* o = reinterpret_cast<float4*>(dst + c * 32);
+#pragma unroll
+        for (int v4 = 0; v4 < 8; ++v4)
+            o[v4] = make_float4(__uint_as_float(rr[4 * v4]), __uint_as_float(rr[4 * v4 + 1]),
+                                __uint_as_float(rr[4 * v4 + 2]), __uint_as_float(rr[4 * v4 + 3]));
+    }
+}
+
+// compact keys row i reads: the multiples of the stride before its window start, at most cap
+__device__ __forceinline__ int bwd_ncomp(const BwdParams& p, int i) {
+    const int lo = max(0, i - p.W + 1);
+    return min((lo + p.stride - 1) / p.stride, p.cap);
 }
 
 // delta_r = dout_r . out_r for every row r of [rows][D] (bf16), fp32 accumulation.
@@ -160,7 +209,11 @@ __global__ void bwd_delta_kernel(const __nv_bfloat16* __restrict__ out,
     delta[r] = acc;
 }
 
-// The two kernels share their set-up; KIND 0 is the dk/dv kernel, KIND 1 the dq kernel.
+// The kernels share their set-up; KIND 0 is the dk/dv kernel, KIND 1 the dq kernel, KIND 2
+// the dk/dv kernel of the compact keys (local + strided and global-prefix masks: a compact key
+// r, at position r * stride, is read by every row i >= r * stride + W; the kernel walks those
+// rows in chunks and writes fp32 partial sums that the KIND 0 kernel adds before rounding).
+// In those masks the dq kernel walks the row tile's compact tiles before its window tiles.
 //
 // Pipelining.  A step's products are issued so that the tensor core works on one step while
 // the compute warps work on another, and each ring entry is released by its last product.
@@ -176,8 +229,9 @@ __global__ void bwd_delta_kernel(const __nv_bfloat16* __restrict__ out,
 // exist for exactly this).
 template <int D, int KIND>
 __global__ void __launch_bounds__(BWD_THREADS, 1) attn_bwd_kernel(const __grid_constant__ BwdParams p) {
-    using L = BwdLayout<D, KIND>;
-    constexpr bool DKDV = (KIND == 0);
+    using L = BwdLayout<D, KIND == 1 ? 1 : 0>;
+    constexpr bool DKDV = (KIND != 1);
+    constexpr bool COMPACT = (KIND == 2);
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
@@ -194,26 +248,43 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) attn_bwd_kernel(const __grid_c
     // dk/dv: blockIdx.y = b * Hkv + hk, the 128 keys from t0; step s reads query head
     //   hk*g + s / nq, query tile i_lo + s % nq (the tiles whose rows can see one of the keys).
     // dq: blockIdx.y = b * Hq + h, the 128 rows from t0; step s reads KV tile j_lo + s.
-    const int t0 = (int)blockIdx.x * BM;
+    // compact: blockIdx.x = compact tile * cchunks + chunk; t0 is a compact row (key r)
+    const int ctile = COMPACT ? (int)blockIdx.x / p.cchunks : 0;
+    const int chunk = COMPACT ? (int)blockIdx.x % p.cchunks : 0;
+    const int t0 = (COMPACT ? ctile : (int)blockIdx.x) * BM;
     const int bz = (int)blockIdx.y;
-    int lo_t, nq, n_steps;
-    if (DKDV) {
+    const int n_qtiles = (p.N + BM - 1) / BM;
+    int lo_t, nq, n_steps, n_ct = 0;  // n_ct: dq kernel, compact tiles before the window's
+    if (KIND == 0) {
         lo_t = (int)blockIdx.x;
         const int hi = min(p.N - 1, t0 + BN - 1 + p.W - 1) / BM;
         nq = hi - lo_t + 1;
+        n_steps = g * nq;
+    } else if (COMPACT) {
+        // rows from the first reader of the tile's first key, in cchunks equal ranges
+        const long long r_first = (long long)t0 * p.stride + p.W;
+        const int qt0 = (t0 < p.ncomp && r_first < p.N) ? (int)(r_first / BM) : n_qtiles;
+        const int per = (n_qtiles - qt0 + p.cchunks - 1) / p.cchunks;
+        lo_t = qt0 + chunk * per;
+        nq = max(0, min(per, n_qtiles - lo_t));
         n_steps = g * nq;
     } else {
         lo_t = max(0, t0 - p.W + 1) / BN;
         const int hi = min(p.N - 1, t0 + BM - 1) / BN;
         nq = hi - lo_t + 1;
-        n_steps = nq;
+        if (p.cap > 0) n_ct = (bwd_ncomp(p, min(p.N - 1, t0 + BM - 1)) + BN - 1) / BN;
+        n_steps = n_ct + nq;
     }
     const int b = DKDV ? bz / p.Hkv : bz / p.Hq;
     const int kvmat = DKDV ? bz : b * p.Hkv + (bz % p.Hq) / g;  // K / V matrix
     auto step_qmat = [&](int s) -> int {  // query-side matrix (Q, dO, lse, delta) of a step
         return DKDV ? b * p.Hq + (bz % p.Hkv) * g + s / nq : bz;
     };
-    auto step_tile = [&](int s) -> int { return lo_t + (DKDV ? s % nq : s); };
+    // query tile (dk/dv kinds) or window KV tile (dq) of a step; dq: -1 - c for compact tile c
+    auto step_tile = [&](int s) -> int {
+        if (DKDV) return lo_t + s % nq;
+        return s < n_ct ? -1 - s : lo_t + (s - n_ct);
+    };
 
     // ---- setup
     if (warp == BWD_MMA_WARP) {
@@ -245,6 +316,10 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) attn_bwd_kernel(const __grid_c
         tma_prefetch_desc(&p.tm_k);
         tma_prefetch_desc(&p.tm_v);
         tma_prefetch_desc(&p.tm_do);
+        if (p.cap > 0) {
+            tma_prefetch_desc(&p.tm_k2);
+            tma_prefetch_desc(&p.tm_v2);
+        }
     }
     tc_fence_before();
     __syncthreads();
@@ -257,8 +332,10 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) attn_bwd_kernel(const __grid_c
             bool ok = true;
             mbar_arrive_expect_tx(bar(L::BAR_FIX), 2 * L::TB);
             if (DKDV) {
-                bwd_load_tile<D>(sbase + L::OFF_FIX, &p.tm_k, bar(L::BAR_FIX), t0, kvmat);
-                bwd_load_tile<D>(sbase + L::OFF_FIX + L::TB, &p.tm_v, bar(L::BAR_FIX), t0, kvmat);
+                const CUtensorMap* mk = COMPACT ? &p.tm_k2 : &p.tm_k;
+                const CUtensorMap* mv = COMPACT ? &p.tm_v2 : &p.tm_v;
+                bwd_load_tile<D>(sbase + L::OFF_FIX, mk, bar(L::BAR_FIX), t0, kvmat);
+                bwd_load_tile<D>(sbase + L::OFF_FIX + L::TB, mv, bar(L::BAR_FIX), t0, kvmat);
             } else {
                 bwd_load_tile<D>(sbase + L::OFF_FIX, &p.tm_q, bar(L::BAR_FIX), t0, bz);
                 bwd_load_tile<D>(sbase + L::OFF_FIX + L::TB, &p.tm_do, bar(L::BAR_FIX), t0, bz);
@@ -272,11 +349,13 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) attn_bwd_kernel(const __grid_c
                     return false;
                 mbar_arrive_expect_tx(bar(L::BAR_AFULL + e), L::TB);
                 const uint32_t dst = sbase + L::OFF_RA + (uint32_t)e * L::TB;
+                const int tl = step_tile(s);
                 if (DKDV)
-                    bwd_load_tile<D>(dst, &p.tm_q, bar(L::BAR_AFULL + e), step_tile(s) * BM,
-                                     step_qmat(s));
+                    bwd_load_tile<D>(dst, &p.tm_q, bar(L::BAR_AFULL + e), tl * BM, step_qmat(s));
+                else if (tl < 0)  // compact tile -1 - tl
+                    bwd_load_tile<D>(dst, &p.tm_k2, bar(L::BAR_AFULL + e), (-1 - tl) * BN, kvmat);
                 else
-                    bwd_load_tile<D>(dst, &p.tm_k, bar(L::BAR_AFULL + e), step_tile(s) * BN, kvmat);
+                    bwd_load_tile<D>(dst, &p.tm_k, bar(L::BAR_AFULL + e), tl * BN, kvmat);
                 return true;
             };
             auto load_b = [&](int s) -> bool {
@@ -286,11 +365,13 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) attn_bwd_kernel(const __grid_c
                     return false;
                 mbar_arrive_expect_tx(bar(L::BAR_BFULL + e), L::TB);
                 const uint32_t dst = sbase + L::OFF_RB + (uint32_t)e * L::TB;
+                const int tl = step_tile(s);
                 if (DKDV)
-                    bwd_load_tile<D>(dst, &p.tm_do, bar(L::BAR_BFULL + e), step_tile(s) * BM,
-                                     step_qmat(s));
+                    bwd_load_tile<D>(dst, &p.tm_do, bar(L::BAR_BFULL + e), tl * BM, step_qmat(s));
+                else if (tl < 0)
+                    bwd_load_tile<D>(dst, &p.tm_v2, bar(L::BAR_BFULL + e), (-1 - tl) * BN, kvmat);
                 else
-                    bwd_load_tile<D>(dst, &p.tm_v, bar(L::BAR_BFULL + e), step_tile(s) * BN, kvmat);
+                    bwd_load_tile<D>(dst, &p.tm_v, bar(L::BAR_BFULL + e), tl * BN, kvmat);
                 return true;
             };
             int issued_a = 0, issued_b = 0;
@@ -441,8 +522,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) attn_bwd_kernel(const __grid_c
         const uint32_t tDP = tL + (DKDV ? 128u : 256u);
         const uint32_t tA1 = tL + (DKDV ? 256u : 384u);
         const uint32_t tA2 = tL + 256u + (uint32_t)D;
-        const int my = t0 + t;  // dk/dv: this thread's key;  dq: its query row
-        const bool valid = my < p.N;
+        const int my = t0 + t;  // dk/dv: this thread's key (compact: key index r);  dq: its row
+        const bool valid = COMPACT ? (my < p.ncomp_pad) : (my < p.N);
         const float sl2 = p.scale_log2;
         float lse2_row = 0.f, delta_row = 0.f;  // dq kernel: the row's own values
         if (!DKDV && valid) {
@@ -468,14 +549,25 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) attn_bwd_kernel(const __grid_c
                     delta_c[cc] = (qc < p.N) ? __ldg(p.delta + base + qc) : 0.f;
                 }
             }
-            // allowed pairs: key j and query i with i - W < j <= i, both < N
+            // allowed pairs: key j and query i with i - W < j <= i, both < N; compact key r
+            // (position r * stride) and query i with r < ncomp(i), i.e. i >= r * stride + W
             //   dk/dv: this thread's key j = my, column = query ct*128 + col
-            //   dq:    this thread's query i = my, column = key ct*128 + col
+            //   compact dk/dv: this thread's compact key r = my, column = query ct*128 + col
+            //   dq:    this thread's query i = my, column = key ct*128 + col, or compact key
+            //          c*128 + col of compact tile c = -1 - ct
             int a, bnd;  // allowed columns [a, bnd]
-            if (DKDV) {
+            if (KIND == 0) {
                 const int q0 = ct * BM;
                 a = my - q0;                                   // i >= j
                 bnd = min(my + p.W - 1, p.N - 1) - q0;         // i <= j + W - 1, i < N
+            } else if (COMPACT) {
+                const int q0 = ct * BM;
+                const long long first = (long long)my * p.stride + p.W;  // first reader
+                a = (int)min(first - q0, (long long)BM);
+                bnd = (my < p.ncomp) ? p.N - 1 - q0 : -1;
+            } else if (ct < 0) {
+                a = 0;
+                bnd = bwd_ncomp(p, my) - 1 - (-1 - ct) * BN;
             } else {
                 const int k0 = ct * BN;
                 a = max(0, my - p.W + 1) - k0;
@@ -574,12 +666,26 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) attn_bwd_kernel(const __grid_c
         if (ok) ok = wait(bar(L::BAR_FIN), 0u);
         if (ok) {
             tc_fence_after();
-            const size_t row = (size_t)bz * p.N + (size_t)(valid ? my : 0);
             const int c0 = half * (D / 64);
-            if (DKDV) {
-                bwd_store_half_row<D>(tA1, 1.f, p.dv + row * D, valid, c0);
-                bwd_store_half_row<D>(tA2, p.scale, p.dk + row * D, valid, c0);
+            const size_t part = (size_t)p.cchunks * p.B * p.Hkv * p.ncomp_pad * D;  // dk -> dv
+            if (COMPACT) {
+                // fp32 partial sums of this chunk (dK unscaled, as the window kernel's)
+                float* pk = p.cpart + (((size_t)chunk * p.B * p.Hkv + bz) * p.ncomp_pad + my) * D;
+                bwd_store_half_row_f32<D>(tA1, pk + part, n_steps > 0, c0);
+                bwd_store_half_row_f32<D>(tA2, pk, n_steps > 0, c0);
+            } else if (DKDV) {
+                const size_t row = (size_t)bz * p.N + (size_t)(valid ? my : 0);
+                // a key that is also a compact key takes the compact pass's partial sums
+                const float* xk = nullptr;
+                if (p.cap > 0 && valid && my % p.stride == 0 && my / p.stride < p.ncomp)
+                    xk = p.cpart + ((size_t)bz * p.ncomp_pad + my / p.stride) * D;
+                const size_t cstride = (size_t)p.B * p.Hkv * p.ncomp_pad * D;
+                bwd_store_half_row<D>(tA1, 1.f, p.dv + row * D, valid, c0, xk ? xk + part : nullptr,
+                                      p.cchunks, cstride);
+                bwd_store_half_row<D>(tA2, p.scale, p.dk + row * D, valid, c0, xk, p.cchunks,
+                                      cstride);
             } else {
+                const size_t row = (size_t)bz * p.N + (size_t)(valid ? my : 0);
                 bwd_store_half_row<D>(tA1, p.scale, p.dq + row * D, valid, c0);
             }
         }

@@ -38,7 +38,7 @@ struct DeviceState {
     int num_sms = 0;
     bool attr_set[2][3] = {};
     bool dec_attr_set[2][5] = {};
-    bool bwd_attr_set[2][2] = {};
+    bool bwd_attr_set[2][3] = {};
     // strided tile lists, keyed by (N, W, stride, rows per block, compact-key cap)
     std::map<std::tuple<int, int, int, int, int>, int*> tile_lists;
 };
@@ -355,10 +355,30 @@ size_t bwd_workspace_bytes(int B, int Hq, int N) {
     return ((size_t)B * Hq * N * sizeof(float) + 255) / 256 * 256;
 }
 
+// The compact keys of the local + strided / global-prefix backward: how many any row reads,
+// that count padded to whole tiles, and the query-tile chunks the compact pass is split into
+// (about two CTAs per SM of a 148-SM part, at most one chunk per query tile).
+struct CompactPlan {
+    int ncomp = 0, ncomp_pad = 0, cchunks = 1;
+};
+CompactPlan compact_plan(int B, int Hkv, int N, int W, int stride, int cap) {
+    CompactPlan c;
+    if (cap <= 0 || N <= W) return c;
+    c.ncomp = (int)std::min<long long>(cap, ((long long)N - W + stride - 1) / stride);
+    c.ncomp_pad = (c.ncomp + BN - 1) / BN * BN;
+    const long long ctas = (long long)(c.ncomp_pad / BN) * B * Hkv;
+    const int n_qtiles = (N + BM - 1) / BM;
+    c.cchunks = (int)std::max<long long>(1, std::min<long long>(n_qtiles, (296 + ctas - 1) / ctas));
+    return c;
+}
+size_t compact_part_bytes(const CompactPlan& c, int B, int Hkv, int d) {
+    return (size_t)2 * c.cchunks * B * Hkv * c.ncomp_pad * d * sizeof(float);
+}
+
 template <int D, int KIND>
 int launch_bwd(const swa::BwdParams& bp, int n_tiles, int n_mats, cudaStream_t stream,
                DeviceState& st) {
-    using L = swa::BwdLayout<D, KIND>;
+    using L = swa::BwdLayout<D, KIND == 1 ? 1 : 0>;
     auto kern = swa::attn_bwd_kernel<D, KIND>;
     bool& set = st.bwd_attr_set[D == 128 ? 1 : 0][KIND];
     if (!set) {
@@ -384,8 +404,12 @@ int run_bwd(const swa::BwdParams& bp, const void* out, const void* dout, float* 
         static_cast<const __nv_bfloat16*>(out), static_cast<const __nv_bfloat16*>(dout), delta,
         rows);
     if (cudaPeekAtLastError() != cudaSuccess) return SWA_ERR_CUDA;
-    int rc = launch_bwd<D, 0>(bp, n_tiles, bp.B * bp.Hkv, stream, st);
-    if (rc) return rc;
+    int rc;
+    if (bp.cap > 0 && bp.ncomp > 0 &&
+        (rc = launch_bwd<D, 2>(bp, (bp.ncomp_pad / swa::BN) * bp.cchunks, bp.B * bp.Hkv, stream,
+                               st)))
+        return rc;
+    if ((rc = launch_bwd<D, 0>(bp, n_tiles, bp.B * bp.Hkv, stream, st))) return rc;
     return launch_bwd<D, 1>(bp, n_tiles, bp.B * bp.Hq, stream, st);
 }
 }  // namespace
@@ -722,23 +746,30 @@ size_t swa_attn_bwd_workspace_bytes(int B, int Hq, int N) {
     return bwd_workspace_bytes(B, Hq, N);
 }
 
-int swa_attn_bwd(const void* q, const void* k, const void* v, const void* out, const float* lse,
-                 const void* dout, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int N,
-                 int d, int W, float scale, void* workspace, size_t workspace_bytes,
-                 void* stream) {
+namespace {
+// The backward of the window mask and of its local + strided / global-prefix extensions:
+// cap = 0 is the plain window; otherwise row i also reads the keys r * stride with
+// r < min(ceil(lo(i) / stride), cap).
+int bwd_common(const void* q, const void* k, const void* v, const void* out, const float* lse,
+               const void* dout, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int N,
+               int d, int W, int stride, int cap, float scale, void* workspace,
+               size_t workspace_bytes, void* stream) {
     if (!q || !k || !v || !out || !lse || !dout || !dq || !dk || !dv || !workspace)
         return SWA_ERR_NULL;
     int rc = check_common(B, Hq, Hkv, N, d, scale);
     if (rc) return rc;
-    if (W < 1) return SWA_ERR_SHAPE;
+    if (W < 1 || stride < 1 || cap < 0) return SWA_ERR_SHAPE;
     if (W > N) W = N;
+    if (stride > N) stride = N;  // a stride >= N reaches key 0 only, as stride N does
     // grid: (row tiles, heads); the second grid dimension is at most 65535
     if ((long long)B * Hq > 65535 || (long long)B * Hq * N > (1ll << 38)) return SWA_ERR_SHAPE;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(dout) ||
         !aligned16(dq) || !aligned16(dk) || !aligned16(dv) || !aligned16(workspace) ||
         (reinterpret_cast<uintptr_t>(lse) & 3u) != 0)
         return SWA_ERR_ALIGN;
-    if (workspace_bytes < bwd_workspace_bytes(B, Hq, N)) return SWA_ERR_TOO_LARGE;
+    const CompactPlan cp = compact_plan(B, Hkv, N, W, stride, cap);
+    const size_t delta_bytes = bwd_workspace_bytes(B, Hq, N);
+    if (workspace_bytes < delta_bytes + compact_part_bytes(cp, B, Hkv, d)) return SWA_ERR_TOO_LARGE;
     std::lock_guard<std::mutex> lock(g_mutex);
     DeviceState* st = nullptr;
     if ((rc = current_device_state(&st))) return rc;
@@ -748,11 +779,21 @@ int swa_attn_bwd(const void* q, const void* k, const void* v, const void* out, c
     if ((rc = make_map(&bp.tm_do, dout, d, N, d, (long long)B * Hq, (long long)N * d))) return rc;
     if ((rc = make_map(&bp.tm_k, k, d, N, d, (long long)B * Hkv, (long long)N * d))) return rc;
     if ((rc = make_map(&bp.tm_v, v, d, N, d, (long long)B * Hkv, (long long)N * d))) return rc;
+    if (cap > 0) {
+        const long long ns = (N - 1) / stride + 1;  // keys 0, s, 2s, ... < N
+        if ((rc = make_map(&bp.tm_k2, k, d, ns, (long long)stride * d, (long long)B * Hkv,
+                           (long long)N * d)))
+            return rc;
+        if ((rc = make_map(&bp.tm_v2, v, d, ns, (long long)stride * d, (long long)B * Hkv,
+                           (long long)N * d)))
+            return rc;
+    }
     bp.lse = lse;
     bp.delta = static_cast<const float*>(workspace);
     bp.dq = static_cast<__nv_bfloat16*>(dq);
     bp.dk = static_cast<__nv_bfloat16*>(dk);
     bp.dv = static_cast<__nv_bfloat16*>(dv);
+    bp.cpart = reinterpret_cast<float*>(static_cast<char*>(workspace) + delta_bytes);
     bp.status = st->status;
     bp.wait_limit_ns = kWaitLimitNs;
     bp.B = B;
@@ -760,12 +801,69 @@ int swa_attn_bwd(const void* q, const void* k, const void* v, const void* out, c
     bp.Hkv = Hkv;
     bp.N = N;
     bp.W = W;
+    bp.stride = stride;
+    bp.cap = cap;
+    bp.ncomp = cp.ncomp;
+    bp.ncomp_pad = cp.ncomp_pad;
+    bp.cchunks = cp.cchunks;
     bp.scale = scale;
     bp.scale_log2 = scale * 1.4426950408889634f;
     float* delta = static_cast<float*>(workspace);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (d == 128) return run_bwd<128>(bp, out, dout, delta, s, *st);
     return run_bwd<64>(bp, out, dout, delta, s, *st);
+}
+}  // namespace
+
+int swa_attn_bwd(const void* q, const void* k, const void* v, const void* out, const float* lse,
+                 const void* dout, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int N,
+                 int d, int W, float scale, void* workspace, size_t workspace_bytes,
+                 void* stream) {
+    return bwd_common(q, k, v, out, lse, dout, dq, dk, dv, B, Hq, Hkv, N, d, W, 1, 0, scale,
+                      workspace, workspace_bytes, stream);
+}
+
+size_t strided_attn_bwd_workspace_bytes(int B, int Hq, int Hkv, int N, int d, int W,
+                                        int stride) {
+    if (B < 1 || Hq < 1 || Hkv < 1 || N < 1 || W < 1 || stride < 1 || (d != 64 && d != 128))
+        return 0;
+    const CompactPlan cp = compact_plan(B, Hkv, N, std::min(W, N), std::min(stride, N), 0x7fffffff);
+    return bwd_workspace_bytes(B, Hq, N) + compact_part_bytes(cp, B, Hkv, d);
+}
+
+int strided_attn_bwd(const void* q, const void* k, const void* v, const void* out,
+                     const float* lse, const void* dout, void* dq, void* dk, void* dv, int B,
+                     int Hq, int Hkv, int N, int d, int W, int stride, float scale,
+                     void* workspace, size_t workspace_bytes, void* stream) {
+    if (stride < 1) return SWA_ERR_SHAPE;
+    return bwd_common(q, k, v, out, lse, dout, dq, dk, dv, B, Hq, Hkv, N, d, W, stride,
+                      0x7fffffff, scale, workspace, workspace_bytes, stream);
+}
+
+size_t global_attn_bwd_workspace_bytes(int B, int Hq, int Hkv, int N, int d, int W,
+                                       int n_global) {
+    if (B < 1 || Hq < 1 || Hkv < 1 || N < 1 || W < 1 || n_global < 0 || (d != 64 && d != 128))
+        return 0;
+    const CompactPlan cp = compact_plan(B, Hkv, N, std::min(W, N), 1, std::min(n_global, N));
+    return bwd_workspace_bytes(B, Hq, N) + compact_part_bytes(cp, B, Hkv, d);
+}
+
+int global_attn_bwd(const void* q, const void* k, const void* v, const void* out,
+                    const float* lse, const void* dout, void* dq, void* dk, void* dv, int B,
+                    int Hq, int Hkv, int N, int d, int W, int n_global, float scale,
+                    void* workspace, size_t workspace_bytes, void* stream) {
+    if (n_global < 0) return SWA_ERR_SHAPE;
+    return bwd_common(q, k, v, out, lse, dout, dq, dk, dv, B, Hq, Hkv, N, d, W, 1,
+                      std::min(n_global, std::max(N, 1)), scale, workspace, workspace_bytes,
+                      stream);
+}
+
+int global_attn_fwd_lse(const void* q, const void* k, const void* v, void* out, float* lse,
+                        int B, int Hq, int Hkv, int N, int d, int W, int n_global, float scale,
+                        void* stream) {
+    if (n_global < 0) return SWA_ERR_SHAPE;
+    return strided_common(q, k, v, out, lse, B, Hq, Hkv, N, d, W, 1,
+                          std::min(n_global, std::max(N, 1)), scale, stream);
 }
 
 int swa_cache_append(const void* k_new, const void* v_new, void* k_cache, void* v_cache,

@@ -80,19 +80,40 @@ def _row_chunks(rows: np.ndarray, block: int):
         start = end
 
 
-def _band(qi, rows, kk, W, scale):
-    """Softmax weights of `rows` over the keys kk (absolute positions lo..hi)."""
-    lo = max(0, int(rows[0]) - W + 1)
+def _allowed(rows, keys, W, kind, stride, widen=0):
+    """The mask on (rows x keys): the causal window of W positions (W + widen, for the planted
+    mistake), plus, for "strided", the multiples of `stride` and, for "global", the keys below
+    `stride` (the number of global tokens), each only where j <= i."""
+    i, j = rows[:, None], keys[None, :]
+    m = (j >= i - W + 1 - widen) & (j <= i)
+    if kind == "strided":
+        m |= (j % stride == 0) & (j <= i)
+    elif kind == "global":
+        m |= (j < stride) & (j <= i)
+    return m
+
+
+def _band(qi, rows, kk, W, scale, kind="window", stride=0, widen=0):
+    """Scores of `rows` over the keys any of them may read (a sorted index array `keys`),
+    masked to -inf outside the mask."""
+    lo = max(0, int(rows[0]) - W + 1 - widen)
     hi = int(rows[-1])
-    j = np.arange(lo, hi + 1)
-    allowed = (j[None, :] >= rows[:, None] - W + 1) & (j[None, :] <= rows[:, None])
-    s = scale * (qi @ kk[lo:hi + 1].T)
+    keys = np.arange(lo, hi + 1)
+    if kind == "strided":
+        keys = np.union1d(np.arange(0, lo, stride), keys)
+    elif kind == "global":
+        keys = np.union1d(np.arange(0, min(lo, stride)), keys)
+    allowed = _allowed(rows, keys, W, kind, stride, widen)
+    s = scale * (qi @ kk[keys].T)
     s = np.where(allowed, s, -np.inf)
-    return lo, hi, allowed, s
+    return keys, allowed, s
 
 
-def bwd_bounds(q, k, v, dout, W: int, scale: float, rows=None, block: int = 256):
-    """Exact gradients and their per-element bounds for causal SWA with window W.
+def bwd_bounds(q, k, v, dout, W: int, scale: float, rows=None, block: int = 256,
+               kind: str = "window", stride: int = 0):
+    """Exact gradients and their per-element bounds for causal SWA with window W (kind
+    "window"), or its local + strided ("strided", stride = the stride) or global-prefix
+    ("global", stride = the number of global tokens) extensions.
 
     q, dout: [B, Hq, N, d]; k, v: [B, Hkv, N, d] (fp64 or bf16 bit patterns).
     rows: the query rows whose terms are taken (default all); dq is zero on the other rows and
@@ -113,10 +134,10 @@ def bwd_bounds(q, k, v, dout, W: int, scale: float, rows=None, block: int = 256)
             hk = h // grp
             kk, vv = k[b, hk], v[b, hk]
             for rr in _row_chunks(rows, block):
-                lo, hi, allowed, s = _band(q[b, h, rr], rr, kk, W, scale)
+                keys, allowed, s = _band(q[b, h, rr], rr, kk, W, scale, kind, stride)
                 a = np.exp(s - s.max(axis=1, keepdims=True))
                 a /= a.sum(axis=1, keepdims=True)
-                kb, vb, gr, qr = kk[lo:hi + 1], vv[lo:hi + 1], g[b, h, rr], q[b, h, rr]
+                kb, vb, gr, qr = kk[keys], vv[keys], g[b, h, rr], q[b, h, rr]
                 out = a @ vb
                 dp = np.where(allowed, gr @ vb.T, 0.0)
                 delta = np.sum(a * dp, axis=1)
@@ -129,7 +150,7 @@ def bwd_bounds(q, k, v, dout, W: int, scale: float, rows=None, block: int = 256)
                 dq_s2[b, h, rr] = scale ** 2 * ((ds * ds) @ (kb * kb))
                 dq_D[b, h, rr] = scale * e[:, None] * (a @ np.abs(kb))
                 dq_A[b, h, rr] = scale * (mag @ np.abs(kb))
-                sl = slice(lo, hi + 1)
+                sl = keys
                 dk[b, hk, sl] += scale * (ds.T @ qr)
                 dk_s2[b, hk, sl] += scale ** 2 * ((ds * ds).T @ (qr * qr))
                 dk_D[b, hk, sl] += scale * ((a * e[:, None]).T @ np.abs(qr))
@@ -146,7 +167,8 @@ def bwd_bounds(q, k, v, dout, W: int, scale: float, rows=None, block: int = 256)
             "dv": (dv, bound(dv, dv_s2, 0.0, dv_A))}
 
 
-def emulate_kernel_bwd(q, k, v, dout, W: int, scale: float, plant: str = ""):
+def emulate_kernel_bwd(q, k, v, dout, W: int, scale: float, plant: str = "",
+                       kind: str = "window", stride: int = 0):
     """The backward as the kernels round it (roundings 1-4 above, everything else in fp64):
     the forward's bf16 weights and bf16 output, bf16 a_ij in dV, bf16 ds_ij in dK and dQ,
     bf16 gradients.  `plant` injects a mistake for the tests of the bound's power:
@@ -165,25 +187,24 @@ def emulate_kernel_bwd(q, k, v, dout, W: int, scale: float, plant: str = ""):
             hk = h // grp
             kk, vv = k[b, hk], v[b, hk]
             for rr in _row_chunks(np.arange(N), 256):
-                lo, hi, allowed, s = _band(q[b, h, rr], rr, kk, W, scale)
-                kb, vb, gr, qr = kk[lo:hi + 1], vv[lo:hi + 1], g[b, h, rr], q[b, h, rr]
+                widen = 1 if plant == "window" else 0
+                keys, allowed, s = _band(q[b, h, rr], rr, kk, W, scale, kind, stride, widen)
+                kb, vb, gr, qr = kk[keys], vv[keys], g[b, h, rr], q[b, h, rr]
+                # the forward sees the true mask: scores outside it are -inf
+                s_true = np.where(_allowed(rr, keys, W, kind, stride), s, -np.inf)
                 # forward: bf16 weights against the row maximum, fp32-exact normaliser
-                m = s.max(axis=1, keepdims=True)
-                p = np.exp(s - m)
+                m = s_true.max(axis=1, keepdims=True)
+                p = np.exp(s_true - m)
                 l = p.sum(axis=1, keepdims=True)
                 out16 = bf16_round((bf16_round(p) @ vb) / l)
                 lse = m + np.log(l)
-                if plant == "window":
-                    j = np.arange(lo, hi + 1)
-                    wider = (j[None, :] >= rr[:, None] - W) & (j[None, :] <= rr[:, None])
-                    s = np.where(wider, scale * (qr @ kb.T), -np.inf)
                 a = np.exp(s - lse)
                 dp = np.where(np.isfinite(s), gr @ vb.T, 0.0)
                 delta = 0.0 if plant == "delta" else np.sum(out16 * gr, axis=1)[:, None]
                 ds16 = bf16_round(a * (dp - delta))
                 sq = 1.0 if plant == "scale" else scale
                 dq[b, h, rr] = sq * (ds16 @ kb)
-                sl = slice(lo, hi + 1)
+                sl = keys
                 dk[b, hk, sl] += scale * (ds16.T @ qr)
                 gv = g[b, (h + 1) % Hq, rr] if plant == "head" else gr
                 dv[b, hk, sl] += bf16_round(a).T @ gv

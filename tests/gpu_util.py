@@ -78,3 +78,20 @@ def assert_close(w: swa_inputs.Workload, got: np.ndarray, ref: np.ndarray, label
                              f"{tuple(idx)} gpu={got[tuple(idx)]} ref={ref[tuple(idx)]}; "
                              f"max err {err.max():.3e}")
     return float(err.max())
+
+
+def check_bound_one(a: np.ndarray, r: np.ndarray, bnd: np.ndarray, label: str) -> float:
+    """Element by element: |a - r| <= bnd; returns the worst ratio |a - r| / bnd."""
+    assert np.all(np.isfinite(a)), f"{label}: non-finite"
+    bad = np.abs(a - r) > bnd
+    if bad.any():
+        idx = tuple(np.argwhere(bad)[0])
+        raise AssertionError(f"{label}: {int(bad.sum())} of {a.size} out of tolerance; first "
+                             f"at {idx}: gpu={a[idx]} oracle={r[idx]} bound={bnd[idx]:.3e}")
+    return float(np.max(np.abs(a - r) / bnd)) if a.size else 0.0
+
+
+def check_bound(got, ref, bounds, label: str) -> dict:
+    """dq, dk, dv element by element against per-element bounds; worst ratio per tensor."""
+    return {name: check_bound_one(a, r, bnd, f"{label} {name}")
+            for name, a, r, bnd in zip(("dq", "dk", "dv"), got, ref, bounds)}

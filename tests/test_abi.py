@@ -194,6 +194,40 @@ def test_bwd_validation(L):
     assert call(nb=n - 1) == 8
 
 
+@pytest.mark.parametrize("form", ["strided", "global"])
+def test_strided_and_global_bwd_validation(L, form):
+    f = getattr(L, f"{form}_attn_bwd")
+    wsf = getattr(L, f"{form}_attn_bwd_workspace_bytes")
+    B, Hq, Hkv, N, d, W, x = 2, 4, 2, 3000, 64, 256, 128 if form == "strided" else 64
+    n = wsf(B, Hq, Hkv, N, d, W, x)
+    plain = L.swa_attn_bwd_workspace_bytes(B, Hq, N)
+    assert n > plain  # delta plus the compact keys' partial sums
+    assert wsf(B, Hq, Hkv, N, d, N, x) == plain  # W >= N: no key before any window
+    assert wsf(0, Hq, Hkv, N, d, W, x) == 0 and wsf(B, Hq, Hkv, N, 96, W, x) == 0
+    if form == "global":
+        assert wsf(B, Hq, Hkv, N, d, W, 0) == plain  # no global tokens: the window
+    ok = dict(q=P, k=P, v=P, out=P, lse=P, g=P, dq=P, dk=P, dv=P, B=B, Hq=Hq, Hkv=Hkv, N=N, d=d,
+              W=W, x=x, scale=0.125, ws=P, nb=n)
+
+    def call(**kw):
+        a = {**ok, **kw}
+        return f(a["q"], a["k"], a["v"], a["out"], a["lse"], a["g"], a["dq"], a["dk"], a["dv"],
+                 a["B"], a["Hq"], a["Hkv"], a["N"], a["d"], a["W"], a["x"], a["scale"], a["ws"],
+                 a["nb"], None)
+
+    assert call(dq=None) == 1
+    assert call(W=0) == 2
+    assert call(x=-1) == 2
+    if form == "strided":
+        assert call(x=0) == 2
+    assert call(d=96) == 4
+    assert call(scale=0.0) == 7
+    assert call(dv=P + 8) == 3
+    assert call(nb=n - 1) == 8
+    assert L.global_attn_fwd_lse(P, P, P, P, P, 1, 2, 2, 128, 64, 16, -1, 0.125, None) == 2
+    assert L.global_attn_fwd_lse(P, P, P, P, P + 2, 1, 2, 2, 128, 64, 16, 4, 0.125, None) == 3
+
+
 def test_header_compiles_and_library_links_from_c(tmp_path):
     """The header is valid C and the library links and answers from a C program."""
     import shutil

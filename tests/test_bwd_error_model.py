@@ -6,6 +6,7 @@
    roundings stays inside the per-element bound on every element.
 3. The bound has power: a planted mistake in that emulation (a window one key too wide, a
    dropped delta, a missing scale, the wrong query head) breaks it.
+The same for the local + strided and global-prefix masks.
 """
 import numpy as np
 import pytest
@@ -77,3 +78,26 @@ def test_planted_mistakes_break_the_bound(oracle_mod, plant):
     worst = max(worst_ratio(e, r, model[n][1]) for n, r, e in zip(("dq", "dk", "dv"), ref, emu))
     print(f"planted {plant}: worst ratio {worst:.2f}")
     assert worst > 1.0
+
+
+@pytest.mark.parametrize("kind,B,Hq,Hkv,N,d,W,x", [("strided", 1, 2, 1, 300, 16, 40, 7),
+                                                  ("strided", 2, 3, 3, 200, 32, 1, 64),
+                                                  ("strided", 1, 4, 2, 129, 16, 129, 5),
+                                                  ("global", 1, 2, 2, 300, 16, 33, 10),
+                                                  ("global", 1, 4, 1, 250, 32, 1, 250)])
+def test_masks_gradients_are_the_oracles_and_emulation_within_bound(oracle_mod, kind, B, Hq, Hkv,
+                                                                     N, d, W, x):
+    q, k, v, g = _inputs(3 * N + W + x, B, Hq, Hkv, N, d)
+    sc = 1.0 / np.sqrt(d)
+    ref = oracle_mod.attn_bwd(q, k, v, g, W, sc, kind=kind, stride=x)
+    model = bwd_bounds(q, k, v, g, W, sc, kind=kind, stride=x)
+    emu = emulate_kernel_bwd(q, k, v, g, W, sc, kind=kind, stride=x)
+    for name, r, e in zip(("dq", "dk", "dv"), ref, emu):
+        m, bnd = model[name]
+        np.testing.assert_allclose(m, r, rtol=0, atol=1e-12 * max(1.0, np.abs(r).max()))
+        ratio = worst_ratio(e, r, bnd)
+        print(f"{kind} N={N} W={W} x={x} {name}: worst |emulation - oracle| / bound = {ratio:.3f}")
+        assert ratio <= 1.0
+    planted = emulate_kernel_bwd(q, k, v, g, W, sc, plant="delta", kind=kind, stride=x)
+    assert max(worst_ratio(e, r, model[n][1])
+               for n, r, e in zip(("dq", "dk", "dv"), ref, planted)) > 1.0

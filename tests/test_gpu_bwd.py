@@ -23,8 +23,8 @@ import oracle
 import swa_inputs
 from swa_inputs import f32_to_bf16_bits
 import sparse_causal_attention_swa_b300 as pkg
-from bwd_error_model import bwd_bounds, worst_ratio
-from gpu_util import canary_intact, out_like, to_dev, to_f64
+from bwd_error_model import bwd_bounds
+from gpu_util import canary_intact, check_bound as _check, check_bound_one as _check_one, out_like, to_dev, to_f64
 
 pytestmark = pytest.mark.gpu
 
@@ -51,23 +51,6 @@ def _bwd_gpu(q, k, v, g, W, scale):
     for t, b in ((dq, bq), (dk, bk), (dv, bv)):
         assert canary_intact(b, t.numel()), "write past the end of a gradient"
     return to_f64(dq), to_f64(dk), to_f64(dv)
-
-
-def _check_one(a, r, bnd, label):
-    """Element by element: |a - r| <= bnd; returns the worst ratio |a - r| / bnd."""
-    assert np.all(np.isfinite(a)), f"{label}: non-finite"
-    bad = np.abs(a - r) > bnd
-    if bad.any():
-        idx = tuple(np.argwhere(bad)[0])
-        raise AssertionError(f"{label}: {int(bad.sum())} of {a.size} out of tolerance; first "
-                             f"at {idx}: gpu={a[idx]} oracle={r[idx]} bound={bnd[idx]:.3e}")
-    return worst_ratio(a, r, bnd)
-
-
-def _check(got, ref, bounds, label):
-    """dq, dk, dv element by element; returns the worst ratio per tensor."""
-    return {name: _check_one(a, r, bnd, f"{label} {name}")
-            for name, a, r, bnd in zip(("dq", "dk", "dv"), got, ref, bounds)}
 
 
 def _case(B, Hq, Hkv, N, d, W, seed, scale=None):
