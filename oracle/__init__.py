@@ -28,6 +28,10 @@ Parity status per function (what pins it is listed in the tests):
                        the full causal denominator 8 (ln 8); W = 1 (the row's own
                        score); exp(lse) equals the softmax denominator used by attn
                        (weights_row); brute force on tiny inputs.
+  diff_bwd             pinned: central differences of sum(dout * diff_heads(...)) for
+                       every entry of dq1, dk1, dq2, dk2, dv and every head's lambda;
+                       lambda = 0 gives attn_bwd for map 1 and no gradient to map 2;
+                       equal maps give dq2 = -lambda dq1 and dv = (1 - lambda) x attn_bwd's.
   decode, cache_slot   pinned: the SWA note's W = 3 slot walk-through (§4.2),
                        equality with row t of attn(kind="window") over the whole
                        sequence when the cache was filled by rolling writes,
@@ -101,6 +105,9 @@ def _load():
             lib.oracle_attn_bwd_rows.argtypes = [ctypes.c_int, _P, _P, _P, _P, _P, _P, _P, _I64,
                                                  _I64, _I64, _I64, _I64, _I64, _I64,
                                                  ctypes.c_double, _P, _I64, ctypes.c_int]
+            lib.oracle_diff_bwd.restype = ctypes.c_int
+            lib.oracle_diff_bwd.argtypes = [_P] * 13 + [_I64] * 6 + [ctypes.c_double,
+                                                                    ctypes.c_int]
             lib.oracle_cache_slot.restype = ctypes.c_int64
             lib.oracle_cache_slot.argtypes = [_I64, _I64]
             lib.oracle_max_threads.restype = ctypes.c_int
@@ -275,6 +282,29 @@ def attn_bwd(q, k, v, dout, W: int, scale: float, kind: str = "window", stride: 
     if rc != 0:
         raise ValueError(f"oracle_attn_bwd rejected its arguments (code {rc})")
     return dq, dk, dv
+
+
+def diff_bwd(q1, k1, q2, k2, v, lams, dout, W: int, scale: float, nthreads: int = 0):
+    """Gradients of differential attention (A1 - lambda_h A2) V, both maps under the window W
+    (0 or W >= N: causal), one lambda per query head (``lams`` [Hq]; a scalar lambda is the
+    same value for every head).  Returns (dq1, dk1, dq2, dk2, dv, dlam) with dlam [Hq] the
+    gradient of each head's lambda (summed over batches)."""
+    lib = _load()
+    a = [_f64(x) for x in (q1, k1, q2, k2, v)]
+    g64 = _f64(dout)
+    B, Hq, N, d = a[0].shape
+    Hkv = a[1].shape[1]
+    lam = np.ascontiguousarray(np.broadcast_to(np.asarray(lams, dtype=np.float64), (Hq,)))
+    dq1, dq2 = np.empty_like(a[0]), np.empty_like(a[0])
+    dk1, dk2, dv = np.empty_like(a[1]), np.empty_like(a[1]), np.empty_like(a[1])
+    dlam = np.empty(Hq, dtype=np.float64)
+    Wm = N if W == 0 else int(W)
+    rc = lib.oracle_diff_bwd(*[_ptr(x) for x in a], _ptr(lam), _ptr(g64), _ptr(dq1), _ptr(dk1),
+                             _ptr(dq2), _ptr(dk2), _ptr(dv), _ptr(dlam), B, Hq, Hkv, N, d, Wm,
+                             float(scale), int(nthreads))
+    if rc != 0:
+        raise ValueError(f"oracle_diff_bwd rejected its arguments (code {rc})")
+    return dq1, dk1, dq2, dk2, dv, dlam
 
 
 def cache_slot(j: int, W: int) -> int:

@@ -459,6 +459,98 @@ int oracle_attn_bwd_rows(int kind, const double* q, const double* k, const doubl
     return 0;
 }
 
+/*
+ * Gradients of the differential attention forward ([AVpt] "Atenção Diferencial",
+ * out = (A1 - lambda_h A2) V, both maps under the window mask of width W, W >= N causal),
+ * with one lambda per query head (lams[h]), for an upstream gradient dout.  The chain rule
+ * row by row, with da_ij = dout_i . v_j:
+ *   dv_j   += (a1_ij - lambda a2_ij) dout_i               (out is linear in v)
+ *   dz1_ij  = a1_ij (da_ij - sum_j' a1_ij' da_ij')        (the softmax Jacobian of map 1)
+ *   dz2_ij  = a2_ij (-lambda da_ij + lambda sum_j' a2_ij' da_ij')   (map 2 enters with -lambda)
+ *   dq1_i  += scale sum_j dz1_ij k1_j,   dk1_j += scale dz1_ij q1_i   (map 2 likewise)
+ *   dlam_h += -sum_j a2_ij da_ij                          (d out_i / d lambda = -(A2 V)_i)
+ * dk1, dk2, dv of a KV head sum over its query heads; dlam[h] sums over batches and rows.
+ */
+int oracle_diff_bwd(const double* q1, const double* k1, const double* q2, const double* k2,
+                    const double* v, const double* lams, const double* dout, double* dq1,
+                    double* dk1, double* dq2, double* dk2, double* dv, double* dlam, int64_t B,
+                    int64_t Hq, int64_t Hkv, int64_t N, int64_t d, int64_t W, double scale,
+                    int nthreads) {
+    if (check_shape(B, Hq, Hkv, N, d)) return 2;
+    if (W < 1) return 2;
+    const int64_t g = Hq / Hkv;
+    const size_t nq = (size_t)(B * Hq * N * d), nk = (size_t)(B * Hkv * N * d);
+    memset(dq1, 0, sizeof(double) * nq);
+    memset(dq2, 0, sizeof(double) * nq);
+    memset(dk1, 0, sizeof(double) * nk);
+    memset(dk2, 0, sizeof(double) * nk);
+    memset(dv, 0, sizeof(double) * nk);
+    double* dlam_bh = (double*)calloc((size_t)(B * Hq), sizeof(double));
+    if (!dlam_bh) return 3;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#endif
+    /* one (batch, KV head) per task: its dk1, dk2, dv and its heads' dlam_bh are its own */
+#pragma omp parallel
+    {
+        double* M = (double*)malloc(sizeof(double) * (size_t)N);
+        double* z = (double*)malloc(sizeof(double) * (size_t)N);
+        double* a1 = (double*)malloc(sizeof(double) * (size_t)N);
+        double* a2 = (double*)malloc(sizeof(double) * (size_t)N);
+        double* da = (double*)malloc(sizeof(double) * (size_t)N);
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t t = 0; t < B * Hkv; ++t) {
+            const int64_t b = t / Hkv, hk = t % Hkv;
+            const size_t koff = (size_t)((b * Hkv + hk) * N * d);
+            for (int64_t h = hk * g; h < (hk + 1) * g; ++h) {
+                const double lam = lams[h];
+                for (int64_t i = 0; i < N; ++i) {
+                    const size_t qoff = (size_t)(((b * Hq + h) * N + i) * d);
+                    mask_row(MASK_WINDOW, i, W, 0, M);
+                    softmax_row(q1 + qoff, k1 + koff, d, i, scale, M, z, a1);
+                    softmax_row(q2 + qoff, k2 + koff, d, i, scale, M, z, a2);
+                    double s1 = 0.0, s2 = 0.0;
+                    for (int64_t j = 0; j <= i; ++j) {
+                        da[j] = 0.0;
+                        if (M[j] != 0.0) continue;
+                        const double* vj = v + koff + (size_t)(j * d);
+                        double dot = 0.0;
+                        for (int64_t c = 0; c < d; ++c) dot += dout[qoff + c] * vj[c];
+                        da[j] = dot;
+                        s1 += a1[j] * dot;
+                        s2 += a2[j] * dot;
+                    }
+                    dlam_bh[b * Hq + h] -= s2;
+                    for (int64_t j = 0; j <= i; ++j) {
+                        if (M[j] != 0.0) continue;
+                        const double dz1 = a1[j] * (da[j] - s1);
+                        const double dz2 = a2[j] * (-lam * da[j] + lam * s2);
+                        const size_t jo = koff + (size_t)(j * d);
+                        for (int64_t c = 0; c < d; ++c) {
+                            dq1[qoff + c] += scale * dz1 * k1[jo + c];
+                            dk1[jo + c] += scale * dz1 * q1[qoff + c];
+                            dq2[qoff + c] += scale * dz2 * k2[jo + c];
+                            dk2[jo + c] += scale * dz2 * q2[qoff + c];
+                            dv[jo + c] += (a1[j] - lam * a2[j]) * dout[qoff + c];
+                        }
+                    }
+                }
+            }
+        }
+        free(M);
+        free(z);
+        free(a1);
+        free(a2);
+        free(da);
+    }
+    for (int64_t h = 0; h < Hq; ++h) {
+        dlam[h] = 0.0;
+        for (int64_t b = 0; b < B; ++b) dlam[h] += dlam_bh[b * Hq + h];
+    }
+    free(dlam_bh);
+    return 0;
+}
+
 /* Slot of absolute position j in a W-slot rolling cache ([SWA] §4.2, 0-indexed). */
 int64_t oracle_cache_slot(int64_t j, int64_t W) { return (W < 1 || j < 0) ? -1 : j % W; }
 

@@ -686,3 +686,63 @@ def test_bwd_row_subsets_partition_the_gradients(oracle_mod):
         np.testing.assert_allclose(x[:, :, 9:14], f[:, :, 9:14], rtol=0, atol=1e-13)
     with pytest.raises(ValueError):
         oracle_mod.attn_bwd(q, k, v, g, W, sc, rows=np.array([0, 23]))
+
+
+# ------------------------------------------------------------------ differential gradients
+def _diff_inputs(seed, B=1, Hq=4, Hkv=2, N=11, d=4):
+    rng = np.random.default_rng(seed)
+    return ([rng.standard_normal((B, h, N, d)) for h in (Hq, Hkv, Hq, Hkv, Hkv)],
+            rng.standard_normal((B, Hq, N, d)))
+
+
+@pytest.mark.parametrize("W", [4, 0])
+def test_diff_bwd_matches_central_differences(oracle_mod, W):
+    """Every entry of dq1, dk1, dq2, dk2, dv and each head's lambda against a central difference
+    of L = sum(dout * out) through the (separately pinned) differential forward."""
+    (q1, k1, q2, k2, v), g = _diff_inputs(120 + W, B=2)
+    lams = np.array([0.8, 0.3, -0.2, 1.1])
+    scale, h = 0.5, 1e-5
+    grads = oracle_mod.diff_bwd(q1, k1, q2, k2, v, lams, g, W, scale)
+    args = {"q1": q1, "k1": k1, "q2": q2, "k2": k2, "v": v}
+
+    def loss(a, lm):
+        return float(np.sum(g * oracle_mod.diff_heads(a["q1"], a["k1"], a["q2"], a["k2"], a["v"],
+                                                      lm, scale, W=W)))
+
+    for name, grad in zip(("q1", "k1", "q2", "k2", "v"), grads[:5]):
+        x = args[name]
+        fd = np.empty_like(x)
+        for idx in np.ndindex(x.shape):
+            ap, am = dict(args), dict(args)
+            ap[name], am[name] = x.copy(), x.copy()
+            ap[name][idx] += h
+            am[name][idx] -= h
+            fd[idx] = (loss(ap, lams) - loss(am, lams)) / (2 * h)
+        assert np.max(np.abs(fd - grad)) < 1e-7 * max(1.0, np.max(np.abs(grad))), name
+    fd = np.empty(4)
+    for i in range(4):
+        lp, lm = lams.copy(), lams.copy()
+        lp[i] += h
+        lm[i] -= h
+        fd[i] = (loss(args, lp) - loss(args, lm)) / (2 * h)
+    np.testing.assert_allclose(grads[5], fd, rtol=0, atol=1e-7 * max(1.0, np.abs(fd).max()))
+
+
+def test_diff_bwd_reductions(oracle_mod):
+    (q1, k1, q2, k2, v), g = _diff_inputs(130, B=2, Hq=6, Hkv=3, N=17, d=5)
+    W, sc = 6, 0.4
+    # lambda = 0: map 1 is window attention, map 2 gets no gradient
+    dq1, dk1, dq2, dk2, dv, dlam = oracle_mod.diff_bwd(q1, k1, q2, k2, v, 0.0, g, W, sc)
+    ref = oracle_mod.attn_bwd(q1, k1, v, g, W, sc)
+    for a, b in zip((dq1, dk1, dv), ref):
+        np.testing.assert_allclose(a, b, rtol=0, atol=1e-13)
+    assert np.all(dq2 == 0.0) and np.all(dk2 == 0.0)
+    # dlam = -sum_i dout_i . (A2 V)_i
+    out2 = oracle_mod.attn(q2, k2, v, W, sc, kind="window")
+    np.testing.assert_allclose(dlam, -np.sum(g * out2, axis=(0, 2, 3)), rtol=0, atol=1e-12)
+    # equal maps: dq2 = -lambda dq1, dk2 = -lambda dk1, dv = (1 - lambda) x the attention's
+    lam = 0.7
+    dq1, dk1, dq2, dk2, dv, _ = oracle_mod.diff_bwd(q1, k1, q1, k1, v, lam, g, W, sc)
+    np.testing.assert_allclose(dq2, -lam * dq1, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(dk2, -lam * dk1, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(dv, (1 - lam) * ref[2], rtol=0, atol=1e-13)
