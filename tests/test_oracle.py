@@ -689,7 +689,7 @@ def test_bwd_row_subsets_partition_the_gradients(oracle_mod):
 
 
 # ------------------------------------------------------------------ differential gradients
-def _diff_inputs(seed, B=1, Hq=4, Hkv=2, N=11, d=4):
+def _diff_bwd_inputs(seed, B=1, Hq=4, Hkv=2, N=11, d=4):
     rng = np.random.default_rng(seed)
     return ([rng.standard_normal((B, h, N, d)) for h in (Hq, Hkv, Hq, Hkv, Hkv)],
             rng.standard_normal((B, Hq, N, d)))
@@ -699,7 +699,7 @@ def _diff_inputs(seed, B=1, Hq=4, Hkv=2, N=11, d=4):
 def test_diff_bwd_matches_central_differences(oracle_mod, W):
     """Every entry of dq1, dk1, dq2, dk2, dv and each head's lambda against a central difference
     of L = sum(dout * out) through the (separately pinned) differential forward."""
-    (q1, k1, q2, k2, v), g = _diff_inputs(120 + W, B=2)
+    (q1, k1, q2, k2, v), g = _diff_bwd_inputs(120 + W, B=2)
     lams = np.array([0.8, 0.3, -0.2, 1.1])
     scale, h = 0.5, 1e-5
     grads = oracle_mod.diff_bwd(q1, k1, q2, k2, v, lams, g, W, scale)
@@ -729,7 +729,7 @@ def test_diff_bwd_matches_central_differences(oracle_mod, W):
 
 
 def test_diff_bwd_reductions(oracle_mod):
-    (q1, k1, q2, k2, v), g = _diff_inputs(130, B=2, Hq=6, Hkv=3, N=17, d=5)
+    (q1, k1, q2, k2, v), g = _diff_bwd_inputs(130, B=2, Hq=6, Hkv=3, N=17, d=5)
     W, sc = 6, 0.4
     # lambda = 0: map 1 is window attention, map 2 gets no gradient
     dq1, dk1, dq2, dk2, dv, dlam = oracle_mod.diff_bwd(q1, k1, q2, k2, v, 0.0, g, W, sc)
