@@ -253,6 +253,34 @@ int global_attn_bwd(const void* q, const void* k, const void* v, const void* out
                     int Hq, int Hkv, int N, int d, int W, int n_global, float scale,
                     void* workspace, size_t workspace_bytes, void* stream);
 
+/*
+ * Backward pass of differential attention ([AVpt] "Atenção Diferencial", out = (A1 - lambda_h
+ * A2) V; both maps under the window W as in diff_swa_attn_fwd, W >= N causal as in
+ * diff_attn_fwd / diff_attn_fwd_heads).  With dout = dL/dout and da_ij = dout_i . v_j:
+ *   dv_j  = sum_i (a1_ij - lambda_h a2_ij) dout_i
+ *   dq1_i = scale sum_j a1_ij (da_ij - dout_i . out1_i) k1_j,   dk1 likewise
+ *   dq2_i = -lambda_h scale sum_j a2_ij (da_ij - dout_i . out2_i) k2_j,   dk2 likewise
+ *   dlambda_h = -sum over batches and rows of dout_i . out2_i
+ * where out1 = A1 V and out2 = A2 V with their row log-sum-exps lse1, lse2 are what
+ * swa_attn_fwd_lse(q1, k1, v, ...) and swa_attn_fwd_lse(q2, k2, v, ...) write with the same
+ * W and scale (the training forward runs those two calls; diff_swa_attn_fwd gives out itself).
+ *   lambda / lambda_heads: as diff_swa_attn_fwd (lambda_heads: float32 [Hq] device, or NULL)
+ *   dlambda:   float32 [Hq] device (4-byte aligned), each head's lambda gradient, or NULL
+ *   q1, q2, out1, out2, dout, dq1, dq2: bf16 [B, Hq, N, d];  k1, k2, v, dk1, dk2, dv: bf16
+ *   [B, Hkv, N, d] (dk and dv of a KV head sum over its query heads);  lse1, lse2: fp32 [B, Hq, N]
+ *   workspace: at least diff_attn_bwd_workspace_bytes(B, Hq, Hkv, N, d) bytes, 16-byte aligned
+ *              (two deltas and map 1's fp32 dv)
+ * Map 2 runs the SWA backward kernels with each step's weights scaled by -lambda_h; dv of the
+ * two maps is summed in fp32 and rounded once.  Deterministic.  Errors as swa_attn_bwd.
+ */
+size_t diff_attn_bwd_workspace_bytes(int B, int Hq, int Hkv, int N, int d);
+int diff_attn_bwd(const void* q1, const void* k1, const void* q2, const void* k2, const void* v,
+                  float lambda, const float* lambda_heads, const void* out1, const float* lse1,
+                  const void* out2, const float* lse2, const void* dout, void* dq1, void* dk1,
+                  void* dq2, void* dk2, void* dv, float* dlambda, int B, int Hq, int Hkv, int N,
+                  int d, int W, float scale, void* workspace, size_t workspace_bytes,
+                  void* stream);
+
 int swa_decode_fwd(const void* q, const void* k_cache, const void* v_cache, const int* pos,
                    void* out, int B, int Hq, int Hkv, int W, int d, float scale, void* workspace,
                    size_t workspace_bytes, void* stream);

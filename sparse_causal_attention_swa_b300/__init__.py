@@ -11,7 +11,7 @@ Low-level calls (pointers or tensors, explicit sizes, asynchronous on ``stream``
     strided_attn_fwd_noalloc, swa_attn_fwd_lse, strided_attn_fwd_lse, global_attn_fwd,
     global_attn_fwd_lse, swa_attn_bwd_workspace_bytes, swa_attn_bwd,
     strided_attn_bwd_workspace_bytes, strided_attn_bwd, global_attn_bwd_workspace_bytes,
-    global_attn_bwd,
+    global_attn_bwd, diff_attn_bwd_workspace_bytes, diff_attn_bwd,
     swa_decode_workspace_bytes, swa_decode_fwd, swa_cache_append, swa_chunk_fwd,
     swa_cache_gather,
     swa_status_string, swa_device_status, swa_watchdog_selftest
@@ -85,6 +85,11 @@ def load():
         lib.global_attn_bwd.restype = I
         lib.global_attn_fwd_lse.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, F, P]
         lib.global_attn_fwd_lse.restype = I
+        lib.diff_attn_bwd_workspace_bytes.argtypes = [I, I, I, I, I]
+        lib.diff_attn_bwd_workspace_bytes.restype = ctypes.c_size_t
+        lib.diff_attn_bwd.argtypes = [P, P, P, P, P, F, P, P, P, P, P, P, P, P, P, P, P, P, I, I,
+                                      I, I, I, I, F, P, ctypes.c_size_t, P]
+        lib.diff_attn_bwd.restype = I
         SZ = ctypes.c_size_t
         lib.swa_decode_workspace_bytes.argtypes = [I, I, I, I]
         lib.swa_decode_workspace_bytes.restype = SZ
@@ -269,6 +274,24 @@ def global_attn_bwd(q, k, v, out, lse, dout, dq, dk, dv, B, Hq, Hkv, N, d, W, n_
                                   _ptr(dq), _ptr(dk), _ptr(dv), B, Hq, Hkv, N, d, int(W),
                                   int(n_global), float(scale), _ptr(workspace),
                                   int(workspace_bytes), _stream(stream)), "global_attn_bwd")
+
+
+def diff_attn_bwd_workspace_bytes(B, Hq, Hkv, N, d) -> int:
+    return int(load().diff_attn_bwd_workspace_bytes(B, Hq, Hkv, N, d))
+
+
+def diff_attn_bwd(q1, k1, q2, k2, v, lam, lam_heads, out1, lse1, out2, lse2, dout, dq1, dk1,
+                  dq2, dk2, dv, dlam, B, Hq, Hkv, N, d, W, scale, workspace, workspace_bytes,
+                  stream=None):
+    """Gradients of differential attention; out1 / lse1 and out2 / lse2 come from
+    swa_attn_fwd_lse on (q1, k1, v) and (q2, k2, v); ``dlam`` (float32 [Hq] or None) receives
+    each head's lambda gradient."""
+    _check(load().diff_attn_bwd(_ptr(q1), _ptr(k1), _ptr(q2), _ptr(k2), _ptr(v), float(lam),
+                                _ptr(lam_heads), _ptr(out1), _ptr(lse1), _ptr(out2), _ptr(lse2),
+                                _ptr(dout), _ptr(dq1), _ptr(dk1), _ptr(dq2), _ptr(dk2), _ptr(dv),
+                                _ptr(dlam), B, Hq, Hkv, N, d, int(W), float(scale),
+                                _ptr(workspace), int(workspace_bytes), _stream(stream)),
+           "diff_attn_bwd")
 
 
 def swa_device_status(stream=None) -> int:

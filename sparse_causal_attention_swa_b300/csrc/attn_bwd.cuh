@@ -65,6 +65,13 @@ struct BwdParams {
     int ncomp;          // compact keys any row reads: ncomp(N - 1)
     int ncomp_pad;      // ncomp rounded up to a whole 128-row tile
     int cchunks;        // query-tile chunks of the compact dk/dv pass
+    // the second map of differential attention enters the loss with weight mu_h = -lambda_h:
+    // mu_mode 1 scales the weights in dV and the dS of every step by mu of its query head
+    int mu_mode;
+    float lam;                // lambda of every head, unless lam_heads is set
+    const float* lam_heads;   // [Hq] per-head lambda (device), or null
+    float* dv32_out;          // dk/dv: write dV unrounded (fp32 [B*Hkv][N][d]) here, not dv
+    const float* dv32_in;     // dk/dv: fp32 [B*Hkv][N][d] added to dV before rounding, or null
     float scale, scale_log2;
 };
 
@@ -157,10 +164,11 @@ __device__ __forceinline__ void bwd_store_half_row(uint32_t taddr, float mul,
 }
 
 // Columns [32 c0, 32 c0 + D/2) of fp32 from TMEM lane to the same columns of an fp32 row
-// (zeros when `have` is false: no product wrote the accumulator).
+// (zeros when `have` is false: no product wrote the accumulator).  `have` must be the same in
+// every lane of the warp (tcgen05.ld is warp-collective); only lanes with `valid` store.
 template <int D>
 __device__ __forceinline__ void bwd_store_half_row_f32(uint32_t taddr, float* dst, bool have,
-                                                       int c0) {
+                                                       bool valid, int c0) {
 #pragma unroll
     for (int cc = 0; cc < D / 64; ++cc) {
         const int c = c0 + cc;
@@ -171,11 +179,26 @@ __device__ __forceinline__ void bwd_store_half_row_f32(uint32_t taddr, float* ds
 #pragma unroll
             for (int e = 0; e < 32; ++e) rr[e] = 0u;
         }
+        if (!valid) continue;
         float4* o = reinterpret_cast<float4*>(dst + c * 32);
 #pragma unroll
         for (int v4 = 0; v4 < 8; ++v4)
             o[v4] = make_float4(__uint_as_float(rr[4 * v4]), __uint_as_float(rr[4 * v4 + 1]),
                                 __uint_as_float(rr[4 * v4 + 2]), __uint_as_float(rr[4 * v4 + 3]));
+    }
+}
+
+// The weight mu of query head h (1, or -lambda_h for the second differential map), as the
+// log2 of its magnitude (folded into the row's log-sum-exp: |mu| p = exp2(x - lse2 + log2|mu|))
+// and the sign bits to flip in a packed bf16 pair.
+__device__ __forceinline__ void bwd_mu(const BwdParams& p, int h, float& log2_abs,
+                                       uint32_t& sign2) {
+    log2_abs = 0.f;
+    sign2 = 0u;
+    if (p.mu_mode) {
+        const float mu = -(p.lam_heads ? p.lam_heads[h] : p.lam);
+        log2_abs = log2f(fabsf(mu));  // -inf for mu = 0: every weight becomes 0
+        sign2 = signbit(mu) ? 0x80008000u : 0u;
     }
 }
 
@@ -207,6 +230,28 @@ __global__ void bwd_delta_kernel(const __nv_bfloat16* __restrict__ out,
         }
     }
     delta[r] = acc;
+}
+
+// dlam[h] = -sum over batches and rows of delta[b, h, i] (the gradient of a differential
+// head's lambda: d out_i / d lambda = -(A2 V)_i, and delta2_i = dout_i . (A2 V)_i); one CTA of
+// 256 threads per head, a fixed summation order, so the result is deterministic.
+__global__ void __launch_bounds__(256) bwd_dlam_kernel(const float* __restrict__ delta2,
+                                                       float* __restrict__ dlam, int B, int Hq,
+                                                       int N) {
+    __shared__ float part[256];
+    const int h = blockIdx.x;
+    float acc = 0.f;
+    for (int b = 0; b < B; ++b) {
+        const float* r = delta2 + ((size_t)b * Hq + h) * N;
+        for (int i = threadIdx.x; i < N; i += 256) acc += r[i];
+    }
+    part[threadIdx.x] = acc;
+    __syncthreads();
+    for (int w = 128; w > 0; w >>= 1) {
+        if ((int)threadIdx.x < w) part[threadIdx.x] += part[threadIdx.x + w];
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) dlam[h] = -part[0];
 }
 
 // The kernels share their set-up; KIND 0 is the dk/dv kernel, KIND 1 the dq kernel, KIND 2
@@ -526,9 +571,14 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) attn_bwd_kernel(const __grid_c
         const bool valid = COMPACT ? (my < p.ncomp_pad) : (my < p.N);
         const float sl2 = p.scale_log2;
         float lse2_row = 0.f, delta_row = 0.f;  // dq kernel: the row's own values
-        if (!DKDV && valid) {
-            lse2_row = __ldg(p.lse + (size_t)bz * p.N + my) * LOG2E_F;
-            delta_row = __ldg(p.delta + (size_t)bz * p.N + my);
+        float mu_l2 = 0.f;                       // log2 |mu| of the step's query head
+        uint32_t mu_sign = 0u;                   // its sign, on a packed bf16 pair
+        if (!DKDV) {
+            bwd_mu(p, bz % p.Hq, mu_l2, mu_sign);
+            if (valid) {
+                lse2_row = __ldg(p.lse + (size_t)bz * p.N + my) * LOG2E_F - mu_l2;
+                delta_row = __ldg(p.delta + (size_t)bz * p.N + my);
+            }
         }
         auto wait = [&](uint32_t bb, uint32_t parity) -> bool {
             const bool r = mbar_wait_bounded(bb, parity, abort_flag, lim);
@@ -541,11 +591,13 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) attn_bwd_kernel(const __grid_c
             float lse2_c[2], delta_c[2];
             const int ct = step_tile(s);
             if (DKDV) {
-                const size_t base = (size_t)step_qmat(s) * p.N;
+                const int qm = step_qmat(s);
+                bwd_mu(p, qm % p.Hq, mu_l2, mu_sign);
+                const size_t base = (size_t)qm * p.N;
 #pragma unroll
                 for (int cc = 0; cc < 2; ++cc) {
                     const int qc = ct * BM + (2 * half + cc) * 32 + (int)lane;
-                    lse2_c[cc] = (qc < p.N) ? __ldg(p.lse + base + qc) * LOG2E_F : 0.f;
+                    lse2_c[cc] = (qc < p.N) ? __ldg(p.lse + base + qc) * LOG2E_F - mu_l2 : 0.f;
                     delta_c[cc] = (qc < p.N) ? __ldg(p.delta + base + qc) : 0.f;
                 }
             }
@@ -600,7 +652,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) attn_bwd_kernel(const __grid_c
                 for (int cc = 0; cc < 2; ++cc) {
 #pragma unroll
                     for (int u = 0; u < 16; ++u)
-                        pk[u] = pack_bf16x2(pv[cc * 32 + 2 * u], pv[cc * 32 + 2 * u + 1]);
+                        pk[u] = pack_bf16x2(pv[cc * 32 + 2 * u], pv[cc * 32 + 2 * u + 1]) ^ mu_sign;
                     tmem_st16(tS + (uint32_t)(half * 64 + cc * 16), pk);
                 }
                 tmem_wait_st();
@@ -626,7 +678,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) attn_bwd_kernel(const __grid_c
                             DKDV ? __shfl_sync(0xffffffffu, delta_c[cc], 2 * u + e) : delta_row;
                         dsv[e] = pv[cc * 32 + 2 * u + e] * (__uint_as_float(dr[2 * u + e]) - dl);
                     }
-                    dsw[cc * 16 + u] = pack_bf16x2(dsv[0], dsv[1]);
+                    dsw[cc * 16 + u] = pack_bf16x2(dsv[0], dsv[1]) ^ mu_sign;
                 }
             }
             // dP has been read: the issuer may overwrite it with the next step's
@@ -671,8 +723,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) attn_bwd_kernel(const __grid_c
             if (COMPACT) {
                 // fp32 partial sums of this chunk (dK unscaled, as the window kernel's)
                 float* pk = p.cpart + (((size_t)chunk * p.B * p.Hkv + bz) * p.ncomp_pad + my) * D;
-                bwd_store_half_row_f32<D>(tA1, pk + part, n_steps > 0, c0);
-                bwd_store_half_row_f32<D>(tA2, pk, n_steps > 0, c0);
+                bwd_store_half_row_f32<D>(tA1, pk + part, n_steps > 0, true, c0);
+                bwd_store_half_row_f32<D>(tA2, pk, n_steps > 0, true, c0);
             } else if (DKDV) {
                 const size_t row = (size_t)bz * p.N + (size_t)(valid ? my : 0);
                 // a key that is also a compact key takes the compact pass's partial sums
@@ -680,8 +732,15 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) attn_bwd_kernel(const __grid_c
                 if (p.cap > 0 && valid && my % p.stride == 0 && my / p.stride < p.ncomp)
                     xk = p.cpart + ((size_t)bz * p.ncomp_pad + my / p.stride) * D;
                 const size_t cstride = (size_t)p.B * p.Hkv * p.ncomp_pad * D;
-                bwd_store_half_row<D>(tA1, 1.f, p.dv + row * D, valid, c0, xk ? xk + part : nullptr,
-                                      p.cchunks, cstride);
+                if (p.dv32_out) {  // the first differential map: dV stays fp32 for the second
+                    bwd_store_half_row_f32<D>(tA1, p.dv32_out + row * D, true, valid, c0);
+                } else if (p.dv32_in) {  // the second map: dV of both maps, rounded once
+                    bwd_store_half_row<D>(tA1, 1.f, p.dv + row * D, valid, c0,
+                                          p.dv32_in + row * D, 1, 0);
+                } else {
+                    bwd_store_half_row<D>(tA1, 1.f, p.dv + row * D, valid, c0,
+                                          xk ? xk + part : nullptr, p.cchunks, cstride);
+                }
                 bwd_store_half_row<D>(tA2, p.scale, p.dk + row * D, valid, c0, xk, p.cchunks,
                                       cstride);
             } else {

@@ -11,6 +11,7 @@
 #include <map>
 #include <mutex>
 #include <tuple>
+#include <type_traits>
 #include <utility>
 #include <vector>
 
@@ -814,6 +815,109 @@ int bwd_common(const void* q, const void* k, const void* v, const void* out, con
     return run_bwd<64>(bp, out, dout, delta, s, *st);
 }
 }  // namespace
+
+size_t diff_attn_bwd_workspace_bytes(int B, int Hq, int Hkv, int N, int d) {
+    if (B < 1 || Hq < 1 || Hkv < 1 || N < 1 || (d != 64 && d != 128)) return 0;
+    return 2 * bwd_workspace_bytes(B, Hq, N) + (size_t)B * Hkv * N * d * sizeof(float);
+}
+
+int diff_attn_bwd(const void* q1, const void* k1, const void* q2, const void* k2, const void* v,
+                  float lambda, const float* lambda_heads, const void* out1, const float* lse1,
+                  const void* out2, const float* lse2, const void* dout, void* dq1, void* dk1,
+                  void* dq2, void* dk2, void* dv, float* dlambda, int B, int Hq, int Hkv, int N,
+                  int d, int W, float scale, void* workspace, size_t workspace_bytes,
+                  void* stream) {
+    if (!q1 || !k1 || !q2 || !k2 || !v || !out1 || !lse1 || !out2 || !lse2 || !dout || !dq1 ||
+        !dk1 || !dq2 || !dk2 || !dv || !workspace)
+        return SWA_ERR_NULL;
+    int rc = check_common(B, Hq, Hkv, N, d, scale);
+    if (rc) return rc;
+    if (W < 1) return SWA_ERR_SHAPE;
+    if (W > N) W = N;
+    if (!lambda_heads && !std::isfinite(lambda)) return SWA_ERR_VALUE;
+    if ((long long)B * Hq > 65535 || (long long)B * Hq * N > (1ll << 38)) return SWA_ERR_SHAPE;
+    const void* al16[] = {q1, k1, q2, k2, v, out1, out2, dout, dq1, dk1, dq2, dk2, dv, workspace};
+    for (const void* ptr : al16)
+        if (!aligned16(ptr)) return SWA_ERR_ALIGN;
+    for (const void* ptr : {static_cast<const void*>(lse1), static_cast<const void*>(lse2),
+                            static_cast<const void*>(lambda_heads), static_cast<const void*>(dlambda)})
+        if (ptr && (reinterpret_cast<uintptr_t>(ptr) & 3u) != 0) return SWA_ERR_ALIGN;
+    if (workspace_bytes < diff_attn_bwd_workspace_bytes(B, Hq, Hkv, N, d)) return SWA_ERR_TOO_LARGE;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceState* st = nullptr;
+    if ((rc = current_device_state(&st))) return rc;
+    // workspace: delta of map 1, delta of map 2, dV of map 1 (fp32)
+    const size_t db = bwd_workspace_bytes(B, Hq, N);
+    float* delta1 = static_cast<float*>(workspace);
+    float* delta2 = reinterpret_cast<float*>(static_cast<char*>(workspace) + db);
+    float* dv32 = reinterpret_cast<float*>(static_cast<char*>(workspace) + 2 * db);
+    swa::BwdParams p1;
+    std::memset(&p1, 0, sizeof(p1));
+    swa::BwdParams p2;
+    std::memset(&p2, 0, sizeof(p2));
+    if ((rc = make_map(&p1.tm_q, q1, d, N, d, (long long)B * Hq, (long long)N * d))) return rc;
+    if ((rc = make_map(&p1.tm_k, k1, d, N, d, (long long)B * Hkv, (long long)N * d))) return rc;
+    if ((rc = make_map(&p1.tm_v, v, d, N, d, (long long)B * Hkv, (long long)N * d))) return rc;
+    if ((rc = make_map(&p1.tm_do, dout, d, N, d, (long long)B * Hq, (long long)N * d))) return rc;
+    if ((rc = make_map(&p2.tm_q, q2, d, N, d, (long long)B * Hq, (long long)N * d))) return rc;
+    if ((rc = make_map(&p2.tm_k, k2, d, N, d, (long long)B * Hkv, (long long)N * d))) return rc;
+    p2.tm_v = p1.tm_v;
+    p2.tm_do = p1.tm_do;
+    for (swa::BwdParams* bp : {&p1, &p2}) {
+        bp->status = st->status;
+        bp->wait_limit_ns = kWaitLimitNs;
+        bp->B = B;
+        bp->Hq = Hq;
+        bp->Hkv = Hkv;
+        bp->N = N;
+        bp->W = W;
+        bp->stride = 1;
+        bp->cap = 0;
+        bp->cchunks = 1;
+        bp->scale = scale;
+        bp->scale_log2 = scale * 1.4426950408889634f;
+        bp->dv = static_cast<__nv_bfloat16*>(dv);
+    }
+    p1.lse = lse1;
+    p1.delta = delta1;
+    p1.dq = static_cast<__nv_bfloat16*>(dq1);
+    p1.dk = static_cast<__nv_bfloat16*>(dk1);
+    p1.dv32_out = dv32;
+    p2.lse = lse2;
+    p2.delta = delta2;
+    p2.dq = static_cast<__nv_bfloat16*>(dq2);
+    p2.dk = static_cast<__nv_bfloat16*>(dk2);
+    p2.dv32_in = dv32;
+    p2.mu_mode = 1;
+    p2.lam = lambda_heads ? 0.f : lambda;
+    p2.lam_heads = lambda_heads;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const long long rows = (long long)B * Hq * N;
+    const unsigned dgrid = (unsigned)((rows + 255) / 256);
+    const int n_tiles = (N + BM - 1) / BM;
+    auto run = [&](auto dtag) -> int {
+        constexpr int D = decltype(dtag)::value;
+        swa::bwd_delta_kernel<D><<<dgrid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(out1),
+                                                         static_cast<const __nv_bfloat16*>(dout),
+                                                         delta1, rows);
+        swa::bwd_delta_kernel<D><<<dgrid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(out2),
+                                                         static_cast<const __nv_bfloat16*>(dout),
+                                                         delta2, rows);
+        if (cudaPeekAtLastError() != cudaSuccess) return SWA_ERR_CUDA;
+        int r;
+        if ((r = launch_bwd<D, 0>(p1, n_tiles, B * Hkv, s, *st))) return r;  // dk1, dV1 (fp32)
+        if ((r = launch_bwd<D, 0>(p2, n_tiles, B * Hkv, s, *st))) return r;  // dk2, dv
+        if ((r = launch_bwd<D, 1>(p1, n_tiles, B * Hq, s, *st))) return r;   // dq1
+        if ((r = launch_bwd<D, 1>(p2, n_tiles, B * Hq, s, *st))) return r;   // dq2
+        if (dlambda) {
+            swa::bwd_dlam_kernel<<<(unsigned)Hq, 256, 0, s>>>(delta2, dlambda, B, Hq, N);
+            if (cudaPeekAtLastError() != cudaSuccess) return SWA_ERR_CUDA;
+        }
+        return SWA_OK;
+    };
+    if (d == 128) return run(std::integral_constant<int, 128>{});
+    return run(std::integral_constant<int, 64>{});
+}
 
 int swa_attn_bwd(const void* q, const void* k, const void* v, const void* out, const float* lse,
                  const void* dout, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int N,

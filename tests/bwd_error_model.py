@@ -118,7 +118,9 @@ def bwd_bounds(q, k, v, dout, W: int, scale: float, rows=None, block: int = 256,
     q, dout: [B, Hq, N, d]; k, v: [B, Hkv, N, d] (fp64 or bf16 bit patterns).
     rows: the query rows whose terms are taken (default all); dq is zero on the other rows and
     dk, dv hold the sums over these rows (as the oracle's row-subset form).
-    Returns {"dq": (ref, bound), "dk": (ref, bound), "dv": (ref, bound)}."""
+    Returns {"dq": (ref, bound), "dk": (ref, bound), "dv": (ref, bound),
+    "delta": (delta_i, e_i)}, the last the rows' delta = dout_i . out_i and the bound e_i on
+    the error of the delta the kernels form ([B, Hq, N]; zero on rows not taken)."""
     q, k, v, g = _widen(q), _widen(k), _widen(v), _widen(dout)
     B, Hq, N, d = q.shape
     Hkv = k.shape[1]
@@ -129,6 +131,7 @@ def bwd_bounds(q, k, v, dout, W: int, scale: float, rows=None, block: int = 256,
     dq, dq_s2, dq_D, dq_A = (np.zeros_like(q) for _ in range(4))
     dk, dk_s2, dk_D, dk_A = (np.zeros_like(k) for _ in range(4))
     dv, dv_s2, dv_A = (np.zeros_like(v) for _ in range(3))
+    dl_ref, dl_e = np.zeros(q.shape[:3]), np.zeros(q.shape[:3])
     for b in range(B):
         for h in range(Hq):
             hk = h // grp
@@ -146,6 +149,8 @@ def bwd_bounds(q, k, v, dout, W: int, scale: float, rows=None, block: int = 256,
                 e = (LAM * u * (np.sqrt(np.sum(gr * gr * out * out, axis=1)) +
                                 np.sqrt(np.sum(a * a * dp * dp, axis=1))) +
                      FP32_SLACK * np.sum(np.abs(gr) * np.abs(out), axis=1))
+                dl_ref[b, h, rr] = delta
+                dl_e[b, h, rr] = e
                 dq[b, h, rr] = scale * (ds @ kb)
                 dq_s2[b, h, rr] = scale ** 2 * ((ds * ds) @ (kb * kb))
                 dq_D[b, h, rr] = scale * e[:, None] * (a @ np.abs(kb))
@@ -164,7 +169,8 @@ def bwd_bounds(q, k, v, dout, W: int, scale: float, rows=None, block: int = 256,
 
     return {"dq": (dq, bound(dq, dq_s2, dq_D, dq_A)),
             "dk": (dk, bound(dk, dk_s2, dk_D, dk_A)),
-            "dv": (dv, bound(dv, dv_s2, 0.0, dv_A))}
+            "dv": (dv, bound(dv, dv_s2, 0.0, dv_A)),
+            "delta": (dl_ref, dl_e)}
 
 
 def emulate_kernel_bwd(q, k, v, dout, W: int, scale: float, plant: str = "",

@@ -228,6 +228,36 @@ def test_strided_and_global_bwd_validation(L, form):
     assert L.global_attn_fwd_lse(P, P, P, P, P + 2, 1, 2, 2, 128, 64, 16, 4, 0.125, None) == 3
 
 
+def test_diff_bwd_validation(L):
+    f = L.diff_attn_bwd
+    n = L.diff_attn_bwd_workspace_bytes(2, 4, 2, 300, 64)
+    assert n == 2 * L.swa_attn_bwd_workspace_bytes(2, 4, 300) + 2 * 2 * 300 * 64 * 4
+    assert L.diff_attn_bwd_workspace_bytes(2, 4, 2, 300, 96) == 0
+    ok = dict(q1=P, k1=P, q2=P, k2=P, v=P, lam=0.8, lh=None, o1=P, l1=P, o2=P, l2=P, g=P, dq1=P,
+              dk1=P, dq2=P, dk2=P, dv=P, dl=None, B=2, Hq=4, Hkv=2, N=300, d=64, W=100,
+              scale=0.125, ws=P, nb=n)
+
+    def call(**kw):
+        a = {**ok, **kw}
+        return f(a["q1"], a["k1"], a["q2"], a["k2"], a["v"], a["lam"], a["lh"], a["o1"], a["l1"],
+                 a["o2"], a["l2"], a["g"], a["dq1"], a["dk1"], a["dq2"], a["dk2"], a["dv"], a["dl"],
+                 a["B"], a["Hq"], a["Hkv"], a["N"], a["d"], a["W"], a["scale"], a["ws"], a["nb"],
+                 None)
+
+    assert call(o2=None) == 1
+    assert call(l1=None) == 1
+    assert call(dk2=None) == 1
+    assert call(W=0) == 2
+    assert call(Hq=4, Hkv=3) == 2
+    assert call(d=96) == 4
+    assert call(lam=float("nan")) == 7
+    assert call(scale=-1.0) == 7
+    assert call(dq2=P + 8) == 3
+    assert call(dl=P + 2) == 3
+    assert call(lh=P + 1) == 3
+    assert call(nb=n - 1) == 8
+
+
 def test_header_compiles_and_library_links_from_c(tmp_path):
     """The header is valid C and the library links and answers from a C program."""
     import shutil
