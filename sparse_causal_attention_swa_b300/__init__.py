@@ -18,8 +18,10 @@ Low-level calls (pointers or tensors, explicit sizes, asynchronous on ``stream``
 Convenience wrappers on [B, H, N, d] bf16 tensors (allocate ``out``; CPU inputs are
 copied to the current CUDA device and the result copied back):
     swa_attention, strided_attention, diff_attention, swa_decode
-For training, swa_attention_trainable (CUDA tensors) records the forward for autograd and
-runs swa_attn_bwd in the backward.
+For training, swa_attention_trainable, strided_attention_trainable,
+global_attention_trainable and diff_attention_trainable (CUDA tensors) record the forward for
+autograd and run swa_attn_bwd / strided_attn_bwd / global_attn_bwd / diff_attn_bwd in the
+backward.
 """
 from __future__ import annotations
 
@@ -414,6 +416,138 @@ def swa_attention_trainable(q, k, v, window: int, scale: float | None = None):
     sc = scale if scale is not None else 1.0 / math.sqrt(q.shape[-1])
     return _swa_autograd_fn().apply(q.contiguous(), k.contiguous(), v.contiguous(), int(window),
                                     float(sc))
+
+
+_MASK_AUTOGRAD = None
+
+
+def _mask_autograd_fn():
+    """torch.autograd.Function for the local + strided and global-prefix masks: the forward is
+    strided_attn_fwd_lse / global_attn_fwd_lse, the backward strided_attn_bwd /
+    global_attn_bwd (``x`` is the stride or the number of global tokens)."""
+    global _MASK_AUTOGRAD
+    if _MASK_AUTOGRAD is None:
+        import torch
+
+        class MaskedAttention(torch.autograd.Function):
+            @staticmethod
+            def forward(ctx, q, k, v, kind, window, x, scale):
+                B, Hq, N, d = q.shape
+                out = torch.empty_like(q)
+                lse = torch.empty((B, Hq, N), dtype=torch.float32, device=q.device)
+                fwd = strided_attn_fwd_lse if kind == "strided" else global_attn_fwd_lse
+                fwd(q, k, v, out, lse, B, Hq, k.shape[1], N, d, window, x, scale)
+                ctx.save_for_backward(q, k, v, out, lse)
+                ctx.kind, ctx.window, ctx.x, ctx.scale = kind, window, x, scale
+                return out
+
+            @staticmethod
+            def backward(ctx, dout):
+                q, k, v, out, lse = ctx.saved_tensors
+                B, Hq, N, d = q.shape
+                Hkv = k.shape[1]
+                g = dout.to(torch.bfloat16).contiguous()
+                dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+                if ctx.kind == "strided":
+                    wsf, bwd = strided_attn_bwd_workspace_bytes, strided_attn_bwd
+                else:
+                    wsf, bwd = global_attn_bwd_workspace_bytes, global_attn_bwd
+                nb = wsf(B, Hq, Hkv, N, d, ctx.window, ctx.x)
+                ws = torch.empty(nb, dtype=torch.uint8, device=q.device)
+                bwd(q, k, v, out, lse, g, dq, dk, dv, B, Hq, Hkv, N, d, ctx.window, ctx.x,
+                    ctx.scale, ws, nb)
+                return dq, dk, dv, None, None, None, None
+
+        _MASK_AUTOGRAD = MaskedAttention
+    return _MASK_AUTOGRAD
+
+
+_DIFF_AUTOGRAD = None
+
+
+def _diff_autograd_fn():
+    """torch.autograd.Function for differential attention with one lambda per head: the forward
+    is diff_swa_attn_fwd (per-head lambda) for the output, plus swa_attn_fwd_lse on both maps
+    for the outputs and log-sum-exps the backward needs; the backward is diff_attn_bwd, which
+    also returns the gradient of every head's lambda."""
+    global _DIFF_AUTOGRAD
+    if _DIFF_AUTOGRAD is None:
+        import torch
+
+        class DiffAttention(torch.autograd.Function):
+            @staticmethod
+            def forward(ctx, q1, k1, q2, k2, v, lam, window, scale):
+                B, Hq, N, d = q1.shape
+                Hkv = k1.shape[1]
+                outs = []
+                for qq, kk in ((q1, k1), (q2, k2)):
+                    o = torch.empty_like(qq)
+                    lse = torch.empty((B, Hq, N), dtype=torch.float32, device=qq.device)
+                    swa_attn_fwd_lse(qq, kk, v, o, lse, B, Hq, Hkv, N, d, window, scale)
+                    outs += [o, lse]
+                lam32 = lam.detach().to(torch.float32).contiguous()
+                out = torch.empty_like(q1)
+                diff_swa_attn_fwd(q1, k1, q2, k2, v, 0.0, lam32, out, B, Hq, Hkv, N, d, window,
+                                  scale)
+                ctx.save_for_backward(q1, k1, q2, k2, v, lam32, *outs)
+                ctx.window, ctx.scale = window, scale
+                return out
+
+            @staticmethod
+            def backward(ctx, dout):
+                q1, k1, q2, k2, v, lam32, o1, l1, o2, l2 = ctx.saved_tensors
+                B, Hq, N, d = q1.shape
+                Hkv = k1.shape[1]
+                g = dout.to(torch.bfloat16).contiguous()
+                grads = [torch.empty_like(x) for x in (q1, k1, q2, k2, v)]
+                dlam = torch.empty(Hq, dtype=torch.float32, device=q1.device)
+                nb = diff_attn_bwd_workspace_bytes(B, Hq, Hkv, N, d)
+                ws = torch.empty(nb, dtype=torch.uint8, device=q1.device)
+                diff_attn_bwd(q1, k1, q2, k2, v, 0.0, lam32, o1, l1, o2, l2, g, *grads, dlam, B,
+                              Hq, Hkv, N, d, ctx.window, ctx.scale, ws, nb)
+                return (*grads, dlam, None, None)
+
+        _DIFF_AUTOGRAD = DiffAttention
+    return _DIFF_AUTOGRAD
+
+
+def _want_cuda_bf16(*ts):
+    import torch
+
+    for t in ts:
+        if t.dtype != torch.bfloat16 or t.dim() != 4 or not t.is_cuda:
+            raise ValueError("expected bf16 CUDA tensors of shape [B, H, N, d]")
+
+
+def strided_attention_trainable(q, k, v, window: int, stride: int, scale: float | None = None):
+    """Local + strided attention that records itself for autograd (forward
+    strided_attn_fwd_lse, backward strided_attn_bwd)."""
+    _want_cuda_bf16(q, k, v)
+    sc = scale if scale is not None else 1.0 / math.sqrt(q.shape[-1])
+    return _mask_autograd_fn().apply(q.contiguous(), k.contiguous(), v.contiguous(), "strided",
+                                     int(window), int(stride), float(sc))
+
+
+def global_attention_trainable(q, k, v, window: int, n_global: int, scale: float | None = None):
+    """Window plus a global prefix that records itself for autograd (forward
+    global_attn_fwd_lse, backward global_attn_bwd)."""
+    _want_cuda_bf16(q, k, v)
+    sc = scale if scale is not None else 1.0 / math.sqrt(q.shape[-1])
+    return _mask_autograd_fn().apply(q.contiguous(), k.contiguous(), v.contiguous(), "global",
+                                     int(window), int(n_global), float(sc))
+
+
+def diff_attention_trainable(q1, k1, q2, k2, v, lam, window: int | None = None,
+                             scale: float | None = None):
+    """Differential attention with a learnable lambda per head (``lam``: a float tensor [Hq] on
+    the device, e.g. an nn.Parameter) that records itself for autograd; gradients reach q1, k1,
+    q2, k2, v and lam.  window None is the causal form."""
+    _want_cuda_bf16(q1, k1, q2, k2, v)
+    N = q1.shape[2]
+    sc = scale if scale is not None else 1.0 / math.sqrt(q1.shape[-1])
+    return _diff_autograd_fn().apply(q1.contiguous(), k1.contiguous(), q2.contiguous(),
+                                     k2.contiguous(), v.contiguous(), lam,
+                                     N if window is None else int(window), float(sc))
 
 
 def swa_decode(q, k_cache, v_cache, pos, scale: float | None = None, out=None, workspace=None):

@@ -144,3 +144,37 @@ def test_diff_swa_full_size_sampled():
                 worst[name] = max(worst.get(name, 0.0),
                                   check_bound_one(a, r, bnd, f"diff_swa head {h} [{p0},{p1}) {name}"))
     print(f"diff_swa backward sampled: worst |gpu - oracle| / bound = {worst}")
+
+
+def test_trainable_wrappers_match_the_calls():
+    """diff_attention_trainable (a learnable lambda per head) and strided_attention_trainable
+    give, through torch autograd, the gradients of the direct C-ABI calls, bit for bit."""
+    rng = np.random.default_rng(31)
+    B, Hq, Hkv, N, d, W = 1, 4, 2, 300, 64, 100
+    arrs = [_rand(rng, (B, h, N, d)) for h in (Hq, Hkv, Hq, Hkv, Hkv, Hq)]
+    lams = np.array([0.8, 0.3, -0.2, 0.5], dtype=np.float32)
+    sc = 1.0 / np.sqrt(d)
+    t = [to_dev(a).requires_grad_() for a in arrs[:5]]
+    lam = torch.tensor(lams, device="cuda", requires_grad=True)
+    out = pkg.diff_attention_trainable(*t, lam, window=W)
+    out.backward(to_dev(arrs[5]))
+    want = _diff_bwd_gpu(*arrs, lams, True, W, sc)
+    for x, y in zip([a.grad for a in t] + [lam.grad], want):
+        assert np.array_equal(x.detach().float().cpu().numpy().astype(np.float64), y)
+    # local + strided through its wrapper against strided_attn_bwd
+    q, k, v = (to_dev(a).requires_grad_() for a in (arrs[0], arrs[1], arrs[4]))
+    o = pkg.strided_attention_trainable(q, k, v, 64, 16)
+    o.backward(to_dev(arrs[5]))
+    B_, Hq_, N_, d_ = q.shape
+    tq, tk, tv, tg = (to_dev(a) for a in (arrs[0], arrs[1], arrs[4], arrs[5]))
+    of = torch.empty_like(tq)
+    lse = torch.empty((B_, Hq_, N_), dtype=torch.float32, device="cuda")
+    pkg.strided_attn_fwd_lse(tq, tk, tv, of, lse, B_, Hq_, Hkv, N_, d_, 64, 16, sc)
+    nb = pkg.strided_attn_bwd_workspace_bytes(B_, Hq_, Hkv, N_, d_, 64, 16)
+    ws = torch.empty(nb, dtype=torch.uint8, device="cuda")
+    dq, dk, dv = torch.empty_like(tq), torch.empty_like(tk), torch.empty_like(tv)
+    pkg.strided_attn_bwd(tq, tk, tv, of, lse, tg, dq, dk, dv, B_, Hq_, Hkv, N_, d_, 64, 16, sc,
+                         ws, nb)
+    torch.cuda.synchronize()
+    for x, y in ((q.grad, dq), (k.grad, dk), (v.grad, dv)):
+        assert torch.equal(x, y)
