@@ -21,8 +21,10 @@ the host cores over bounded row samples of the same workload.
 Other workloads (``--workload``, or ``--all`` for one line each): the Gemma-3-shaped layers
 and ``gemma_group`` (one step = the 5:1 group: five W=1024 layers and one full-causal layer),
 local + strided, window plus a global prefix, the differential forms, decode against a
-rolling cache, and ``mistral_swa_bwd``, where one step is one backward call (dq, dk, dv) of
-the Mistral-shaped layer with the forward's output and log-sum-exp computed once beforehand.
+rolling cache, and the backward calls: ``mistral_swa_bwd`` (one step = one swa_attn_bwd call of
+the Mistral-shaped layer), ``strided_bwd`` (strided_attn_bwd at the strided workload's shape)
+and ``diff_swa_bwd`` (diff_attn_bwd at the windowed differential workload's shape), each with
+the forward's outputs and log-sum-exps computed once beforehand.
 """
 from __future__ import annotations
 
@@ -72,8 +74,13 @@ TRAFFIC = {
 }
 
 
+BWD_KINDS = ("bwd", "strided_bwd", "diff_bwd")
+
+
 def kernel_family(w: swa_inputs.Workload) -> str:
-    return {"decode": "decode", "bwd": "attn_bwd"}.get(w.kind, "attn_fwd")
+    if w.kind in BWD_KINDS:
+        return "attn_bwd"
+    return {"decode": "decode"}.get(w.kind, "attn_fwd")
 
 
 def kernel_hash(family: str = "attn_fwd") -> str:
@@ -266,19 +273,30 @@ def run_oracle_bwd(w, inp, n_rows: int) -> float:
     import oracle
 
     sub = bwd_prefix(w, inp, n_rows)
-    oracle.attn_bwd(sub["q"], sub["k"], sub["v"], sub["dout"], w.W, w.scale)
-    return flopcount.useful_flops("bwd", 1, w.Hq, n_rows, w.d, w.W)
+    if w.kind == "diff_bwd":
+        oracle.diff_bwd(sub["q1"], sub["k1"], sub["q2"], sub["k2"], sub["v"], w.lam, sub["dout"],
+                        w.W, w.scale)
+    elif w.kind == "strided_bwd":
+        oracle.attn_bwd(sub["q"], sub["k"], sub["v"], sub["dout"], w.W, w.scale, kind="strided",
+                        stride=w.stride)
+    else:
+        oracle.attn_bwd(sub["q"], sub["k"], sub["v"], sub["dout"], w.W, w.scale)
+    return flopcount.useful_flops(w.kind, 1, w.Hq, n_rows, w.d, w.W, w.stride)
 
 
 def bwd_sample_rows(w, inp, budget_s: float) -> int:
     """Prefix length whose oracle backward takes about budget_s seconds."""
     n = min(w.N, 1024)  # large enough that thread start-up does not dominate the probe
     t0 = time.perf_counter()
-    run_oracle_bwd(w, inp, n)
+    fl = run_oracle_bwd(w, inp, n)
     dt = max(time.perf_counter() - t0, 1e-3)
-    # cost grows with the pairs: linearly in n once n exceeds W
-    per_pair = dt / flopcount.pairs_window(n, w.W)
-    while n < w.N and flopcount.pairs_window(min(w.N, 2 * n), w.W) * per_pair < budget_s:
+    # cost grows with the useful work (the allowed pairs) of the prefix
+    per_flop = dt / fl
+
+    def work(m):
+        return flopcount.useful_flops(w.kind, 1, w.Hq, m, w.d, w.W, w.stride)
+
+    while n < w.N and work(min(w.N, 2 * n)) * per_flop < budget_s:
         n = min(w.N, 2 * n)
     return n
 
@@ -304,7 +322,7 @@ def cpu_baseline(w, inp, budget_s: float = 15.0):
 
     if w.kind == "decode":
         return cpu_baseline_decode(w, inp, budget_s)
-    if w.kind == "bwd":
+    if w.kind in BWD_KINDS:
         return cpu_baseline_bwd(w, inp, budget_s)
     oracle.build()
     inp = oracle_inputs_f64(inp)
@@ -343,7 +361,7 @@ def reference_arm(args, w, ws, rank):
     oracle.build()
     inp = oracle_inputs_f64(swa_inputs.make_inputs(w))
     fl_full, _ = workload_units(w)
-    if w.kind == "bwd":
+    if w.kind in BWD_KINDS:
         reference_arm_bwd(args, w, ws, inp, fl_full)
         return
     # size every step so warmup + steps stay within about two minutes
@@ -422,6 +440,14 @@ def workload_config(w, fl, flush=False):
         cfg["layers"] = (f"{w.stride} causal SWA layers with W={w.W} and one full-causal layer "
                          f"(W=N), each a swa_attn_fwd call on the same inputs")
         cfg["flop_convention"] = "4 d per allowed (row, key) pair, summed over the group's layers"
+    if w.kind == "strided_bwd":
+        cfg["stride"] = w.stride
+        cfg["flop_convention"] = ("10 d per allowed (row, key) pair: the products S, dP, dV, dK, "
+                                  "dQ (2.5 x the forward)")
+    if w.kind == "diff_bwd":
+        cfg["lambda"] = w.lam
+        cfg["flop_convention"] = ("20 d per (row, key) pair in the window: the five products of "
+                                  "each of the two maps")
     if w.kind == "bwd":
         cfg["flop_convention"] = ("10 d per (row, key) pair in the window: the products S, dP, "
                                   "dV, dK, dQ (2.5 x the forward)")
@@ -475,6 +501,15 @@ def launch(pkg, w, t, out, stream):
         pkg.swa_attn_bwd(t["q"], t["k"], t["v"], t["out_fwd"], t["lse"], t["dout"], out, t["dk"],
                          t["dv"], w.B, w.Hq, w.Hkv, w.N, w.d, w.W, w.scale, t["ws"],
                          t["ws"].numel(), stream)
+    elif w.kind == "strided_bwd":  # out receives dq
+        pkg.strided_attn_bwd(t["q"], t["k"], t["v"], t["out_fwd"], t["lse"], t["dout"], out,
+                             t["dk"], t["dv"], w.B, w.Hq, w.Hkv, w.N, w.d, w.W, w.stride, w.scale,
+                             t["ws"], t["ws"].numel(), stream)
+    elif w.kind == "diff_bwd":  # out receives dq1
+        pkg.diff_attn_bwd(t["q1"], t["k1"], t["q2"], t["k2"], t["v"], w.lam, None, t["out1"],
+                          t["lse1"], t["out2"], t["lse2"], t["dout"], out, t["dk1"], t["dq2"],
+                          t["dk2"], t["dv"], t["dlam"], w.B, w.Hq, w.Hkv, w.N, w.d, w.W, w.scale,
+                          t["ws"], t["ws"].numel(), stream)
     elif w.W < w.N:
         pkg.diff_swa_attn_fwd(t["q1"], t["k1"], t["q2"], t["k2"], t["v"], w.lam, None, out, w.B,
                               w.Hq, w.Hkv, w.N, w.d, w.W, w.scale, stream)
@@ -484,19 +519,42 @@ def launch(pkg, w, t, out, stream):
 
 
 def bwd_buffers(pkg, w, t, stream):
-    """Device buffers of a backward step besides q, k, v, dout: the forward's output and row
-    log-sum-exp (computed here, once, by the forward call), the delta workspace and dk, dv."""
+    """Device buffers of a backward step besides its inputs: the forward's outputs and row
+    log-sum-exps (computed here, once, by the forward calls), the workspace and the gradients
+    other than the first (which the step's `out` receives).  Returns the names of the tensors
+    a step writes, besides `out`."""
     import torch
 
+    if w.kind == "diff_bwd":
+        q1 = t["q1"]
+        for m, (qq, kk) in enumerate(((q1, t["k1"]), (t["q2"], t["k2"])), start=1):
+            t[f"out{m}"] = torch.empty_like(qq)
+            t[f"lse{m}"] = torch.empty((w.B, w.Hq, w.N), dtype=torch.float32, device=q1.device)
+            pkg.swa_attn_fwd_lse(qq, kk, t["v"], t[f"out{m}"], t[f"lse{m}"], w.B, w.Hq, w.Hkv, w.N,
+                                 w.d, w.W, w.scale, stream)
+        nb = pkg.diff_attn_bwd_workspace_bytes(w.B, w.Hq, w.Hkv, w.N, w.d)
+        t["ws"] = torch.empty(nb, dtype=torch.uint8, device=q1.device)
+        t["dq2"] = torch.empty_like(q1)
+        t["dk1"] = torch.empty_like(t["k1"])
+        t["dk2"] = torch.empty_like(t["k2"])
+        t["dv"] = torch.empty_like(t["v"])
+        t["dlam"] = torch.empty(w.Hq, dtype=torch.float32, device=q1.device)
+        return ["dk1", "dq2", "dk2", "dv", "dlam"]
     q = t["q"]
     t["out_fwd"] = torch.empty_like(q)
     t["lse"] = torch.empty((w.B, w.Hq, w.N), dtype=torch.float32, device=q.device)
-    pkg.swa_attn_fwd_lse(q, t["k"], t["v"], t["out_fwd"], t["lse"], w.B, w.Hq, w.Hkv, w.N, w.d,
-                         w.W, w.scale, stream)
-    nb = pkg.swa_attn_bwd_workspace_bytes(w.B, w.Hq, w.N)
+    if w.kind == "strided_bwd":
+        pkg.strided_attn_fwd_lse(q, t["k"], t["v"], t["out_fwd"], t["lse"], w.B, w.Hq, w.Hkv,
+                                 w.N, w.d, w.W, w.stride, w.scale, stream)
+        nb = pkg.strided_attn_bwd_workspace_bytes(w.B, w.Hq, w.Hkv, w.N, w.d, w.W, w.stride)
+    else:
+        pkg.swa_attn_fwd_lse(q, t["k"], t["v"], t["out_fwd"], t["lse"], w.B, w.Hq, w.Hkv, w.N,
+                             w.d, w.W, w.scale, stream)
+        nb = pkg.swa_attn_bwd_workspace_bytes(w.B, w.Hq, w.N)
     t["ws"] = torch.empty(nb, dtype=torch.uint8, device=q.device)
     t["dk"] = torch.empty_like(t["k"])
     t["dv"] = torch.empty_like(t["v"])
+    return ["dk", "dv"]
 
 
 def bench_workload(args, w, ws, rank, dev, want_cpu, want_e2e):
@@ -507,11 +565,11 @@ def bench_workload(args, w, ws, rank, dev, want_cpu, want_e2e):
     pkg.load()
     inp = swa_inputs.make_inputs(w)
     t = to_device(inp, dev)
-    first = t["q1"] if w.kind == "diff" else t["q"]
+    first = t["q1"] if w.kind in ("diff", "diff_bwd") else t["q"]
     out = torch.empty_like(first)
     stream = torch.cuda.current_stream(dev)
     sh = stream.cuda_stream
-    if w.kind == "bwd":
+    if w.kind in BWD_KINDS:
         bwd_buffers(pkg, w, t, sh)
     fl, algo_bytes = workload_units(w)
 
@@ -577,6 +635,12 @@ def bench_workload(args, w, ws, rank, dev, want_cpu, want_e2e):
     if w.kind == "bwd":
         kname = (f"bwd_delta_kernel<{w.d}> + attn_bwd_kernel<{w.d},0> (dk, dv) + "
                  f"attn_bwd_kernel<{w.d},1> (dq), one call")
+    elif w.kind == "strided_bwd":
+        kname = (f"bwd_delta_kernel<{w.d}> + attn_bwd_kernel<{w.d},2> (dk, dv of the strided "
+                 f"keys) + attn_bwd_kernel<{w.d},0> + attn_bwd_kernel<{w.d},1>, one call")
+    elif w.kind == "diff_bwd":
+        kname = (f"2 x bwd_delta_kernel<{w.d}> + 2 x attn_bwd_kernel<{w.d},0> + 2 x "
+                 f"attn_bwd_kernel<{w.d},1> + bwd_dlam_kernel, one call")
     elif w.kind == "decode":
         kname = "decode_split_kernel + decode_combine_kernel"
     elif w.kind == "group":
@@ -606,7 +670,8 @@ def bench_workload(args, w, ws, rank, dev, want_cpu, want_e2e):
         "data": "synthetic", "config": workload_config(w, fl, flush),
         "pct_of_bf16_peak": 100.0 * achieved_tf / bf16_peak,
         "roofline": roofline,
-        "gpu_launches": args.steps * {"decode": 2, "bwd": 3, "group": w.stride + 1}.get(w.kind, 1),
+        "gpu_launches": args.steps * {"decode": 2, "bwd": 3, "strided_bwd": 4, "diff_bwd": 7,
+                                      "group": w.stride + 1}.get(w.kind, 1),
         "clocks": clk,
     }
     if ws > 1:
@@ -627,21 +692,22 @@ def e2e_measure(args, w, inp, pkg, dev, ws):
     host = {n: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).pin_memory()
             for n, a in inp.items()}
     dev_t = {n: torch.empty_like(h, device=dev) for n, h in host.items()}
-    first = dev_t["q1"] if w.kind == "diff" else dev_t["q"]
+    first = dev_t["q1"] if w.kind in ("diff", "diff_bwd") else dev_t["q"]
     out = torch.empty_like(first)
     stream = torch.cuda.current_stream(dev)
     sh = stream.cuda_stream
     results = [out]
-    if w.kind == "bwd":
-        # the forward's output and log-sum-exp are inputs of the backward: made once on the
-        # device, then copied from pinned host buffers every step like q, k, v and dout
+    if w.kind in BWD_KINDS:
+        # the forward's outputs and log-sum-exps are inputs of the backward: made once on the
+        # device, then copied from pinned host buffers every step like the inputs and dout
         for n in host:
             dev_t[n].copy_(host[n])
-        bwd_buffers(pkg, w, dev_t, sh)
+        written = bwd_buffers(pkg, w, dev_t, sh)
         torch.cuda.synchronize(dev)
-        for n in ("out_fwd", "lse"):
+        fwd_names = ("out1", "lse1", "out2", "lse2") if w.kind == "diff_bwd" else ("out_fwd", "lse")
+        for n in fwd_names:
             host[n] = dev_t[n].cpu().pin_memory()
-        results = [out, dev_t["dk"], dev_t["dv"]]
+        results = [out] + [dev_t[n] for n in written]
     res_host = [torch.empty(r.shape, dtype=r.dtype).pin_memory() for r in results]
     h2d = sum(h.numel() * h.element_size() for h in host.values())
     d2h = sum(r.numel() * r.element_size() for r in results)

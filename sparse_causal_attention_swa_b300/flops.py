@@ -60,6 +60,10 @@ def useful_flops(kind: str, B: int, Hq: int, N: int, d: int, W: int, stride: int
     if kind == "bwd":  # S, dP, dV, dK, dQ: five products of 2 d per pair (2.5 x forward)
         p = pairs_window(N, W)
         return 10.0 * d * p * B * Hq
+    if kind == "strided_bwd":  # the same five products per pair of the local + strided mask
+        return 10.0 * d * pairs_strided(N, W, stride) * B * Hq
+    if kind == "diff_bwd":  # five products per pair for each of the two maps
+        return 20.0 * d * pairs_window(N, W) * B * Hq
     if kind == "diff":  # both maps under the window W (W >= N: causal)
         p = pairs_window(N, W)
         return 8.0 * d * p * B * Hq
@@ -95,6 +99,8 @@ def algorithmic_bytes(kind: str, B: int, Hq: int, Hkv: int, N: int, d: int,
         return layers * (q + 2 * kv + q)
     if kind == "diff":
         return 2 * q + 3 * kv + q  # q1, q2, k1, k2, v, out
-    if kind == "bwd":  # q, out, dout, lse (fp32), k, v read; dq, dk, dv written
+    if kind in ("bwd", "strided_bwd"):  # q, out, dout, lse (fp32), k, v read; dq, dk, dv written
         return 4 * q + 4 * kv + B * Hq * N * 4
+    if kind == "diff_bwd":  # q1, q2, out1, out2, dout, lse1, lse2, k1, k2, v; dq1, dq2, dk1, dk2, dv
+        return 7 * q + 6 * kv + 2 * B * Hq * N * 4
     return q + 2 * kv + q  # q, k, v, out

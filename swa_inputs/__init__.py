@@ -25,7 +25,8 @@ class Workload:
     """One synthetic workload: the sizes of one call of the hot path."""
 
     name: str
-    kind: str  # "swa" | "strided" | "diff" | "decode" | "global" | "group" | "bwd"
+    kind: str  # "swa" | "strided" | "diff" | "decode" | "global" | "group" | "bwd" |
+    #            "strided_bwd" | "diff_bwd"
     # (for "strided" the stride field is the stride; for "global" it is the number of global
     # prefix tokens; for "group" it is the number of W-window layers per full-causal layer)
     B: int
@@ -74,6 +75,12 @@ WORKLOADS = {
     # backward pass of the Mistral-shaped SWA layer: q, k, v as the forward, plus dL/dout
     "mistral_swa_bwd": Workload("mistral_swa_bwd", "bwd", 1, 32, 8, 16384, 128, 4096,
                                 seed_index=9),
+    # backward of local + strided attention at the strided workload's shape, plus dL/dout
+    "strided_bwd": Workload("strided_bwd", "strided_bwd", 1, 16, 16, 16384, 64, 256, stride=128,
+                            seed_index=10),
+    # backward of the windowed differential workload (both maps, lambda 0.8), plus dL/dout
+    "diff_swa_bwd": Workload("diff_swa_bwd", "diff_bwd", 1, 16, 16, 16384, 64, 1024, lam=0.8,
+                             sink_shift=3.0, seed_index=11),
     # window plus a global prefix (Longformer-style [CLS] / question tokens): W=512, 64 global
     "global": Workload("global", "global", 1, 16, 16, 16384, 64, 512, stride=64, seed_index=7),
     # decode against a W-slot rolling KV cache, Mistral-7B heads: one new query per
@@ -114,6 +121,10 @@ def _normal_bf16(rng: np.random.Generator, shape, shift_row0: float = 0.0) -> np
 def tensor_names(kind: str) -> tuple[str, ...]:
     if kind == "decode":
         return ("q", "kc", "vc")
+    if kind == "diff_bwd":
+        return ("q1", "k1", "q2", "k2", "v", "dout")
+    if kind in ("bwd", "strided_bwd"):
+        return ("q", "k", "v", "dout")
     return ("q1", "k1", "q2", "k2", "v") if kind == "diff" else ("q", "k", "v")
 
 
@@ -131,15 +142,18 @@ def make_inputs(w: Workload, seed: int | None = None) -> dict[str, np.ndarray]:
         }
     qs = (w.B, w.Hq, w.N, w.d)
     ks = (w.B, w.Hkv, w.N, w.d)
-    if w.kind == "diff":
-        return {
+    if w.kind in ("diff", "diff_bwd"):
+        d = {
             "q1": _normal_bf16(rng, qs),
             "k1": _normal_bf16(rng, ks, w.sink_shift),
             "q2": _normal_bf16(rng, qs),
             "k2": _normal_bf16(rng, ks),
             "v": _normal_bf16(rng, ks),
         }
-    if w.kind == "bwd":  # the forward's inputs, then the upstream gradient dL/dout
+        if w.kind == "diff_bwd":  # then the upstream gradient dL/dout
+            d["dout"] = _normal_bf16(rng, qs)
+        return d
+    if w.kind in ("bwd", "strided_bwd"):  # the forward's inputs, then dL/dout
         return {
             "q": _normal_bf16(rng, qs),
             "k": _normal_bf16(rng, ks),

@@ -70,3 +70,26 @@ def test_small_workload_cpu_baseline_has_one_core_time():
     cb = bench.cpu_baseline(w, swa_inputs.make_inputs(w), budget_s=0.5)
     assert cb["value"] > 0 and cb["one_core"]["value"] > 0
     assert oracle.max_threads() == nt  # the thread count is restored
+
+
+def test_strided_and_diff_bwd_units_inputs_and_oracle_legs():
+    ws = swa_inputs.WORKLOADS["strided_bwd"]
+    fl, by = bench.workload_units(ws)
+    assert fl == 2.5 * flops.useful_flops("strided", ws.B, ws.Hq, ws.N, ws.d, ws.W, ws.stride)
+    wd = swa_inputs.WORKLOADS["diff_swa_bwd"]
+    fl, by = bench.workload_units(wd)
+    assert fl == 2.5 * flops.useful_flops("diff", wd.B, wd.Hq, wd.N, wd.d, wd.W)
+    q = wd.B * wd.Hq * wd.N * wd.d * 2
+    assert by == 7 * q + 6 * q + 2 * wd.B * wd.Hq * wd.N * 4  # Hq == Hkv here
+    assert bench.kernel_family(ws) == bench.kernel_family(wd) == "attn_bwd"
+    for w in (ws.replace(N=300, Hq=2, Hkv=2), wd.replace(N=300, Hq=2, Hkv=2)):
+        inp = swa_inputs.make_inputs(w)
+        assert "dout" in inp and inp["dout"].shape == (1, 2, 300, 64)
+        cb = bench.cpu_baseline(w, inp, budget_s=0.3)
+        assert cb["kind"] == "oracle" and cb["value"] > 0
+        args = argparse.Namespace(steps=2, warmup=3)
+        buf = io.StringIO()
+        with redirect_stdout(buf):
+            bench.reference_arm(args, w, 1, 0)
+        line = json.loads(buf.getvalue().strip().splitlines()[-1])
+        assert line["impl"] == "reference" and line["value"] > 0 and line["config"]["kind"] == w.kind
