@@ -322,6 +322,12 @@ int swa_cache_gather(const void* k_cache, const void* v_cache, void* k_ctx, void
 const char* swa_status_string(int status);
 
 /*
+ * The cause of the calling thread's last SWA_ERR_CUDA: the CUDA call that failed and its
+ * error name (thread-local storage, valid until the thread's next failing call; "" if none).
+ */
+const char* swa_last_error_detail(void);
+
+/*
  * Synchronise `stream`, then read and clear the library's device status word on the
  * current device.  Returns SWA_OK, SWA_ERR_TIMEOUT if a kernel's bounded wait ran out
  * since the last call (that kernel wrote no output rows it could not finish), or

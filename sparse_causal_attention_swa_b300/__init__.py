@@ -39,7 +39,11 @@ _lib = None
 class SwaError(RuntimeError):
     def __init__(self, code: int, where: str):
         self.code = code
-        super().__init__(f"{where}: {swa_status_string(code)} (status {code})")
+        detail = ""
+        if code == 5:  # SWA_ERR_CUDA: which CUDA call failed, and how
+            detail = load().swa_last_error_detail().decode()
+        super().__init__(f"{where}: {swa_status_string(code)} (status {code})"
+                         + (f" [{detail}]" if detail else ""))
 
 
 def load():
@@ -105,6 +109,8 @@ def load():
         lib.swa_cache_gather.restype = I
         lib.swa_status_string.argtypes = [I]
         lib.swa_status_string.restype = ctypes.c_char_p
+        lib.swa_last_error_detail.argtypes = []
+        lib.swa_last_error_detail.restype = ctypes.c_char_p
         lib.swa_device_status.argtypes = [P]
         lib.swa_device_status.restype = I
         lib.swa_watchdog_selftest.argtypes = [I, P]

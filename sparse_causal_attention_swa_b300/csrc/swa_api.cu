@@ -6,6 +6,7 @@
 #include <cudaTypedefs.h>
 
 #include <cmath>
+#include <cstdio>
 #include <cstdint>
 #include <cstring>
 #include <map>
@@ -46,12 +47,27 @@ struct DeviceState {
 
 std::mutex g_mutex;
 DeviceState g_dev[kMaxDevices];
+
+// The cause of the calling thread's last SWA_ERR_CUDA (read by swa_last_error_detail).
+thread_local char t_err_detail[160] = "";
+
+int cuda_fail(const char* what, const char* err) {
+    std::snprintf(t_err_detail, sizeof(t_err_detail), "%s: %s", what, err ? err : "?");
+    return SWA_ERR_CUDA;
+}
+int cuda_fail(const char* what, cudaError_t e) { return cuda_fail(what, cudaGetErrorName(e)); }
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 int current_device_state(DeviceState** out) {
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return SWA_ERR_CUDA;
+    cudaError_t e0 = cudaGetDevice(&dev);
+    if (e0 != cudaSuccess) return cuda_fail("cudaGetDevice", e0);
     if (dev < 0 || dev >= kMaxDevices) return SWA_ERR_UNSUPPORTED;
+    // make the device's primary context current on this thread: the tensor-map encoder is a
+    // driver call, and a thread that has made no runtime call yet (an autograd worker, say)
+    // has no current context
+    e0 = cudaSetDevice(dev);
+    if (e0 != cudaSuccess) return cuda_fail("cudaSetDevice", e0);
     DeviceState& st = g_dev[dev];
     if (!st.probed) {
         int major = 0, minor = 0;
@@ -121,13 +137,30 @@ int make_map(CUtensorMap* m, const void* base, int d, long long rows, long long 
                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) return SWA_ERR_CUDA;
+    if (r != CUDA_SUCCESS) {
+        char msg[64];
+        std::snprintf(msg, sizeof(msg), "CUresult %d", (int)r);
+        return cuda_fail("cuTensorMapEncodeTiled", msg);
+    }
     if (g_map_cache.size() >= kMapCacheMax) g_map_cache.clear();
     g_map_cache.emplace(key, *m);
     return SWA_OK;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// A plain launch whose error comes back from the launch call itself (never from the thread's
+// last-error state, which may hold an earlier error of another library on the same thread).
+template <typename... KArgs, typename... Args>
+int launch_plain(void (*kern)(KArgs...), unsigned grid, unsigned block, cudaStream_t stream,
+                 Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(block, 1, 1);
+    cfg.stream = stream;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, args...);
+    return e == cudaSuccess ? SWA_OK : cuda_fail("cudaLaunchKernelEx", e);
+}
 
 int check_common(int B, int Hq, int Hkv, int N, int d, float scale) {
     if (B < 1 || Hq < 1 || Hkv < 1 || N < 1) return SWA_ERR_SHAPE;
@@ -145,9 +178,9 @@ int launch(const KParams& kp, int n_items, cudaStream_t stream, DeviceState& st)
     auto kern = swa::attn_fwd_kernel<D, MODE>;
     bool& set = st.attr_set[D == 128 ? 1 : 0][MODE];
     if (!set) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::BYTES) !=
-            cudaSuccess)
-            return SWA_ERR_CUDA;
+        const cudaError_t ea =
+            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::BYTES);
+        if (ea != cudaSuccess) return cuda_fail("cudaFuncSetAttribute (forward)", ea);
         set = true;
     }
     // persistent grid: one CTA per SM (tensor memory and shared memory allow no more),
@@ -161,7 +194,7 @@ int launch(const KParams& kp, int n_items, cudaStream_t stream, DeviceState& st)
     cfg.dynamicSmemBytes = L::BYTES;
     cfg.stream = stream;
     cudaError_t e = cudaLaunchKernelEx(&cfg, kern, kq);
-    return e == cudaSuccess ? SWA_OK : SWA_ERR_CUDA;
+    return e == cudaSuccess ? SWA_OK : cuda_fail("cudaLaunchKernelEx (forward)", e);
 }
 
 template <int MODE>
@@ -383,9 +416,9 @@ int launch_bwd(const swa::BwdParams& bp, int n_tiles, int n_mats, cudaStream_t s
     auto kern = swa::attn_bwd_kernel<D, KIND>;
     bool& set = st.bwd_attr_set[D == 128 ? 1 : 0][KIND];
     if (!set) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::BYTES) !=
-            cudaSuccess)
-            return SWA_ERR_CUDA;
+        const cudaError_t ea =
+            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::BYTES);
+        if (ea != cudaSuccess) return cuda_fail("cudaFuncSetAttribute (backward)", ea);
         set = true;
     }
     cudaLaunchConfig_t cfg = {};
@@ -393,7 +426,8 @@ int launch_bwd(const swa::BwdParams& bp, int n_tiles, int n_mats, cudaStream_t s
     cfg.blockDim = dim3(swa::BWD_THREADS, 1, 1);
     cfg.dynamicSmemBytes = L::BYTES;
     cfg.stream = stream;
-    return cudaLaunchKernelEx(&cfg, kern, bp) == cudaSuccess ? SWA_OK : SWA_ERR_CUDA;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, bp);
+    return e == cudaSuccess ? SWA_OK : cuda_fail("cudaLaunchKernelEx (backward)", e);
 }
 
 template <int D>
@@ -401,11 +435,10 @@ int run_bwd(const swa::BwdParams& bp, const void* out, const void* dout, float* 
             cudaStream_t stream, DeviceState& st) {
     const long long rows = (long long)bp.B * bp.Hq * bp.N;
     const int n_tiles = (bp.N + swa::BM - 1) / swa::BM;
-    swa::bwd_delta_kernel<D><<<(unsigned)((rows + 255) / 256), 256, 0, stream>>>(
-        static_cast<const __nv_bfloat16*>(out), static_cast<const __nv_bfloat16*>(dout), delta,
-        rows);
-    if (cudaPeekAtLastError() != cudaSuccess) return SWA_ERR_CUDA;
-    int rc;
+    int rc = launch_plain(swa::bwd_delta_kernel<D>, (unsigned)((rows + 255) / 256), 256u, stream,
+                          static_cast<const __nv_bfloat16*>(out),
+                          static_cast<const __nv_bfloat16*>(dout), delta, rows);
+    if (rc) return rc;
     if (bp.cap > 0 && bp.ncomp > 0 &&
         (rc = launch_bwd<D, 2>(bp, (bp.ncomp_pad / swa::BN) * bp.cchunks, bp.B * bp.Hkv, stream,
                                st)))
@@ -416,6 +449,8 @@ int run_bwd(const swa::BwdParams& bp, const void* out, const void* dout, float* 
 }  // namespace
 
 extern "C" {
+
+const char* swa_last_error_detail(void) { return t_err_detail; }
 
 const char* swa_status_string(int status) {
     switch (status) {
@@ -684,9 +719,8 @@ int swa_watchdog_selftest(int limit_us, void* stream) {
     DeviceState* st = nullptr;
     int rc = current_device_state(&st);
     if (rc) return rc;
-    swa::watchdog_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
-        st->status, (unsigned long long)limit_us * 1000ull);
-    return cudaPeekAtLastError() == cudaSuccess ? SWA_OK : SWA_ERR_CUDA;
+    return launch_plain(swa::watchdog_selftest_kernel, 1u, 32u, static_cast<cudaStream_t>(stream),
+                        st->status, (unsigned long long)limit_us * 1000ull);
 }
 
 size_t swa_decode_workspace_bytes(int B, int Hq, int W, int d) {
@@ -897,22 +931,22 @@ int diff_attn_bwd(const void* q1, const void* k1, const void* q2, const void* k2
     const int n_tiles = (N + BM - 1) / BM;
     auto run = [&](auto dtag) -> int {
         constexpr int D = decltype(dtag)::value;
-        swa::bwd_delta_kernel<D><<<dgrid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(out1),
-                                                         static_cast<const __nv_bfloat16*>(dout),
-                                                         delta1, rows);
-        swa::bwd_delta_kernel<D><<<dgrid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(out2),
-                                                         static_cast<const __nv_bfloat16*>(dout),
-                                                         delta2, rows);
-        if (cudaPeekAtLastError() != cudaSuccess) return SWA_ERR_CUDA;
+        const auto* go = static_cast<const __nv_bfloat16*>(dout);
         int r;
+        if ((r = launch_plain(swa::bwd_delta_kernel<D>, dgrid, 256u, s,
+                              static_cast<const __nv_bfloat16*>(out1), go, delta1, rows)))
+            return r;
+        if ((r = launch_plain(swa::bwd_delta_kernel<D>, dgrid, 256u, s,
+                              static_cast<const __nv_bfloat16*>(out2), go, delta2, rows)))
+            return r;
         if ((r = launch_bwd<D, 0>(p1, n_tiles, B * Hkv, s, *st))) return r;  // dk1, dV1 (fp32)
         if ((r = launch_bwd<D, 0>(p2, n_tiles, B * Hkv, s, *st))) return r;  // dk2, dv
         if ((r = launch_bwd<D, 1>(p1, n_tiles, B * Hq, s, *st))) return r;   // dq1
         if ((r = launch_bwd<D, 1>(p2, n_tiles, B * Hq, s, *st))) return r;   // dq2
-        if (dlambda) {
-            swa::bwd_dlam_kernel<<<(unsigned)Hq, 256, 0, s>>>(delta2, dlambda, B, Hq, N);
-            if (cudaPeekAtLastError() != cudaSuccess) return SWA_ERR_CUDA;
-        }
+        if (dlambda &&
+            (r = launch_plain(swa::bwd_dlam_kernel, (unsigned)Hq, 256u, s,
+                              static_cast<const float*>(delta2), dlambda, B, Hq, N)))
+            return r;
         return SWA_OK;
     };
     if (d == 128) return run(std::integral_constant<int, 128>{});
