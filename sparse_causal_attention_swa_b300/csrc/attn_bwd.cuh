@@ -89,27 +89,33 @@ struct BwdLayout {
     // step; dq: K, read again by dQ); ring B that of dP (dk/dv: dO, read again by dV in mid
     // step; dq: V).  The dq kernel's ring A has three entries, so K(s+1) is in place when S(s+1)
     // is issued at the start of step s.
-    static constexpr int NA = (KIND == 0) ? 2 : 3;
-    static constexpr int NB = 2;
+    // (at d = 64 both rings of both kernels take three entries: the tiles are half the size)
+    static constexpr int NA = (KIND == 0 && D == 128) ? 2 : 3;
+    static constexpr int NB = (D == 128) ? 2 : 3;
     static constexpr int OFF_FIX = 0;        // the two tiles the CTA keeps (K, V or Q, dO)
     static constexpr int OFF_RA = 2 * TB;
     static constexpr int OFF_RB = OFF_RA + NA * TB;
     static constexpr int OFF_DS = OFF_RB + NB * TB;  // dk/dv: dS^T, 128 keys x 128 queries
     static constexpr int DS_BYTES = (KIND == 0) ? BM * BN * 2 : 0;
-    static constexpr int OFF_BAR = OFF_DS + DS_BYTES;
+    // d = 64 dk/dv kinds: each compute warp's 64 query columns of lse2 and delta, read as
+    // broadcasts instead of warp shuffles (at d = 128 the 2 KiB do not fit)
+    static constexpr bool LSE_SMEM = (KIND == 0) && (D == 64);
+    static constexpr int OFF_LSE = OFF_DS + DS_BYTES;
+    static constexpr int LSE_BYTES = LSE_SMEM ? BWD_COMPUTE_WARPS * 2 * 64 * 4 : 0;
+    static constexpr int OFF_BAR = OFF_LSE + LSE_BYTES;
     static constexpr int BAR_FIX = 0;
     static constexpr int BAR_AFULL = 1;    // three (ring A entries)
     static constexpr int BAR_AEMPTY = 4;   // three
-    static constexpr int BAR_BFULL = 7;    // two (ring B entries)
-    static constexpr int BAR_BEMPTY = 9;   // two
-    static constexpr int BAR_SREADY = 11;  // S (dq: per region, two) is in TMEM
-    static constexpr int BAR_DPREADY = 13; // dP is in TMEM
-    static constexpr int BAR_P = 14;       // dk/dv: P^T is in TMEM (one arrival per warp)
-    static constexpr int BAR_DPL = 15;     // dP has been read (one arrival per warp)
-    static constexpr int BAR_DS = 16;      // dS^T in smem / dS in TMEM (dq: per region, two)
-    static constexpr int BAR_DSFREE = 18;  // dk/dv: the dS^T tile may be rewritten
-    static constexpr int BAR_FIN = 19;     // every MMA of the CTA has completed
-    static constexpr int NBARS = 20;
+    static constexpr int BAR_BFULL = 7;    // three (ring B entries)
+    static constexpr int BAR_BEMPTY = 10;  // three
+    static constexpr int BAR_SREADY = 13;  // S (dq: per region, two) is in TMEM
+    static constexpr int BAR_DPREADY = 15; // dP is in TMEM
+    static constexpr int BAR_P = 16;       // dk/dv: P^T is in TMEM (one arrival per warp)
+    static constexpr int BAR_DPL = 17;     // dP has been read (one arrival per warp)
+    static constexpr int BAR_DS = 18;      // dS^T in smem / dS in TMEM (dq: per region, two)
+    static constexpr int BAR_DSFREE = 20;  // dk/dv: the dS^T tile may be rewritten
+    static constexpr int BAR_FIN = 21;     // every MMA of the CTA has completed
+    static constexpr int NBARS = 22;
     static constexpr int OFF_TMEM = OFF_BAR + NBARS * 8;
     static constexpr int OFF_ABORT = OFF_TMEM + 4;
     static constexpr int END = OFF_ABORT + 4;
@@ -232,6 +238,22 @@ __global__ void bwd_delta_kernel(const __nv_bfloat16* __restrict__ out,
     delta[r] = acc;
 }
 
+// Sum the compact pass's cchunks partial sums into the first: part[i] += part[c * slot + i]
+// for c = 1 .. cchunks-1, for the dk and the dv halves (2 * slot floats in all), so the window
+// dk/dv kernel adds one row per compact key.  A fixed order: deterministic.
+__global__ void __launch_bounds__(256) bwd_compact_reduce_kernel(float* __restrict__ part,
+                                                                 int cchunks, long long slot) {
+    const long long n = 2 * slot;
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+         i += (long long)gridDim.x * blockDim.x) {
+        const long long half = i / slot, j = i % slot;
+        float* base = part + half * (long long)cchunks * slot;
+        float acc = base[j];
+        for (int c = 1; c < cchunks; ++c) acc += base[(long long)c * slot + j];
+        base[j] = acc;
+    }
+}
+
 // dlam[h] = -sum over batches and rows of delta[b, h, i] (the gradient of a differential
 // head's lambda: d out_i / d lambda = -(A2 V)_i, and delta2_i = dout_i . (A2 V)_i); one CTA of
 // 256 threads per head, a fixed summation order, so the result is deterministic.
@@ -342,9 +364,11 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) attn_bwd_kernel(const __grid_c
             mbar_init(bar(L::BAR_AFULL + i), 1);
             mbar_init(bar(L::BAR_AEMPTY + i), 1);
         }
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < 3; ++i) {
             mbar_init(bar(L::BAR_BFULL + i), 1);
             mbar_init(bar(L::BAR_BEMPTY + i), 1);
+        }
+        for (int i = 0; i < 2; ++i) {
             mbar_init(bar(L::BAR_SREADY + i), 1);
             mbar_init(bar(L::BAR_DS + i), BWD_COMPUTE_WARPS);
         }
@@ -590,6 +614,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) attn_bwd_kernel(const __grid_c
             // cc holds query column 32 (2 half + cc) + l, handed to the other lanes by shuffles
             float lse2_c[2], delta_c[2];
             const int ct = step_tile(s);
+            // d = 64: this warp's 64 lse2 then 64 delta values, broadcast from shared memory
+            float* lsw = reinterpret_cast<float*>(smem + L::OFF_LSE) + warp * 128;
             if (DKDV) {
                 const int qm = step_qmat(s);
                 bwd_mu(p, qm % p.Hq, mu_l2, mu_sign);
@@ -599,7 +625,12 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) attn_bwd_kernel(const __grid_c
                     const int qc = ct * BM + (2 * half + cc) * 32 + (int)lane;
                     lse2_c[cc] = (qc < p.N) ? __ldg(p.lse + base + qc) * LOG2E_F - mu_l2 : 0.f;
                     delta_c[cc] = (qc < p.N) ? __ldg(p.delta + base + qc) : 0.f;
+                    if (L::LSE_SMEM) {
+                        lsw[cc * 32 + lane] = lse2_c[cc];
+                        lsw[64 + cc * 32 + lane] = delta_c[cc];
+                    }
                 }
+                if (L::LSE_SMEM) __syncwarp();
             }
             // allowed pairs: key j and query i with i - W < j <= i, both < N; compact key r
             // (position r * stride) and query i with r < ncomp(i), i.e. i >= r * stride + W
@@ -640,7 +671,9 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) attn_bwd_kernel(const __grid_c
 #pragma unroll
                 for (int u = 0; u < 32; ++u) {
                     const int col = (2 * half + cc) * 32 + u;
-                    const float l2 = DKDV ? __shfl_sync(0xffffffffu, lse2_c[cc], u) : lse2_row;
+                    const float l2 = !DKDV ? lse2_row
+                                     : L::LSE_SMEM ? lsw[cc * 32 + u]
+                                                   : __shfl_sync(0xffffffffu, lse2_c[cc], u);
                     const bool in = (col >= a) && (col <= bnd);
                     pv[cc * 32 + u] = in ? fast_exp2(fmaf(__uint_as_float(sr[u]), sl2, -l2)) : 0.f;
                 }
@@ -675,7 +708,9 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) attn_bwd_kernel(const __grid_c
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
                         const float dl =
-                            DKDV ? __shfl_sync(0xffffffffu, delta_c[cc], 2 * u + e) : delta_row;
+                            !DKDV ? delta_row
+                            : L::LSE_SMEM ? lsw[64 + cc * 32 + 2 * u + e]
+                                          : __shfl_sync(0xffffffffu, delta_c[cc], 2 * u + e);
                         dsv[e] = pv[cc * 32 + 2 * u + e] * (__uint_as_float(dr[2 * u + e]) - dl);
                     }
                     dsw[cc * 16 + u] = pack_bf16x2(dsv[0], dsv[1]) ^ mu_sign;
@@ -737,12 +772,11 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) attn_bwd_kernel(const __grid_c
                 } else if (p.dv32_in) {  // the second map: dV of both maps, rounded once
                     bwd_store_half_row<D>(tA1, 1.f, p.dv + row * D, valid, c0,
                                           p.dv32_in + row * D, 1, 0);
-                } else {
+                } else {  // the compact partials were summed into their first chunk
                     bwd_store_half_row<D>(tA1, 1.f, p.dv + row * D, valid, c0,
-                                          xk ? xk + part : nullptr, p.cchunks, cstride);
+                                          xk ? xk + part : nullptr, 1, cstride);
                 }
-                bwd_store_half_row<D>(tA2, p.scale, p.dk + row * D, valid, c0, xk, p.cchunks,
-                                      cstride);
+                bwd_store_half_row<D>(tA2, p.scale, p.dk + row * D, valid, c0, xk, 1, cstride);
             } else {
                 const size_t row = (size_t)bz * p.N + (size_t)(valid ? my : 0);
                 bwd_store_half_row<D>(tA1, p.scale, p.dq + row * D, valid, c0);

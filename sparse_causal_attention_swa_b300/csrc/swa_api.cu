@@ -439,10 +439,18 @@ int run_bwd(const swa::BwdParams& bp, const void* out, const void* dout, float* 
                           static_cast<const __nv_bfloat16*>(out),
                           static_cast<const __nv_bfloat16*>(dout), delta, rows);
     if (rc) return rc;
-    if (bp.cap > 0 && bp.ncomp > 0 &&
-        (rc = launch_bwd<D, 2>(bp, (bp.ncomp_pad / swa::BN) * bp.cchunks, bp.B * bp.Hkv, stream,
-                               st)))
-        return rc;
+    if (bp.cap > 0 && bp.ncomp > 0) {
+        if ((rc = launch_bwd<D, 2>(bp, (bp.ncomp_pad / swa::BN) * bp.cchunks, bp.B * bp.Hkv,
+                                   stream, st)))
+            return rc;
+        if (bp.cchunks > 1) {
+            const long long slot = (long long)bp.B * bp.Hkv * bp.ncomp_pad * D;
+            const unsigned grid = (unsigned)std::min<long long>((2 * slot + 255) / 256, 4096);
+            if ((rc = launch_plain(swa::bwd_compact_reduce_kernel, grid, 256u, stream, bp.cpart,
+                                   bp.cchunks, slot)))
+                return rc;
+        }
+    }
     if ((rc = launch_bwd<D, 0>(bp, n_tiles, bp.B * bp.Hkv, stream, st))) return rc;
     return launch_bwd<D, 1>(bp, n_tiles, bp.B * bp.Hq, stream, st);
 }
