@@ -662,20 +662,44 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) attn_bwd_kernel(const __grid_c
             ok = wait(bar(L::BAR_SREADY + rg), DKDV ? ((uint32_t)s & 1u) : ((uint32_t)(s >> 1) & 1u));
             if (!ok) break;
             tc_fence_after();
-            // the weights of this warp's 64 columns
+            // the weights of this warp's 64 columns; a 32-column chunk wholly inside every lane's
+            // allowed range (most chunks, for a window much wider than a tile) skips the mask
             float pv[64];
 #pragma unroll
             for (int cc = 0; cc < 2; ++cc) {
                 uint32_t sr[32];
                 tmem_ld32(tS + (uint32_t)(half * 64 + cc * 32), sr);
+                const int c0 = (2 * half + cc) * 32;
+                const bool full = __all_sync(0xffffffffu, a <= c0 && bnd >= c0 + 31);
+                float l2v[32];  // the column's lse2 (dk/dv) or the row's (dq)
+                if (!DKDV) {
 #pragma unroll
-                for (int u = 0; u < 32; ++u) {
-                    const int col = (2 * half + cc) * 32 + u;
-                    const float l2 = !DKDV ? lse2_row
-                                     : L::LSE_SMEM ? lsw[cc * 32 + u]
-                                                   : __shfl_sync(0xffffffffu, lse2_c[cc], u);
-                    const bool in = (col >= a) && (col <= bnd);
-                    pv[cc * 32 + u] = in ? fast_exp2(fmaf(__uint_as_float(sr[u]), sl2, -l2)) : 0.f;
+                    for (int u = 0; u < 32; ++u) l2v[u] = lse2_row;
+                } else if (L::LSE_SMEM) {
+                    const float4* l4 = reinterpret_cast<const float4*>(lsw + cc * 32);
+#pragma unroll
+                    for (int u4 = 0; u4 < 8; ++u4) {
+                        const float4 x = l4[u4];
+                        l2v[4 * u4] = x.x;
+                        l2v[4 * u4 + 1] = x.y;
+                        l2v[4 * u4 + 2] = x.z;
+                        l2v[4 * u4 + 3] = x.w;
+                    }
+                } else {
+#pragma unroll
+                    for (int u = 0; u < 32; ++u) l2v[u] = __shfl_sync(0xffffffffu, lse2_c[cc], u);
+                }
+                if (full) {
+#pragma unroll
+                    for (int u = 0; u < 32; ++u)
+                        pv[cc * 32 + u] = fast_exp2(fmaf(__uint_as_float(sr[u]), sl2, -l2v[u]));
+                } else {
+#pragma unroll
+                    for (int u = 0; u < 32; ++u) {
+                        const bool in = (c0 + u >= a) && (c0 + u <= bnd);
+                        pv[cc * 32 + u] =
+                            in ? fast_exp2(fmaf(__uint_as_float(sr[u]), sl2, -l2v[u])) : 0.f;
+                    }
                 }
             }
             if (DKDV) {
@@ -685,7 +709,11 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) attn_bwd_kernel(const __grid_c
                 for (int cc = 0; cc < 2; ++cc) {
 #pragma unroll
                     for (int u = 0; u < 16; ++u)
-                        pk[u] = pack_bf16x2(pv[cc * 32 + 2 * u], pv[cc * 32 + 2 * u + 1]) ^ mu_sign;
+                        pk[u] = pack_bf16x2(pv[cc * 32 + 2 * u], pv[cc * 32 + 2 * u + 1]);
+                    if (mu_sign) {
+#pragma unroll
+                        for (int u = 0; u < 16; ++u) pk[u] ^= mu_sign;
+                    }
                     tmem_st16(tS + (uint32_t)(half * 64 + cc * 16), pk);
                 }
                 tmem_wait_st();
@@ -702,19 +730,35 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) attn_bwd_kernel(const __grid_c
             for (int cc = 0; cc < 2; ++cc) {
                 uint32_t dr[32];
                 tmem_ld32(tDP + (uint32_t)(half * 64 + cc * 32), dr);
+                float dlv[32];  // the column's delta (dk/dv) or the row's (dq)
+                if (!DKDV) {
+#pragma unroll
+                    for (int u = 0; u < 32; ++u) dlv[u] = delta_row;
+                } else if (L::LSE_SMEM) {
+                    const float4* d4 = reinterpret_cast<const float4*>(lsw + 64 + cc * 32);
+#pragma unroll
+                    for (int u4 = 0; u4 < 8; ++u4) {
+                        const float4 x = d4[u4];
+                        dlv[4 * u4] = x.x;
+                        dlv[4 * u4 + 1] = x.y;
+                        dlv[4 * u4 + 2] = x.z;
+                        dlv[4 * u4 + 3] = x.w;
+                    }
+                } else {
+#pragma unroll
+                    for (int u = 0; u < 32; ++u) dlv[u] = __shfl_sync(0xffffffffu, delta_c[cc], u);
+                }
 #pragma unroll
                 for (int u = 0; u < 16; ++u) {
-                    float dsv[2];
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const float dl =
-                            !DKDV ? delta_row
-                            : L::LSE_SMEM ? lsw[64 + cc * 32 + 2 * u + e]
-                                          : __shfl_sync(0xffffffffu, delta_c[cc], 2 * u + e);
-                        dsv[e] = pv[cc * 32 + 2 * u + e] * (__uint_as_float(dr[2 * u + e]) - dl);
-                    }
-                    dsw[cc * 16 + u] = pack_bf16x2(dsv[0], dsv[1]) ^ mu_sign;
+                    const float d0 = pv[cc * 32 + 2 * u] * (__uint_as_float(dr[2 * u]) - dlv[2 * u]);
+                    const float d1 =
+                        pv[cc * 32 + 2 * u + 1] * (__uint_as_float(dr[2 * u + 1]) - dlv[2 * u + 1]);
+                    dsw[cc * 16 + u] = pack_bf16x2(d0, d1);
                 }
+            }
+            if (mu_sign) {
+#pragma unroll
+                for (int u = 0; u < 32; ++u) dsw[u] ^= mu_sign;
             }
             // dP has been read: the issuer may overwrite it with the next step's
             tc_fence_before();
