@@ -9,7 +9,10 @@
 //
 // The step is bound by HBM: every window key and value row is read once and each feeds
 // Hq/Hkv queries only.  Split-K over the slots:
-//   decode_split_kernel<D, G>   grid (splits of DEC_KS slots, B*Hkv), DEC_KS threads.  TMA
+//   decode_mma_kernel<G>        d = 128: the same split with both products on tcgen05 (the
+//                               slots as the 128 MMA rows, the heads as N = 16 columns); see
+//                               below.
+//   decode_split_kernel<D, G>   d = 64: grid (splits of DEC_KS slots, B*Hkv), DEC_KS threads.  TMA
 //                               loads the split's K and V rows (128B-swizzled boxes) into
 //                               shared memory; thread t scores slot t against the G query
 //                               heads of the KV head (packed fp32x2 products on the CUDA
@@ -20,8 +23,10 @@
 //                               domain) and its sum l.
 //   decode_combine_kernel<D>    grid (B*Hq), D threads: rescales the splits to a common
 //                               maximum, out = sum O_s 2^(m_s - m) / sum l_s 2^(m_s - m).
-// Tensor cores are not used: with G <= 16 queries per KV head the products are far below
-// one MMA tile and the step is bound by HBM.
+// The CUDA-core products of decode_split_kernel keep a split busy long after its load has
+// landed, and only three splits fit on an SM, so too few bytes are in flight; on the tensor
+// core the products take a few hundred cycles although 15 of the 16 columns are padding at
+// G = 1.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -280,6 +285,211 @@ __global__ void __launch_bounds__(DEC_THREADS) decode_split_kernel(const __grid_
             p.part_ml[row * 2] = mh;
             p.part_ml[row * 2 + 1] = l;
         }
+    }
+    if (t == 0 && *abort_flag) atomicExch(p.status, 6 /* SWA_ERR_TIMEOUT */);
+}
+
+// ------------------------------------------------------------------------------------------
+// Tensor-core form of a split (d = 128).  The slots are the 128 rows of two tcgen05 products
+// and the G <= 16 query heads of the KV head their N = 16 columns:
+//   S^T[slot][h] = K Q^T   (A: the K tile, K-major; B: the heads' queries, K-major)
+//   O^T[c][h]    = V^T P^T (A: the V tile read MN-major; B: the weights, K-major)
+// both accumulated in tensor memory (columns [0,16) and [16,32) of a 32-column allocation).
+// Thread t owns slot t (TMEM lane t) for the softmax, as in decode_split_kernel, and column
+// t of the output afterwards.  Only the softmax stays on the CUDA cores, so a split's life
+// is mostly its TMA load.  The weights are rounded to bf16 for the second product (the
+// forward kernel does the same); the sum l adds them unrounded.
+template <int G>
+struct DecMmaSmem {
+    static constexpr int D = 128;
+    static constexpr int NB = 16;                     // MMA N: the heads, padded
+    static constexpr int KV_BYTES = DEC_KS * D * 2;   // a K or V split: two 64-column boxes
+    static constexpr int OFF_K = 0;
+    static constexpr int OFF_V = KV_BYTES;
+    static constexpr int OFF_Q = 2 * KV_BYTES;        // bf16 [NB][D], K-major, 128B-swizzled
+    static constexpr int OFF_P = OFF_Q + NB * D * 2;  // bf16 [NB][DEC_KS], same layout
+    static constexpr int OFF_RED = OFF_P + NB * DEC_KS * 2;          // fp32 [2][DEC_WARPS][G]
+    static constexpr int OFF_BAR = OFF_RED + 2 * DEC_WARPS * G * 4;  // K, V, MMA done
+    static constexpr int OFF_TMEM = OFF_BAR + 24;
+    static constexpr int OFF_ABORT = OFF_TMEM + 4;
+    static constexpr int END = OFF_ABORT + 4;
+    static constexpr int BYTES = END + 1024;  // slack for aligning the base to 1024
+    static constexpr uint32_t TMEM_COLS = 32;
+    static_assert(DEC_KS == 128 && DEC_THREADS == 128, "one slot per thread and TMEM lane");
+    static_assert(G <= NB, "at most 16 query heads per KV head");
+};
+
+// Byte offset of element (row n, column k) of a K-major, 128-byte-swizzled operand tile of
+// `rows` rows (a multiple of 8): 64-column chunks of rows x 128 bytes, the 16-byte unit u of
+// a row stored at u ^ (n & 7).
+__device__ __forceinline__ uint32_t kmajor_sw128(int rows, int n, int k) {
+    return (uint32_t)((k >> 6) * (rows * 128) + n * 128 + ((((k & 63) >> 3) ^ (n & 7)) << 4) +
+                      (k & 7) * 2);
+}
+
+template <int G>
+__global__ void __launch_bounds__(DEC_THREADS) decode_mma_kernel(const __grid_constant__ DecParams p) {
+    constexpr int D = 128;
+    using L = DecMmaSmem<G>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    float* red = reinterpret_cast<float*>(smem + L::OFF_RED);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::OFF_ABORT);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::OFF_TMEM);
+    const uint32_t bar_k = sbase + L::OFF_BAR, bar_v = bar_k + 8, bar_m = bar_k + 16;
+
+    const int split = blockIdx.x;
+    const int bh = blockIdx.y;  // b * Hkv + hk
+    const int b = bh / p.Hkv, hk = bh % p.Hkv;
+    const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+    const uint64_t lim = p.wait_limit_ns;
+    const int posb = p.pos[b];
+    const int nvalid = posb < 0 ? 0 : min(posb + 1, p.W);
+    const int k0 = split * DEC_KS;
+    if (k0 >= nvalid) return;  // the combine reads only the splits that hold window keys
+    const int nk = min(DEC_KS, nvalid - k0);
+
+    if (t == 0) {
+        mbar_init(bar_k, 1);
+        mbar_init(bar_v, 1);
+        mbar_init(bar_m, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+        mbar_arrive_expect_tx(bar_k, L::KV_BYTES);
+        for (int c = 0; c < D / 64; ++c)
+            tma_load_3d(sbase + L::OFF_K + c * (DEC_KS * 128), &p.tm_kc, bar_k, c * 64, k0, bh);
+        mbar_arrive_expect_tx(bar_v, L::KV_BYTES);
+        for (int c = 0; c < D / 64; ++c)
+            tma_load_3d(sbase + L::OFF_V + c * (DEC_KS * 128), &p.tm_vc, bar_v, c * 64, k0, bh);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), L::TMEM_COLS);
+        tmem_relinquish();
+    }
+    // the g <= G query heads of this KV head as rows of the B operand (rows h >= g zero)
+    const int g = p.Hq / p.Hkv;
+    for (int i = t; i < L::NB * (D / 8); i += DEC_THREADS) {
+        const int h = i / (D / 8), u = i % (D / 8);
+        uint4 raw = make_uint4(0u, 0u, 0u, 0u);
+        if (h < g)
+            raw = *reinterpret_cast<const uint4*>(p.q + ((size_t)b * p.Hq + (size_t)hk * g + h) * D +
+                                                  u * 8);
+        *reinterpret_cast<uint4*>(smem + L::OFF_Q + kmajor_sw128(L::NB, h, u * 8)) = raw;
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t tS = tmem, tO = tmem + 16u;
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    constexpr uint32_t ID_S = idesc_bf16_f32(DEC_KS, L::NB, 0, 0);
+    constexpr uint32_t ID_O = idesc_bf16_f32(D, L::NB, 0, 1);  // A = V^T, MN-major
+
+    // ---- S^T = K Q^T, issued by warp 0 (converged; one elected lane per operation)
+    if (warp == 0) {
+        const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar_k, 0, abort_flag, lim));
+        if (ok) {
+            const uint64_t ak = smem_desc_sw128(sbase + L::OFF_K, 16, 1024);
+            const uint64_t bq = smem_desc_sw128(sbase + L::OFF_Q, 16, 1024);
+#pragma unroll
+            for (int k = 0; k < D / 16; ++k) {
+                const uint32_t offk = ((k >> 2) * (DEC_KS * 128) + (k & 3) * 32) >> 4;
+                const uint32_t offq = ((k >> 2) * (L::NB * 128) + (k & 3) * 32) >> 4;
+                mma_ss_elect(tS, ak + offk, bq + offq, ID_S, k > 0 ? 1u : 0u);
+            }
+            mma_commit_elect(bar_m);
+        }
+    }
+    bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(bar_m, 0, abort_flag, lim));
+    tc_fence_after();
+    uint32_t sr[16];
+    if (ok) tmem_ld16(tS + lane_off, sr);  // warp-uniform condition: the load is collective
+    const bool valid = ok && t < nk;
+    float s[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) s[h] = valid ? __uint_as_float(sr[h]) * p.scale_log2 : -INFINITY;
+
+    // ---- per head: maximum and sum over the split (warp shuffles, then the warps)
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+        float v = s[h];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+        if (lane == 0) red[warp * G + h] = v;
+    }
+    __syncthreads();
+    float e[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+        float mh = red[h];
+#pragma unroll
+        for (int w = 1; w < DEC_WARPS; ++w) mh = fmaxf(mh, red[w * G + h]);
+        e[h] = valid ? exp2f(s[h] - mh) : 0.f;
+        float v = e[h];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        if (lane == 0) red[DEC_WARPS * G + warp * G + h] = v;
+    }
+    // the weights of slot t as column t of the B operand P^T (rows h >= G zero)
+#pragma unroll
+    for (int h = 0; h < L::NB; ++h)
+        *reinterpret_cast<__nv_bfloat16*>(smem + L::OFF_P + kmajor_sw128(L::NB, h, t)) =
+            __float2bfloat16_rn(h < G ? e[h] : 0.f);
+    // slots past the window's end may hold anything, even NaN, and a zero weight does not
+    // cancel a NaN in the product: their V rows are zeroed
+    if (ok) ok = mbar_wait_bounded(bar_v, 0, abort_flag, lim);
+    if (ok && t >= nk) {
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c) {
+            uint4* row = reinterpret_cast<uint4*>(smem + L::OFF_V + c * (DEC_KS * 128) + t * 128);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) row[u] = make_uint4(0u, 0u, 0u, 0u);
+        }
+    }
+    fence_proxy_async_smem();
+    const bool go = __syncthreads_and(ok) != 0;
+
+    // ---- O^T = V^T P^T over the split's 128 slots, issued by warp 0
+    if (go && warp == 0) {
+        const uint64_t av = smem_desc_sw128(sbase + L::OFF_V, DEC_KS * 128, 1024);
+        const uint64_t bp = smem_desc_sw128(sbase + L::OFF_P, 16, 1024);
+#pragma unroll
+        for (int k = 0; k < DEC_KS / 16; ++k) {
+            const uint32_t offv = (k * 2048) >> 4;  // 16 slots = 16 rows of 128 bytes
+            const uint32_t offp = ((k >> 2) * (L::NB * 128) + (k & 3) * 32) >> 4;
+            mma_ss_elect(tO, av + offv, bp + offp, ID_O, k > 0 ? 1u : 0u);
+        }
+        mma_commit_elect(bar_m);
+    }
+    ok = __all_sync(0xffffffffu, go && mbar_wait_bounded(bar_m, 1, abort_flag, lim));
+    tc_fence_after();
+    if (ok) {
+        uint32_t orow[16];
+        tmem_ld16(tO + lane_off, orow);  // output column t of every head
+        const size_t row0 = ((size_t)b * p.Hq + (size_t)hk * g) * p.nsplit + split;
+#pragma unroll
+        for (int h = 0; h < G; ++h)
+            if (h < g) p.part_o[(row0 + (size_t)h * p.nsplit) * D + t] = __uint_as_float(orow[h]);
+        if (t < g) {
+            float l = 0.f, mh = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < DEC_WARPS; ++w) {
+                l += red[DEC_WARPS * G + w * G + t];
+                mh = fmaxf(mh, red[w * G + t]);
+            }
+            const size_t row = row0 + (size_t)t * p.nsplit;
+            p.part_ml[row * 2] = mh;
+            p.part_ml[row * 2 + 1] = l;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, L::TMEM_COLS);
     }
     if (t == 0 && *abort_flag) atomicExch(p.status, 6 /* SWA_ERR_TIMEOUT */);
 }

@@ -284,6 +284,17 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
         : "memory");
 }
 
+// Same for 16 columns.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : SWA_R8(0), SWA_R8(8)
+        : "r"(taddr)
+        : "memory");
+}
+
 // Same for 64 columns.
 __device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
     asm volatile(
@@ -387,13 +398,14 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t start, uint32_t lbo
 }
 
 // Instruction descriptor of tcgen05.mma kind::f16 with bf16 A and B and an fp32 accumulator.
-// b_mn_major selects an MN-major (transposed) B operand.
+// b_mn_major / a_mn_major select an MN-major (transposed) B / A operand.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N,
-                                                      uint32_t b_mn_major) {
+                                                      uint32_t b_mn_major,
+                                                      uint32_t a_mn_major = 0) {
     return (1u << 4)                 // D format: f32
            | (1u << 7)               // A format: bf16
            | (1u << 10)              // B format: bf16
-           | (0u << 15)              // A K-major
+           | (a_mn_major << 15)      // A major-ness
            | (b_mn_major << 16)      // B major-ness
            | ((N >> 3) << 17)        // N / 8
            | ((M >> 4) << 24);       // M / 16

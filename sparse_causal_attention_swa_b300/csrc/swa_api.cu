@@ -349,11 +349,16 @@ size_t decode_workspace_bytes(long long B, long long Hq, long long W, int d) {
 template <int D, int G>
 int launch_decode(const swa::DecParams& dp, int B, int Hkv, cudaStream_t stream, DeviceState& st,
                   int gi) {
-    using L = swa::DecSmem<D, G>;
-    auto kern = swa::decode_split_kernel<D, G>;
+    // d = 128: the tensor-core split; d = 64: the CUDA-core split
+    constexpr int BYTES = (D == 128) ? swa::DecMmaSmem<G>::BYTES : swa::DecSmem<D, G>::BYTES;
+    void (*kern)(const swa::DecParams);
+    if constexpr (D == 128)
+        kern = swa::decode_mma_kernel<G>;
+    else
+        kern = swa::decode_split_kernel<D, G>;
     bool& set = st.dec_attr_set[D == 128 ? 1 : 0][gi];
     if (!set) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::BYTES) !=
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, BYTES) !=
             cudaSuccess)
             return SWA_ERR_CUDA;
         set = true;
@@ -361,7 +366,7 @@ int launch_decode(const swa::DecParams& dp, int B, int Hkv, cudaStream_t stream,
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)dp.nsplit, (unsigned)(B * Hkv), 1);
     cfg.blockDim = dim3(swa::DEC_THREADS, 1, 1);
-    cfg.dynamicSmemBytes = L::BYTES;
+    cfg.dynamicSmemBytes = BYTES;
     cfg.stream = stream;
     if (cudaLaunchKernelEx(&cfg, kern, dp) != cudaSuccess) return SWA_ERR_CUDA;
     cudaLaunchConfig_t cc = {};
