@@ -22,14 +22,13 @@
 // The dq kernel recomputes S and dP instead of having the dk/dv kernel scatter dq with
 // atomics: dq stays deterministic and no fp32 dq buffer is needed.
 //
-// CTA organisation (320 threads): warps 0-7 compute; warps w and w + 4 share TMEM lanes
-// 32 (w % 4) .. 32 (w % 4) + 31 (a query row each in the dq kernel, a key row each in the
-// dk/dv kernel) and split the 128 columns of a step, 64 each, so two warps per lane quarter
-// overlap their exponentials; warp 8 lane 0 loads tiles with TMA, warp 9 owns TMEM and
+// CTA organisation (576 threads): warps 0-15 compute; warps w, w + 4, w + 8, w + 12 share
+// TMEM lanes 32 (w % 4) .. 32 (w % 4) + 31 (a query row each in the dq kernel, a key row each
+// in the dk/dv kernel) and split the 128 columns of a step, 32 each, so four warps per lane
+// quarter overlap their latencies; warp 16 lane 0 loads tiles with TMA, warp 17 owns TMEM and
 // issues the MMAs (converged warp, one elected lane per operation).  P^T (dk/dv) and dS
-// (dq) are packed to bf16 pairs over the first 32 of each half's 64 columns of their S
-// region, i.e. its TMEM columns [0, 32) and [64, 96); a warp overwrites only columns it has
-// read.  dS^T (dk/dv) goes to a 128 x 128 shared-memory tile in the 128-byte-swizzled
+// (dq) are packed to bf16 pairs over the first 16 of each warp's 32 columns of their S
+// region; a warp overwrites only columns it has read.  dS^T (dk/dv) goes to a 128 x 128 shared-memory tile in the 128-byte-swizzled
 // K-major layout, the A operand of dK += dS^T Q.
 // Every MMA form here is one the forward kernel uses: S-type products with both operands
 // K-major from shared memory, accumulating products whose A operand (P^T or dS, bf16 packed
@@ -75,33 +74,38 @@ struct BwdParams {
     float scale, scale_log2;
 };
 
-constexpr int BWD_THREADS = 320;
-constexpr int BWD_COMPUTE_WARPS = 8;
-constexpr int BWD_PRODUCER_WARP = 8;
-constexpr int BWD_MMA_WARP = 9;
+#ifndef SWA_BWD_COMPUTE_WARPS
+#define SWA_BWD_COMPUTE_WARPS 16
+#endif
+// compute warps: four per TMEM lane quarter, each taking BWD_CW of a step's 128 columns
+constexpr int BWD_COMPUTE_WARPS = SWA_BWD_COMPUTE_WARPS;
+constexpr int BWD_CW = 128 / (BWD_COMPUTE_WARPS / 4);
+constexpr int BWD_NCH = BWD_CW / 32;  // 32-column chunks per warp and step
+constexpr int BWD_PRODUCER_WARP = BWD_COMPUTE_WARPS;
+constexpr int BWD_MMA_WARP = BWD_COMPUTE_WARPS + 1;
+constexpr int BWD_THREADS = 32 * (BWD_COMPUTE_WARPS + 2);
+static_assert(BWD_CW == 32 || BWD_CW == 64, "8 or 16 compute warps");
 constexpr float LOG2E_F = 1.4426950408889634f;
 
 template <int D, int KIND>
 struct BwdLayout {
     static constexpr int TB = BM * D * 2;    // one 128-row bf16 tile (D/64 boxes of 16 KiB)
     // The moving tiles come through two rings, so each is freed as soon as its last product
-    // is done.  Ring A holds the B operand of S (dk/dv: Q, read again by dK at the end of the
-    // step; dq: K, read again by dQ); ring B that of dP (dk/dv: dO, read again by dV in mid
-    // step; dq: V).  The dq kernel's ring A has three entries, so K(s+1) is in place when S(s+1)
-    // is issued at the start of step s.
-    // (at d = 64 both rings of both kernels take three entries: the tiles are half the size)
-    static constexpr int NA = (KIND == 0 && D == 128) ? 2 : 3;
+    // is done.  Ring A holds the B operand of S (dk/dv: Q, read again by dK; dq: K, read again
+    // by dQ); ring B that of dP (dk/dv: dO, read again by dV; dq: V).  Ring A has three
+    // entries, so the next step's tile is in place when S(s+1) is issued; at d = 64 ring B
+    // has three as well (the tiles are half the size).
+    static constexpr int NA = 3;
     static constexpr int NB = (D == 128) ? 2 : 3;
     static constexpr int OFF_FIX = 0;        // the two tiles the CTA keeps (K, V or Q, dO)
     static constexpr int OFF_RA = 2 * TB;
     static constexpr int OFF_RB = OFF_RA + NA * TB;
-    static constexpr int OFF_DS = OFF_RB + NB * TB;  // dk/dv: dS^T, 128 keys x 128 queries
-    static constexpr int DS_BYTES = (KIND == 0) ? BM * BN * 2 : 0;
+    static constexpr int OFF_DS = OFF_RB + NB * TB;
     // d = 64 dk/dv kinds: each compute warp's 64 query columns of lse2 and delta, read as
     // broadcasts instead of warp shuffles (at d = 128 the 2 KiB do not fit)
     static constexpr bool LSE_SMEM = (KIND == 0) && (D == 64);
-    static constexpr int OFF_LSE = OFF_DS + DS_BYTES;
-    static constexpr int LSE_BYTES = LSE_SMEM ? BWD_COMPUTE_WARPS * 2 * 64 * 4 : 0;
+    static constexpr int OFF_LSE = OFF_DS;
+    static constexpr int LSE_BYTES = LSE_SMEM ? BWD_COMPUTE_WARPS * 2 * BWD_CW * 4 : 0;
     static constexpr int OFF_BAR = OFF_LSE + LSE_BYTES;
     static constexpr int BAR_FIX = 0;
     static constexpr int BAR_AFULL = 1;    // three (ring A entries)
@@ -111,9 +115,8 @@ struct BwdLayout {
     static constexpr int BAR_SREADY = 13;  // S (dq: per region, two) is in TMEM
     static constexpr int BAR_DPREADY = 15; // dP is in TMEM
     static constexpr int BAR_P = 16;       // dk/dv: P^T is in TMEM (one arrival per warp)
-    static constexpr int BAR_DPL = 17;     // dP has been read (one arrival per warp)
-    static constexpr int BAR_DS = 18;      // dS^T in smem / dS in TMEM (dq: per region, two)
-    static constexpr int BAR_DSFREE = 20;  // dk/dv: the dS^T tile may be rewritten
+    static constexpr int BAR_DPL = 17;     // dq: dP has been read (one arrival per warp)
+    static constexpr int BAR_DS = 18;      // dS^T / dS is in TMEM (dq: per region, two)
     static constexpr int BAR_FIN = 21;     // every MMA of the CTA has completed
     static constexpr int NBARS = 22;
     static constexpr int OFF_TMEM = OFF_BAR + NBARS * 8;
@@ -134,30 +137,39 @@ __device__ __forceinline__ void bwd_load_tile(uint32_t dst, const CUtensorMap* m
     for (int c = 0; c < D / 64; ++c) tma_load_3d(dst + c * (BM * 128), m, bar, c * 64, row, mat);
 }
 
-// Columns [32 c0, 32 c0 + D/2) of fp32 from TMEM lane (the calling thread's), times `mul`,
-// to the same columns of one bf16 row (the two warps of a lane quarter store one half each).
+template <int CH>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&r)[CH]) {
+    if constexpr (CH == 32)
+        tmem_ld32(taddr, r);
+    else
+        tmem_ld16(taddr, r);
+}
+
+// Columns [col0, col0 + NC) of fp32 from TMEM lane (the calling thread's), times `mul`, to
+// the same columns of one bf16 row (the warps of a lane quarter store one share each).
 // `extra` (or null): n fp32 rows, `stride` floats apart, added to the columns before `mul`.
-template <int D>
-__device__ __forceinline__ void bwd_store_half_row(uint32_t taddr, float mul,
-                                                   __nv_bfloat16* dst, bool valid, int c0,
-                                                   const float* extra = nullptr, int n = 0,
-                                                   size_t stride = 0) {
+template <int NC>
+__device__ __forceinline__ void bwd_store_cols(uint32_t taddr, float mul, __nv_bfloat16* dst,
+                                               bool valid, int col0,
+                                               const float* extra = nullptr, int n = 0,
+                                               size_t stride = 0) {
+    constexpr int CH = NC < 32 ? NC : 32;
 #pragma unroll
-    for (int cc = 0; cc < D / 64; ++cc) {
-        const int c = c0 + cc;
-        uint32_t rr[32];
-        tmem_ld32(taddr + c * 32, rr);
+    for (int cc = 0; cc < NC / CH; ++cc) {
+        const int c = col0 + cc * CH;
+        uint32_t rr[CH];
+        tmem_ld_cols<CH>(taddr + c, rr);
         if (valid && extra != nullptr) {
             for (int i = 0; i < n; ++i) {
-                const float* x = extra + (size_t)i * stride + c * 32;
+                const float* x = extra + (size_t)i * stride + c;
 #pragma unroll
-                for (int e = 0; e < 32; ++e) rr[e] = __float_as_uint(__uint_as_float(rr[e]) + x[e]);
+                for (int e = 0; e < CH; ++e) rr[e] = __float_as_uint(__uint_as_float(rr[e]) + x[e]);
             }
         }
         if (valid) {
-            uint4* o = reinterpret_cast<uint4*>(dst + c * 32);
+            uint4* o = reinterpret_cast<uint4*>(dst + c);
 #pragma unroll
-            for (int v4 = 0; v4 < 4; ++v4) {
+            for (int v4 = 0; v4 < CH / 8; ++v4) {
                 const int e = v4 * 8;
                 o[v4] = make_uint4(
                     pack_bf16x2(__uint_as_float(rr[e + 0]) * mul, __uint_as_float(rr[e + 1]) * mul),
@@ -169,26 +181,27 @@ __device__ __forceinline__ void bwd_store_half_row(uint32_t taddr, float mul,
     }
 }
 
-// Columns [32 c0, 32 c0 + D/2) of fp32 from TMEM lane to the same columns of an fp32 row
-// (zeros when `have` is false: no product wrote the accumulator).  `have` must be the same in
-// every lane of the warp (tcgen05.ld is warp-collective); only lanes with `valid` store.
-template <int D>
-__device__ __forceinline__ void bwd_store_half_row_f32(uint32_t taddr, float* dst, bool have,
-                                                       bool valid, int c0) {
+// Columns [col0, col0 + NC) of fp32 from TMEM lane to the same columns of an fp32 row (zeros
+// when `have` is false: no product wrote the accumulator).  `have` must be the same in every
+// lane of the warp (tcgen05.ld is warp-collective); only lanes with `valid` store.
+template <int NC>
+__device__ __forceinline__ void bwd_store_cols_f32(uint32_t taddr, float* dst, bool have,
+                                                   bool valid, int col0) {
+    constexpr int CH = NC < 32 ? NC : 32;
 #pragma unroll
-    for (int cc = 0; cc < D / 64; ++cc) {
-        const int c = c0 + cc;
-        uint32_t rr[32];
+    for (int cc = 0; cc < NC / CH; ++cc) {
+        const int c = col0 + cc * CH;
+        uint32_t rr[CH];
         if (have) {
-            tmem_ld32(taddr + c * 32, rr);
+            tmem_ld_cols<CH>(taddr + c, rr);
         } else {
 #pragma unroll
-            for (int e = 0; e < 32; ++e) rr[e] = 0u;
+            for (int e = 0; e < CH; ++e) rr[e] = 0u;
         }
         if (!valid) continue;
-        float4* o = reinterpret_cast<float4*>(dst + c * 32);
+        float4* o = reinterpret_cast<float4*>(dst + c);
 #pragma unroll
-        for (int v4 = 0; v4 < 8; ++v4)
+        for (int v4 = 0; v4 < CH / 4; ++v4)
             o[v4] = make_float4(__uint_as_float(rr[4 * v4]), __uint_as_float(rr[4 * v4 + 1]),
                                 __uint_as_float(rr[4 * v4 + 2]), __uint_as_float(rr[4 * v4 + 3]));
     }
@@ -286,9 +299,13 @@ __global__ void __launch_bounds__(256) bwd_dlam_kernel(const float* __restrict__
 // the compute warps work on another, and each ring entry is released by its last product.
 //   dk/dv: per step s the issuer waits for P^T(s) (packed over S^T in TMEM) and issues
 //          dV += P^T(s) dO(s), then S^T(s+1) (after dV(s) in issue order, so it cannot
-//          overwrite P^T(s) too early); once the compute warps have read dP^T(s) it issues
-//          dP^T(s+1); once dS^T(s) is in shared memory it issues dK += dS^T(s) Q(s).  The
-//          compute warps form dS^T(s) while dV(s), S^T(s+1) and dP^T(s+1) run.
+//          overwrite P^T(s) too early); once dS^T(s) is packed over dP^T(s) in TMEM it
+//          issues dK += dS^T(s) Q(s) and then dP^T(s+1), which overwrites dS^T(s) only after
+//          dK(s) in issue order.  The compute warps form dS^T(s) while dV(s) and S^T(s+1)
+//          run, and P^T(s+1) while dK(s) and dP^T(s+1) run.  With both A operands of the
+//          accumulating products in TMEM, a step reads 64 KiB less of shared memory, whose
+//          128 bytes per cycle the S-type products (both operands from shared memory) and the
+//          TMA fills otherwise nearly exhaust.
 //   dq:    S has two TMEM regions, so S(s+1) is issued at the start of step s; dP(s+1)
 //          once dP(s) has been read; dQ += dS(s) K(s) once dS(s) (packed over S(s)) is in.
 // Every barrier completes at most one phase ahead of its waiters: each next phase needs an
@@ -375,7 +392,6 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) attn_bwd_kernel(const __grid_c
         mbar_init(bar(L::BAR_DPREADY), 1);
         mbar_init(bar(L::BAR_P), BWD_COMPUTE_WARPS);
         mbar_init(bar(L::BAR_DPL), BWD_COMPUTE_WARPS);
-        mbar_init(bar(L::BAR_DSFREE), 1);
         mbar_init(bar(L::BAR_FIN), 1);
         *abort_flag = 0;
         fence_barrier_init();
@@ -501,8 +517,11 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) attn_bwd_kernel(const __grid_c
         auto mn_b = [&](uint32_t tile, int k) -> uint64_t {
             return smem_desc_sw128(tile, BN * 128, 1024) + (uint64_t)((k * 2048) >> 4);
         };
-        // packed pairs of k-step k of P^T / dS / dS^T in TMEM: columns (k / 4) 64 + (k % 4) 8
-        auto pcol = [](int k) -> uint32_t { return (uint32_t)((k >> 2) * 64 + (k & 3) * 8); };
+        // packed pairs of k-step k of P^T / dS in TMEM: each compute warp packs its BWD_CW
+        // columns over the first half of them
+        auto pcol = [](int k) -> uint32_t {
+            return (uint32_t)((k / (BWD_CW / 16)) * BWD_CW + (k % (BWD_CW / 16)) * 8);
+        };
         bool ok = wait(bar(L::BAR_FIX), 0u);
         if (ok && n_steps > 0) ok = wait_a(0);
         if (ok && n_steps > 0) {
@@ -536,7 +555,27 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) attn_bwd_kernel(const __grid_c
                     issue_sprod(tmem_base, fa0, ring_a(s + 1));
                     mma_commit_elect(bar(L::BAR_SREADY));
                 }
-            } else if (more) {
+                // dK += dS^T Q, dS^T packed over the columns of dP^T(s)
+                ok = wait(bar(L::BAR_DS), (uint32_t)s & 1u);
+                if (!ok) break;
+                tc_fence_after();
+#pragma unroll
+                for (int k = 0; k < BN / 16; ++k)
+                    mma_ts_elect(tA2, tDP + pcol(k), mn_b(ring_a(s), k), ID_O,
+                                 (s > 0 || k > 0) ? 1u : 0u);
+                mma_commit_elect(bar(L::BAR_AEMPTY + s % L::NA));  // Q(s) read
+                if (more) {
+                    // dP^T(s+1), after dK(s) in issue order (it overwrites dS^T(s)); the
+                    // compute warps read dP^T(s) before they wrote dS^T(s)
+                    ok = wait_b(s + 1);
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_sprod(tDP, fa1, ring_b(s + 1));
+                    mma_commit_elect(bar(L::BAR_DPREADY));
+                }
+                continue;
+            }
+            if (more) {
                 // dq: S(s+1) into the other region (its last reader, dQ(s-1), went before)
                 ok = wait_a(s + 1);
                 if (!ok) break;
@@ -551,30 +590,17 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) attn_bwd_kernel(const __grid_c
                 tc_fence_after();
                 issue_sprod(tDP, fa1, ring_b(s + 1));
                 mma_commit_elect(bar(L::BAR_DPREADY));
-                if (!DKDV) mma_commit_elect(bar(L::BAR_BEMPTY + (s + 1) % L::NB));  // V(s+1) read
+                mma_commit_elect(bar(L::BAR_BEMPTY + (s + 1) % L::NB));  // V(s+1) read
             }
-            const int rd = DKDV ? 0 : (s & 1);
-            ok = wait(bar(L::BAR_DS + rd), DKDV ? ((uint32_t)s & 1u) : ((uint32_t)(s >> 1) & 1u));
+            const int rd = s & 1;
+            ok = wait(bar(L::BAR_DS + rd), (uint32_t)(s >> 1) & 1u);
             if (!ok) break;
             tc_fence_after();
-            if (DKDV) {
-                // dK += dS^T Q, dS^T from shared memory (K-major, two 64-column boxes)
-                const uint64_t ads = smem_desc_sw128(sbase + L::OFF_DS, 16, 1024);
 #pragma unroll
-                for (int k = 0; k < BN / 16; ++k) {
-                    const uint32_t offa = ((k >> 2) * (BM * 128) + (k & 3) * 32) >> 4;
-                    mma_ss_elect(tA2, ads + offa, mn_b(ring_a(s), k), ID_O,
-                                 (s > 0 || k > 0) ? 1u : 0u);
-                }
-                mma_commit_elect(bar(L::BAR_DSFREE));
-                mma_commit_elect(bar(L::BAR_AEMPTY + s % L::NA));  // Q(s) read
-            } else {
-#pragma unroll
-                for (int k = 0; k < BN / 16; ++k)  // dQ += dS K
-                    mma_ts_elect(tA1, tmem_base + 128u * (uint32_t)rd + pcol(k), mn_b(ring_a(s), k),
-                                 ID_O, (s > 0 || k > 0) ? 1u : 0u);
-                mma_commit_elect(bar(L::BAR_AEMPTY + s % L::NA));  // K(s) read
-            }
+            for (int k = 0; k < BN / 16; ++k)  // dQ += dS K
+                mma_ts_elect(tA1, tmem_base + 128u * (uint32_t)rd + pcol(k), mn_b(ring_a(s), k),
+                             ID_O, (s > 0 || k > 0) ? 1u : 0u);
+            mma_commit_elect(bar(L::BAR_AEMPTY + s % L::NA));  // K(s) read
         }
         // all issued MMAs complete: the compute warps read the accumulators, TMEM may go
         __syncwarp();
@@ -583,8 +609,9 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) attn_bwd_kernel(const __grid_c
         (void)mbar_wait_bounded(bar(L::BAR_FIN), 0u, &never, lim);
         __syncwarp();
     } else {
-        // ===================================== compute warps (0-7)
-        const int quarter = (int)(warp & 3), half = (int)(warp >> 2);
+        // ===================================== compute warps
+        const int quarter = (int)(warp & 3), part = (int)(warp >> 2);
+        const int cb = part * BWD_CW;  // this warp's first column of a step
         const int t = quarter * 32 + (int)lane;  // TMEM lane
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         const uint32_t tL = tmem_base + lane_off;
@@ -611,23 +638,23 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) attn_bwd_kernel(const __grid_c
         bool ok = true;
         for (int s = 0; s < n_steps && ok; ++s) {
             // per-column values of the step's query tile (dk/dv): lane l of this warp's chunk
-            // cc holds query column 32 (2 half + cc) + l, handed to the other lanes by shuffles
-            float lse2_c[2], delta_c[2];
+            // cc holds query column cb + 32 cc + l, handed to the other lanes by shuffles
+            float lse2_c[BWD_NCH], delta_c[BWD_NCH];
             const int ct = step_tile(s);
-            // d = 64: this warp's 64 lse2 then 64 delta values, broadcast from shared memory
-            float* lsw = reinterpret_cast<float*>(smem + L::OFF_LSE) + warp * 128;
+            // d = 64: this warp's lse2 then delta values, broadcast from shared memory
+            float* lsw = reinterpret_cast<float*>(smem + L::OFF_LSE) + warp * (2 * BWD_CW);
             if (DKDV) {
                 const int qm = step_qmat(s);
                 bwd_mu(p, qm % p.Hq, mu_l2, mu_sign);
                 const size_t base = (size_t)qm * p.N;
 #pragma unroll
-                for (int cc = 0; cc < 2; ++cc) {
-                    const int qc = ct * BM + (2 * half + cc) * 32 + (int)lane;
+                for (int cc = 0; cc < BWD_NCH; ++cc) {
+                    const int qc = ct * BM + cb + cc * 32 + (int)lane;
                     lse2_c[cc] = (qc < p.N) ? __ldg(p.lse + base + qc) * LOG2E_F - mu_l2 : 0.f;
                     delta_c[cc] = (qc < p.N) ? __ldg(p.delta + base + qc) : 0.f;
                     if (L::LSE_SMEM) {
                         lsw[cc * 32 + lane] = lse2_c[cc];
-                        lsw[64 + cc * 32 + lane] = delta_c[cc];
+                        lsw[BWD_CW + cc * 32 + lane] = delta_c[cc];
                     }
                 }
                 if (L::LSE_SMEM) __syncwarp();
@@ -662,14 +689,14 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) attn_bwd_kernel(const __grid_c
             ok = wait(bar(L::BAR_SREADY + rg), DKDV ? ((uint32_t)s & 1u) : ((uint32_t)(s >> 1) & 1u));
             if (!ok) break;
             tc_fence_after();
-            // the weights of this warp's 64 columns; a 32-column chunk wholly inside every lane's
+            // the weights of this warp's columns; a 32-column chunk wholly inside every lane's
             // allowed range (most chunks, for a window much wider than a tile) skips the mask
-            float pv[64];
+            float pv[BWD_CW];
 #pragma unroll
-            for (int cc = 0; cc < 2; ++cc) {
+            for (int cc = 0; cc < BWD_NCH; ++cc) {
                 uint32_t sr[32];
-                tmem_ld32(tS + (uint32_t)(half * 64 + cc * 32), sr);
-                const int c0 = (2 * half + cc) * 32;
+                tmem_ld32(tS + (uint32_t)(cb + cc * 32), sr);
+                const int c0 = cb + cc * 32;
                 const bool full = __all_sync(0xffffffffu, a <= c0 && bnd >= c0 + 31);
                 float l2v[32];  // the column's lse2 (dk/dv) or the row's (dq)
                 if (!DKDV) {
@@ -703,10 +730,10 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) attn_bwd_kernel(const __grid_c
                 }
             }
             if (DKDV) {
-                // P^T, packed over the first 32 of this warp's columns (already read)
+                // P^T, packed over the first half of this warp's columns (already read)
                 uint32_t pk[16];
 #pragma unroll
-                for (int cc = 0; cc < 2; ++cc) {
+                for (int cc = 0; cc < BWD_NCH; ++cc) {
 #pragma unroll
                     for (int u = 0; u < 16; ++u)
                         pk[u] = pack_bf16x2(pv[cc * 32 + 2 * u], pv[cc * 32 + 2 * u + 1]);
@@ -714,7 +741,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) attn_bwd_kernel(const __grid_c
 #pragma unroll
                         for (int u = 0; u < 16; ++u) pk[u] ^= mu_sign;
                     }
-                    tmem_st16(tS + (uint32_t)(half * 64 + cc * 16), pk);
+                    tmem_st16(tS + (uint32_t)(cb + cc * 16), pk);
                 }
                 tmem_wait_st();
                 tc_fence_before();
@@ -725,17 +752,17 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) attn_bwd_kernel(const __grid_c
             ok = wait(bar(L::BAR_DPREADY), (uint32_t)s & 1u);
             if (!ok) break;
             tc_fence_after();
-            uint32_t dsw[32];
+            uint32_t dsw[BWD_CW / 2];
 #pragma unroll
-            for (int cc = 0; cc < 2; ++cc) {
+            for (int cc = 0; cc < BWD_NCH; ++cc) {
                 uint32_t dr[32];
-                tmem_ld32(tDP + (uint32_t)(half * 64 + cc * 32), dr);
+                tmem_ld32(tDP + (uint32_t)(cb + cc * 32), dr);
                 float dlv[32];  // the column's delta (dk/dv) or the row's (dq)
                 if (!DKDV) {
 #pragma unroll
                     for (int u = 0; u < 32; ++u) dlv[u] = delta_row;
                 } else if (L::LSE_SMEM) {
-                    const float4* d4 = reinterpret_cast<const float4*>(lsw + 64 + cc * 32);
+                    const float4* d4 = reinterpret_cast<const float4*>(lsw + BWD_CW + cc * 32);
 #pragma unroll
                     for (int u4 = 0; u4 < 8; ++u4) {
                         const float4 x = d4[u4];
@@ -758,52 +785,41 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) attn_bwd_kernel(const __grid_c
             }
             if (mu_sign) {
 #pragma unroll
-                for (int u = 0; u < 32; ++u) dsw[u] ^= mu_sign;
+                for (int u = 0; u < BWD_CW / 2; ++u) dsw[u] ^= mu_sign;
             }
-            // dP has been read: the issuer may overwrite it with the next step's
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(L::BAR_DPL));
-            if (DKDV) {
-                // dS^T into shared memory: this thread's key row, this warp's 64 query columns
-                // (box `half`), 16-byte unit u of the row at u ^ (row & 7)
-                if (s > 0) {
-                    ok = wait(bar(L::BAR_DSFREE), (uint32_t)(s - 1) & 1u);
-                    if (!ok) break;
-                }
-                const uint32_t rowa = sbase + L::OFF_DS + (uint32_t)half * (BM * 128) + (uint32_t)t * 128u;
-#pragma unroll
-                for (int u = 0; u < 8; ++u)
-                    st_shared_v4(rowa + (((uint32_t)u ^ (uint32_t)(t & 7)) << 4), dsw[4 * u],
-                                 dsw[4 * u + 1], dsw[4 * u + 2], dsw[4 * u + 3]);
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar(L::BAR_DS));
-            } else {
-                // dS packed over the step's S region (columns this warp has read)
-#pragma unroll
-                for (int cc = 0; cc < 2; ++cc) {
-                    uint32_t pk[16];
-#pragma unroll
-                    for (int u = 0; u < 16; ++u) pk[u] = dsw[cc * 16 + u];
-                    tmem_st16(tS + (uint32_t)(half * 64 + cc * 16), pk);
-                }
-                tmem_wait_st();
+            // dk/dv: dS^T packed over this warp's columns of dP^T (already read); the issuer
+            // issues dP^T(s+1) after the dK product that reads it.  dq: dP has been read (the
+            // issuer may overwrite it with the next step's), and dS goes over the step's S
+            // region.
+            const uint32_t tdst = DKDV ? tDP : tS;
+            if (!DKDV) {
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(bar(L::BAR_DS + rg));
+                if (lane == 0) mbar_arrive(bar(L::BAR_DPL));
             }
+#pragma unroll
+            for (int cc = 0; cc < BWD_NCH; ++cc) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int u = 0; u < 16; ++u) pk[u] = dsw[cc * 16 + u];
+                tmem_st16(tdst + (uint32_t)(cb + cc * 16), pk);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(L::BAR_DS + rg));
         }
         if (ok) ok = wait(bar(L::BAR_FIN), 0u);
         if (ok) {
             tc_fence_after();
-            const int c0 = half * (D / 64);
-            const size_t part = (size_t)p.cchunks * p.B * p.Hkv * p.ncomp_pad * D;  // dk -> dv
+            constexpr int NC = D * BWD_CW / 128;  // accumulator columns this warp stores
+            const int c0 = part * NC;
+            const size_t dvoff = (size_t)p.cchunks * p.B * p.Hkv * p.ncomp_pad * D;  // dk -> dv
             if (COMPACT) {
                 // fp32 partial sums of this chunk (dK unscaled, as the window kernel's)
                 float* pk = p.cpart + (((size_t)chunk * p.B * p.Hkv + bz) * p.ncomp_pad + my) * D;
-                bwd_store_half_row_f32<D>(tA1, pk + part, n_steps > 0, true, c0);
-                bwd_store_half_row_f32<D>(tA2, pk, n_steps > 0, true, c0);
+                bwd_store_cols_f32<NC>(tA1, pk + dvoff, n_steps > 0, true, c0);
+                bwd_store_cols_f32<NC>(tA2, pk, n_steps > 0, true, c0);
             } else if (DKDV) {
                 const size_t row = (size_t)bz * p.N + (size_t)(valid ? my : 0);
                 // a key that is also a compact key takes the compact pass's partial sums
@@ -812,18 +828,18 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) attn_bwd_kernel(const __grid_c
                     xk = p.cpart + ((size_t)bz * p.ncomp_pad + my / p.stride) * D;
                 const size_t cstride = (size_t)p.B * p.Hkv * p.ncomp_pad * D;
                 if (p.dv32_out) {  // the first differential map: dV stays fp32 for the second
-                    bwd_store_half_row_f32<D>(tA1, p.dv32_out + row * D, true, valid, c0);
+                    bwd_store_cols_f32<NC>(tA1, p.dv32_out + row * D, true, valid, c0);
                 } else if (p.dv32_in) {  // the second map: dV of both maps, rounded once
-                    bwd_store_half_row<D>(tA1, 1.f, p.dv + row * D, valid, c0,
+                    bwd_store_cols<NC>(tA1, 1.f, p.dv + row * D, valid, c0,
                                           p.dv32_in + row * D, 1, 0);
                 } else {  // the compact partials were summed into their first chunk
-                    bwd_store_half_row<D>(tA1, 1.f, p.dv + row * D, valid, c0,
-                                          xk ? xk + part : nullptr, 1, cstride);
+                    bwd_store_cols<NC>(tA1, 1.f, p.dv + row * D, valid, c0,
+                                          xk ? xk + dvoff : nullptr, 1, cstride);
                 }
-                bwd_store_half_row<D>(tA2, p.scale, p.dk + row * D, valid, c0, xk, 1, cstride);
+                bwd_store_cols<NC>(tA2, p.scale, p.dk + row * D, valid, c0, xk, 1, cstride);
             } else {
                 const size_t row = (size_t)bz * p.N + (size_t)(valid ? my : 0);
-                bwd_store_half_row<D>(tA1, p.scale, p.dq + row * D, valid, c0);
+                bwd_store_cols<NC>(tA1, p.scale, p.dq + row * D, valid, c0);
             }
         }
     }
