@@ -112,11 +112,12 @@ struct BwdLayout {
     static constexpr int BAR_AEMPTY = 4;   // three
     static constexpr int BAR_BFULL = 7;    // three (ring B entries)
     static constexpr int BAR_BEMPTY = 10;  // three
-    static constexpr int BAR_SREADY = 13;  // S (dq: per region, two) is in TMEM
+    static constexpr int BAR_SREADY = 13;  // S is in TMEM
     static constexpr int BAR_DPREADY = 15; // dP is in TMEM
     static constexpr int BAR_P = 16;       // dk/dv: P^T is in TMEM (one arrival per warp)
-    static constexpr int BAR_DPL = 17;     // dq: dP has been read (one arrival per warp)
-    static constexpr int BAR_DS = 18;      // dS^T / dS is in TMEM (dq: per region, two)
+    static constexpr int BAR_SFREE = 17;   // dq: S has been read (one arrival per warp)
+    static constexpr int BAR_DS = 18;      // dS^T / dS is in TMEM, packed over dP
+    static constexpr int BAR_QT = 19;      // dq: Q and dO are in TMEM (one arrival per warp)
     static constexpr int BAR_FIN = 21;     // every MMA of the CTA has completed
     static constexpr int NBARS = 22;
     static constexpr int OFF_TMEM = OFF_BAR + NBARS * 8;
@@ -385,13 +386,12 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) attn_bwd_kernel(const __grid_c
             mbar_init(bar(L::BAR_BFULL + i), 1);
             mbar_init(bar(L::BAR_BEMPTY + i), 1);
         }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(bar(L::BAR_SREADY + i), 1);
-            mbar_init(bar(L::BAR_DS + i), BWD_COMPUTE_WARPS);
-        }
+        mbar_init(bar(L::BAR_SREADY), 1);
+        mbar_init(bar(L::BAR_DS), BWD_COMPUTE_WARPS);
         mbar_init(bar(L::BAR_DPREADY), 1);
         mbar_init(bar(L::BAR_P), BWD_COMPUTE_WARPS);
-        mbar_init(bar(L::BAR_DPL), BWD_COMPUTE_WARPS);
+        mbar_init(bar(L::BAR_SFREE), BWD_COMPUTE_WARPS);
+        mbar_init(bar(L::BAR_QT), BWD_COMPUTE_WARPS);
         mbar_init(bar(L::BAR_FIN), 1);
         *abort_flag = 0;
         fence_barrier_init();
@@ -488,11 +488,13 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) attn_bwd_kernel(const __grid_c
         // ===================================== MMA issuer (converged warp)
         constexpr uint32_t ID_S = idesc_bf16_f32(BM, BN, 0);
         constexpr uint32_t ID_O = idesc_bf16_f32(BM, D, 1);
-        // TMEM.  dk/dv: S^T [0,128) (P^T packed over it), dP^T [128,256), dV, dK.
-        //        dq:    S regions [0,128) and [128,256) (dS packed over them), dP [256,384), dQ.
-        const uint32_t tDP = tmem_base + (DKDV ? 128u : 256u);
-        const uint32_t tA1 = tmem_base + (DKDV ? 256u : 384u);  // dk/dv: dV;  dq: dQ
-        const uint32_t tA2 = tmem_base + 256u + (uint32_t)D;    // dk/dv: dK
+        // TMEM.  dk/dv: S^T [0,128) (P^T packed over it), dP^T [128,256) (dS^T packed over
+        //               it), dV [256,256+D), dK [256+D,256+2D).
+        //        dq:    S [0,128), dP [128,256) (dS packed over it), dQ [256,256+D), and the
+        //               A operands of S and dP: Q and dO packed in pairs, D/2 columns each.
+        const uint32_t tDP = tmem_base + 128u;
+        const uint32_t tA1 = tmem_base + 256u;                // dk/dv: dV;  dq: dQ
+        const uint32_t tA2 = tmem_base + 256u + (uint32_t)D;  // dk/dv: dK;  dq: Q, then dO
         // fixed operands: A of the two S-type products
         const uint64_t fa0 = smem_desc_sw128(sbase + L::OFF_FIX, 16, 1024);
         const uint64_t fa1 = smem_desc_sw128(sbase + L::OFF_FIX + L::TB, 16, 1024);
@@ -504,15 +506,20 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) attn_bwd_kernel(const __grid_c
         auto ring_b = [&](int s) -> uint32_t { return sbase + L::OFF_RB + (uint32_t)(s % L::NB) * L::TB; };
         auto wait_a = [&](int s) { return wait(bar(L::BAR_AFULL + s % L::NA), (uint32_t)(s / L::NA) & 1u); };
         auto wait_b = [&](int s) { return wait(bar(L::BAR_BFULL + s % L::NB), (uint32_t)(s / L::NB) & 1u); };
-        // an S-type product: D(tmem) = fixed tile (A, K-major) times ring tile (B, K-major)
-        auto issue_sprod = [&](uint32_t dst, uint64_t fa, uint32_t tile) {
+        // an S-type product: D(tmem) = fixed tile (A, K-major) times ring tile (B, K-major);
+        // dq: the fixed tile's copy in TMEM (ta, D/2 packed columns) is the A operand
+        auto issue_sprod = [&](uint32_t dst, uint64_t fa, uint32_t ta, uint32_t tile) {
             const uint64_t bd = smem_desc_sw128(tile, 16, 1024);
 #pragma unroll
             for (int k = 0; k < D / 16; ++k) {
                 const uint32_t off = ((k >> 2) * (BM * 128) + (k & 3) * 32) >> 4;
-                mma_ss_elect(dst, fa + off, bd + off, ID_S, k > 0 ? 1u : 0u);
+                if (DKDV)
+                    mma_ss_elect(dst, fa + off, bd + off, ID_S, k > 0 ? 1u : 0u);
+                else
+                    mma_ts_elect(dst, ta + (uint32_t)(k * 8), bd + off, ID_S, k > 0 ? 1u : 0u);
             }
         };
+        const uint32_t tQ = tA2, tDO = tA2 + (uint32_t)(D / 2);  // dq
         // a ring tile as the MN-major B operand (N = d, K = the tile's 128 rows) of k-step k
         auto mn_b = [&](uint32_t tile, int k) -> uint64_t {
             return smem_desc_sw128(tile, BN * 128, 1024) + (uint64_t)((k * 2048) >> 4);
@@ -523,15 +530,16 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) attn_bwd_kernel(const __grid_c
             return (uint32_t)((k / (BWD_CW / 16)) * BWD_CW + (k % (BWD_CW / 16)) * 8);
         };
         bool ok = wait(bar(L::BAR_FIX), 0u);
+        if (ok && !DKDV) ok = wait(bar(L::BAR_QT), 0u);  // dq: Q and dO copied into TMEM
         if (ok && n_steps > 0) ok = wait_a(0);
         if (ok && n_steps > 0) {
             tc_fence_after();
-            issue_sprod(tmem_base, fa0, ring_a(0));  // S(0) (dq: region 0)
+            issue_sprod(tmem_base, fa0, tQ, ring_a(0));  // S(0)
             mma_commit_elect(bar(L::BAR_SREADY));
             ok = wait_b(0);
             if (ok) {
                 tc_fence_after();
-                issue_sprod(tDP, fa1, ring_b(0));  // dP(0)
+                issue_sprod(tDP, fa1, tDO, ring_b(0));  // dP(0)
                 mma_commit_elect(bar(L::BAR_DPREADY));
                 if (!DKDV) mma_commit_elect(bar(L::BAR_BEMPTY));  // dq: V(0) read
             }
@@ -552,7 +560,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) attn_bwd_kernel(const __grid_c
                     ok = wait_a(s + 1);
                     if (!ok) break;
                     tc_fence_after();
-                    issue_sprod(tmem_base, fa0, ring_a(s + 1));
+                    issue_sprod(tmem_base, fa0, 0u, ring_a(s + 1));
                     mma_commit_elect(bar(L::BAR_SREADY));
                 }
                 // dK += dS^T Q, dS^T packed over the columns of dP^T(s)
@@ -570,37 +578,38 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) attn_bwd_kernel(const __grid_c
                     ok = wait_b(s + 1);
                     if (!ok) break;
                     tc_fence_after();
-                    issue_sprod(tDP, fa1, ring_b(s + 1));
+                    issue_sprod(tDP, fa1, 0u, ring_b(s + 1));
                     mma_commit_elect(bar(L::BAR_DPREADY));
                 }
                 continue;
             }
+            // dq: S(s+1) once the compute warps have read S(s) (its weights stay in their
+            // registers); dQ += dS(s) K(s) once dS(s) is packed over dP(s); then dP(s+1),
+            // which overwrites dS(s) only after dQ(s) in issue order
             if (more) {
-                // dq: S(s+1) into the other region (its last reader, dQ(s-1), went before)
-                ok = wait_a(s + 1);
+                ok = wait(bar(L::BAR_SFREE), (uint32_t)s & 1u);
+                if (ok) ok = wait_a(s + 1);
                 if (!ok) break;
                 tc_fence_after();
-                issue_sprod(tmem_base + 128u * (uint32_t)((s + 1) & 1), fa0, ring_a(s + 1));
-                mma_commit_elect(bar(L::BAR_SREADY + ((s + 1) & 1)));
+                issue_sprod(tmem_base, fa0, tQ, ring_a(s + 1));
+                mma_commit_elect(bar(L::BAR_SREADY));
             }
-            ok = wait(bar(L::BAR_DPL), (uint32_t)s & 1u);  // dP(s) has been read
-            if (ok && more) ok = wait_b(s + 1);
-            if (!ok) break;
-            if (more) {
-                tc_fence_after();
-                issue_sprod(tDP, fa1, ring_b(s + 1));
-                mma_commit_elect(bar(L::BAR_DPREADY));
-                mma_commit_elect(bar(L::BAR_BEMPTY + (s + 1) % L::NB));  // V(s+1) read
-            }
-            const int rd = s & 1;
-            ok = wait(bar(L::BAR_DS + rd), (uint32_t)(s >> 1) & 1u);
+            ok = wait(bar(L::BAR_DS), (uint32_t)s & 1u);
             if (!ok) break;
             tc_fence_after();
 #pragma unroll
             for (int k = 0; k < BN / 16; ++k)  // dQ += dS K
-                mma_ts_elect(tA1, tmem_base + 128u * (uint32_t)rd + pcol(k), mn_b(ring_a(s), k),
-                             ID_O, (s > 0 || k > 0) ? 1u : 0u);
+                mma_ts_elect(tA1, tDP + pcol(k), mn_b(ring_a(s), k), ID_O,
+                             (s > 0 || k > 0) ? 1u : 0u);
             mma_commit_elect(bar(L::BAR_AEMPTY + s % L::NA));  // K(s) read
+            if (more) {
+                ok = wait_b(s + 1);
+                if (!ok) break;
+                tc_fence_after();
+                issue_sprod(tDP, fa1, tDO, ring_b(s + 1));
+                mma_commit_elect(bar(L::BAR_DPREADY));
+                mma_commit_elect(bar(L::BAR_BEMPTY + (s + 1) % L::NB));  // V(s+1) read
+            }
         }
         // all issued MMAs complete: the compute warps read the accumulators, TMEM may go
         __syncwarp();
@@ -615,8 +624,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) attn_bwd_kernel(const __grid_c
         const int t = quarter * 32 + (int)lane;  // TMEM lane
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         const uint32_t tL = tmem_base + lane_off;
-        const uint32_t tDP = tL + (DKDV ? 128u : 256u);
-        const uint32_t tA1 = tL + (DKDV ? 256u : 384u);
+        const uint32_t tDP = tL + 128u;
+        const uint32_t tA1 = tL + 256u;
         const uint32_t tA2 = tL + 256u + (uint32_t)D;
         const int my = t0 + t;  // dk/dv: this thread's key (compact: key index r);  dq: its row
         const bool valid = COMPACT ? (my < p.ncomp_pad) : (my < p.N);
@@ -636,6 +645,38 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) attn_bwd_kernel(const __grid_c
             return __all_sync(0xffffffffu, r);
         };
         bool ok = true;
+        if (!DKDV) {
+            // dq: this thread's rows of Q and dO into TMEM, bf16 packed in pairs (the A operands
+            // of S and dP): the D packed columns of both are split among the lane quarter's four
+            // warps, 16-column pieces read from the swizzled tiles (unit u of row t at u ^ (t & 7))
+            ok = wait(bar(L::BAR_FIX), 0u);
+            if (ok) {
+#pragma unroll
+                for (int piece = 0; piece < D / 64; ++piece) {
+                    const int gc = part * (D / 4) + piece * 16;  // packed column over Q then dO
+                    const int tile = gc / (D / 2), pc = gc % (D / 2);
+                    const int e0 = 2 * pc;                       // first element of the piece
+                    const uint8_t* row = smem + L::OFF_FIX + tile * L::TB + (e0 / 64) * (BM * 128) +
+                                         t * 128;
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int unit = (e0 % 64) / 8 + u;
+                        const uint4 x =
+                            *reinterpret_cast<const uint4*>(row + ((unit ^ (t & 7)) << 4));
+                        pk[4 * u] = x.x;
+                        pk[4 * u + 1] = x.y;
+                        pk[4 * u + 2] = x.z;
+                        pk[4 * u + 3] = x.w;
+                    }
+                    tmem_st16(tA2 + (uint32_t)gc, pk);
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar(L::BAR_QT));
+            }
+        }
         for (int s = 0; s < n_steps && ok; ++s) {
             // per-column values of the step's query tile (dk/dv): lane l of this warp's chunk
             // cc holds query column cb + 32 cc + l, handed to the other lanes by shuffles
@@ -684,9 +725,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) attn_bwd_kernel(const __grid_c
                 bnd = my - k0;
             }
             if (!valid) bnd = -1;
-            const int rg = DKDV ? 0 : (s & 1);  // S region of the step
-            const uint32_t tS = tL + 128u * (uint32_t)rg;
-            ok = wait(bar(L::BAR_SREADY + rg), DKDV ? ((uint32_t)s & 1u) : ((uint32_t)(s >> 1) & 1u));
+            const uint32_t tS = tL;
+            ok = wait(bar(L::BAR_SREADY), (uint32_t)s & 1u);
             if (!ok) break;
             tc_fence_after();
             // the weights of this warp's columns; a 32-column chunk wholly inside every lane's
@@ -696,6 +736,12 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) attn_bwd_kernel(const __grid_c
             for (int cc = 0; cc < BWD_NCH; ++cc) {
                 uint32_t sr[32];
                 tmem_ld32(tS + (uint32_t)(cb + cc * 32), sr);
+                if (!DKDV && cc == BWD_NCH - 1) {
+                    // dq: S has been read; the issuer may overwrite it with S(s+1)
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(bar(L::BAR_SFREE));
+                }
                 const int c0 = cb + cc * 32;
                 const bool full = __all_sync(0xffffffffu, a <= c0 && bnd >= c0 + 31);
                 float l2v[32];  // the column's lse2 (dk/dv) or the row's (dq)
@@ -787,27 +833,19 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) attn_bwd_kernel(const __grid_c
 #pragma unroll
                 for (int u = 0; u < BWD_CW / 2; ++u) dsw[u] ^= mu_sign;
             }
-            // dk/dv: dS^T packed over this warp's columns of dP^T (already read); the issuer
-            // issues dP^T(s+1) after the dK product that reads it.  dq: dP has been read (the
-            // issuer may overwrite it with the next step's), and dS goes over the step's S
-            // region.
-            const uint32_t tdst = DKDV ? tDP : tS;
-            if (!DKDV) {
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar(L::BAR_DPL));
-            }
+            // dS^T (dk/dv) or dS (dq) packed over this warp's columns of dP (already read); the
+            // issuer issues dP(s+1) after the dK / dQ product that reads it
 #pragma unroll
             for (int cc = 0; cc < BWD_NCH; ++cc) {
                 uint32_t pk[16];
 #pragma unroll
                 for (int u = 0; u < 16; ++u) pk[u] = dsw[cc * 16 + u];
-                tmem_st16(tdst + (uint32_t)(cb + cc * 16), pk);
+                tmem_st16(tDP + (uint32_t)(cb + cc * 16), pk);
             }
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar(L::BAR_DS + rg));
+            if (lane == 0) mbar_arrive(bar(L::BAR_DS));
         }
         if (ok) ok = wait(bar(L::BAR_FIN), 0u);
         if (ok) {
