@@ -642,7 +642,8 @@ def bench_workload(args, w, ws, rank, dev, want_cpu, want_e2e):
         kname = (f"2 x bwd_delta_kernel<{w.d}> + 2 x attn_bwd_kernel<{w.d},0> + 2 x "
                  f"attn_bwd_kernel<{w.d},1> + bwd_dlam_kernel, one call")
     elif w.kind == "decode":
-        kname = "decode_split_kernel + decode_combine_kernel"
+        kname = (f"decode_mma_kernel<{w.Hq // w.Hkv}> + decode_combine_kernel<{w.d}>" if w.d == 128
+                 else f"decode_split_kernel<{w.d}> + decode_combine_kernel<{w.d}>")
     elif w.kind == "group":
         kname = (f"attn_fwd_kernel<{w.d},0>, {w.stride} launches with W={w.W} and one with "
                  f"W=N per step")

@@ -101,8 +101,9 @@ struct BwdLayout {
     static constexpr int OFF_RA = 2 * TB;
     static constexpr int OFF_RB = OFF_RA + NA * TB;
     static constexpr int OFF_DS = OFF_RB + NB * TB;
-    // d = 64 dk/dv kinds: each compute warp's 64 query columns of lse2 and delta, read as
-    // broadcasts instead of warp shuffles (at d = 128 the 2 KiB do not fit)
+    // d = 64 dk/dv kinds: each compute warp's query columns of lse2 and delta, read as
+    // broadcasts instead of warp shuffles (at d = 128 they would displace a ring entry, and
+    // measured no faster)
     static constexpr bool LSE_SMEM = (KIND == 0) && (D == 64);
     static constexpr int OFF_LSE = OFF_DS;
     static constexpr int LSE_BYTES = LSE_SMEM ? BWD_COMPUTE_WARPS * 2 * BWD_CW * 4 : 0;
