@@ -637,7 +637,8 @@ def bench_workload(args, w, ws, rank, dev, want_cpu, want_e2e):
                  f"attn_bwd_kernel<{w.d},1> (dq), one call")
     elif w.kind == "strided_bwd":
         kname = (f"bwd_delta_kernel<{w.d}> + attn_bwd_kernel<{w.d},2> (dk, dv of the strided "
-                 f"keys) + attn_bwd_kernel<{w.d},0> + attn_bwd_kernel<{w.d},1>, one call")
+                 f"keys) + bwd_compact_reduce_kernel + attn_bwd_kernel<{w.d},0> + "
+                 f"attn_bwd_kernel<{w.d},1>, one call")
     elif w.kind == "diff_bwd":
         kname = (f"2 x bwd_delta_kernel<{w.d}> + 2 x attn_bwd_kernel<{w.d},0> + 2 x "
                  f"attn_bwd_kernel<{w.d},1> + bwd_dlam_kernel, one call")
@@ -671,7 +672,7 @@ def bench_workload(args, w, ws, rank, dev, want_cpu, want_e2e):
         "data": "synthetic", "config": workload_config(w, fl, flush),
         "pct_of_bf16_peak": 100.0 * achieved_tf / bf16_peak,
         "roofline": roofline,
-        "gpu_launches": args.steps * {"decode": 2, "bwd": 3, "strided_bwd": 4, "diff_bwd": 7,
+        "gpu_launches": args.steps * {"decode": 2, "bwd": 3, "strided_bwd": 5, "diff_bwd": 7,
                                       "group": w.stride + 1}.get(w.kind, 1),
         "clocks": clk,
     }
