@@ -502,14 +502,36 @@ __global__ void __launch_bounds__(D) decode_combine_kernel(const __grid_constant
     const int posb = p.pos[b];
     const int nvalid = posb < 0 ? 0 : min(posb + 1, p.W);
     const int ns = (nvalid + DEC_KS - 1) / DEC_KS;
-    const float* ml = p.part_ml + (size_t)bh * p.nsplit * 2;
+    const float* __restrict__ ml = p.part_ml + (size_t)bh * p.nsplit * 2;
+    const float* __restrict__ po = p.part_o + (size_t)bh * p.nsplit * D + c;
+    // splits in batches of eight: the loads of a batch are issued together (one after the
+    // other they would expose a memory latency per split); the sums keep the split order
     float mx = -INFINITY;
-    for (int s = 0; s < ns; ++s) mx = fmaxf(mx, ml[2 * s]);
+    for (int s0 = 0; s0 < ns; s0 += 8) {
+        float mv[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) mv[u] = (s0 + u < ns) ? __ldg(ml + 2 * (s0 + u)) : -INFINITY;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) mx = fmaxf(mx, mv[u]);
+    }
     float l = 0.f, o = 0.f;
-    for (int s = 0; s < ns; ++s) {
-        const float w = exp2f(ml[2 * s] - mx);
-        l += ml[2 * s + 1] * w;
-        o += p.part_o[((size_t)bh * p.nsplit + s) * D + c] * w;
+    for (int s0 = 0; s0 < ns; s0 += 8) {
+        float mv[8], lv[8], ov[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const bool in = s0 + u < ns;
+            mv[u] = in ? __ldg(ml + 2 * (s0 + u)) : 0.f;
+            lv[u] = in ? __ldg(ml + 2 * (s0 + u) + 1) : 0.f;
+            ov[u] = in ? __ldg(po + (size_t)(s0 + u) * D) : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            if (s0 + u < ns) {
+                const float w = exp2f(mv[u] - mx);
+                l += lv[u] * w;
+                o += ov[u] * w;
+            }
+        }
     }
     p.out[(size_t)bh * D + c] = __float2bfloat16_rn(l > 0.f ? o / l : 0.f);
 }
