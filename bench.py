@@ -64,13 +64,20 @@ PREFILL_CYCLES = 20e6  # about 10 ms of device spin ahead of the timed launches 
 # (KERNEL_SOURCES of its family) when it was taken.  A changed kernel invalidates the figure
 # (reported as null).
 TRAFFIC = {
-    "mistral_swa": (331.90e6, "fcec546b72b2890d"),
-    "gemma_swa": (858.72e6, "fcec546b72b2890d"),
-    "strided": (113.64e6, "fcec546b72b2890d"),
-    "diff": (96.09e6, "fcec546b72b2890d"),
-    "diff_swa": (191.63e6, "fcec546b72b2890d"),
-    "global": (114.90e6, "fcec546b72b2890d"),
-    "mistral_decode": (486.76e6, "86fc03c18c809f41"),
+    "mistral_swa": (330.08e6, "bab5edd6da3da24c"),
+    "gemma_swa": (858.89e6, "bab5edd6da3da24c"),
+    "strided": (112.66e6, "bab5edd6da3da24c"),
+    "diff": (95.20e6, "bab5edd6da3da24c"),
+    "diff_swa": (190.66e6, "bab5edd6da3da24c"),
+    "global": (114.67e6, "bab5edd6da3da24c"),
+    "swa_small": (0.47e6, "bab5edd6da3da24c"),
+    # the backward calls: every kernel of one call (delta, dk/dv, dq, and the compact-key and
+    # differential extras); Q, dO, K and V are read by both the dk/dv and the dq kernel
+    "mistral_swa_bwd": (1123.83e6, "e3a68e1c0fc23834"),
+    "strided_bwd": (483.22e6, "e3a68e1c0fc23834"),
+    "diff_swa_bwd": (886.61e6, "e3a68e1c0fc23834"),
+    # both decode kernels of one step
+    "mistral_decode": (501.14e6, "042df2ba8a4b42f8"),
 }
 
 
