@@ -681,6 +681,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) attn_bwd_kernel(const __grid_c
         for (int s = 0; s < n_steps && ok; ++s) {
             // per-column values of the step's query tile (dk/dv): lane l of this warp's chunk
             // cc holds query column cb + 32 cc + l, handed to the other lanes by shuffles
+            // (every lane reading all of them with broadcast loads measured slower at d = 128)
             float lse2_c[BWD_NCH], delta_c[BWD_NCH];
             const int ct = step_tile(s);
             // d = 64: this warp's lse2 then delta values, broadcast from shared memory
@@ -745,34 +746,42 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) attn_bwd_kernel(const __grid_c
                 }
                 const int c0 = cb + cc * 32;
                 const bool full = __all_sync(0xffffffffu, a <= c0 && bnd >= c0 + 31);
-                float l2v[32];  // the column's lse2 (dk/dv) or the row's (dq)
-                if (!DKDV) {
+                // in two 16-column pieces, so that a piece's lse values need few registers
 #pragma unroll
-                    for (int u = 0; u < 32; ++u) l2v[u] = lse2_row;
-                } else if (L::LSE_SMEM) {
-                    const float4* l4 = reinterpret_cast<const float4*>(lsw + cc * 32);
+                for (int h = 0; h < 2; ++h) {
+                    float l2v[16];  // the column's lse2 (dk/dv) or the row's (dq)
+                    if (!DKDV) {
 #pragma unroll
-                    for (int u4 = 0; u4 < 8; ++u4) {
-                        const float4 x = l4[u4];
-                        l2v[4 * u4] = x.x;
-                        l2v[4 * u4 + 1] = x.y;
-                        l2v[4 * u4 + 2] = x.z;
-                        l2v[4 * u4 + 3] = x.w;
+                        for (int u = 0; u < 16; ++u) l2v[u] = lse2_row;
+                    } else if (L::LSE_SMEM) {
+                        const float4* l4 = reinterpret_cast<const float4*>(lsw + cc * 32 + 16 * h);
+#pragma unroll
+                        for (int u4 = 0; u4 < 4; ++u4) {
+                            const float4 x = l4[u4];
+                            l2v[4 * u4] = x.x;
+                            l2v[4 * u4 + 1] = x.y;
+                            l2v[4 * u4 + 2] = x.z;
+                            l2v[4 * u4 + 3] = x.w;
+                        }
+                    } else {
+#pragma unroll
+                        for (int u = 0; u < 16; ++u)
+                            l2v[u] = __shfl_sync(0xffffffffu, lse2_c[cc], 16 * h + u);
                     }
-                } else {
+                    if (full) {
 #pragma unroll
-                    for (int u = 0; u < 32; ++u) l2v[u] = __shfl_sync(0xffffffffu, lse2_c[cc], u);
-                }
-                if (full) {
+                        for (int u = 0; u < 16; ++u)
+                            pv[cc * 32 + 16 * h + u] =
+                                fast_exp2(fmaf(__uint_as_float(sr[16 * h + u]), sl2, -l2v[u]));
+                    } else {
 #pragma unroll
-                    for (int u = 0; u < 32; ++u)
-                        pv[cc * 32 + u] = fast_exp2(fmaf(__uint_as_float(sr[u]), sl2, -l2v[u]));
-                } else {
-#pragma unroll
-                    for (int u = 0; u < 32; ++u) {
-                        const bool in = (c0 + u >= a) && (c0 + u <= bnd);
-                        pv[cc * 32 + u] =
-                            in ? fast_exp2(fmaf(__uint_as_float(sr[u]), sl2, -l2v[u])) : 0.f;
+                        for (int u = 0; u < 16; ++u) {
+                            const int col = c0 + 16 * h + u;
+                            const bool in = (col >= a) && (col <= bnd);
+                            pv[cc * 32 + 16 * h + u] =
+                                in ? fast_exp2(fmaf(__uint_as_float(sr[16 * h + u]), sl2, -l2v[u]))
+                                   : 0.f;
+                        }
                     }
                 }
             }
@@ -804,30 +813,36 @@ __global__ void __launch_bounds__(BWD_THREADS, 1) attn_bwd_kernel(const __grid_c
             for (int cc = 0; cc < BWD_NCH; ++cc) {
                 uint32_t dr[32];
                 tmem_ld32(tDP + (uint32_t)(cb + cc * 32), dr);
-                float dlv[32];  // the column's delta (dk/dv) or the row's (dq)
-                if (!DKDV) {
 #pragma unroll
-                    for (int u = 0; u < 32; ++u) dlv[u] = delta_row;
-                } else if (L::LSE_SMEM) {
-                    const float4* d4 = reinterpret_cast<const float4*>(lsw + BWD_CW + cc * 32);
+                for (int h = 0; h < 2; ++h) {
+                    float dlv[16];  // the column's delta (dk/dv) or the row's (dq)
+                    if (!DKDV) {
 #pragma unroll
-                    for (int u4 = 0; u4 < 8; ++u4) {
-                        const float4 x = d4[u4];
-                        dlv[4 * u4] = x.x;
-                        dlv[4 * u4 + 1] = x.y;
-                        dlv[4 * u4 + 2] = x.z;
-                        dlv[4 * u4 + 3] = x.w;
+                        for (int u = 0; u < 16; ++u) dlv[u] = delta_row;
+                    } else if (L::LSE_SMEM) {
+                        const float4* d4 =
+                            reinterpret_cast<const float4*>(lsw + BWD_CW + cc * 32 + 16 * h);
+#pragma unroll
+                        for (int u4 = 0; u4 < 4; ++u4) {
+                            const float4 x = d4[u4];
+                            dlv[4 * u4] = x.x;
+                            dlv[4 * u4 + 1] = x.y;
+                            dlv[4 * u4 + 2] = x.z;
+                            dlv[4 * u4 + 3] = x.w;
+                        }
+                    } else {
+#pragma unroll
+                        for (int u = 0; u < 16; ++u)
+                            dlv[u] = __shfl_sync(0xffffffffu, delta_c[cc], 16 * h + u);
                     }
-                } else {
 #pragma unroll
-                    for (int u = 0; u < 32; ++u) dlv[u] = __shfl_sync(0xffffffffu, delta_c[cc], u);
-                }
-#pragma unroll
-                for (int u = 0; u < 16; ++u) {
-                    const float d0 = pv[cc * 32 + 2 * u] * (__uint_as_float(dr[2 * u]) - dlv[2 * u]);
-                    const float d1 =
-                        pv[cc * 32 + 2 * u + 1] * (__uint_as_float(dr[2 * u + 1]) - dlv[2 * u + 1]);
-                    dsw[cc * 16 + u] = pack_bf16x2(d0, d1);
+                    for (int u = 0; u < 8; ++u) {
+                        const int e = cc * 32 + 16 * h + 2 * u;
+                        const float d0 = pv[e] * (__uint_as_float(dr[16 * h + 2 * u]) - dlv[2 * u]);
+                        const float d1 =
+                            pv[e + 1] * (__uint_as_float(dr[16 * h + 2 * u + 1]) - dlv[2 * u + 1]);
+                        dsw[cc * 16 + 8 * h + u] = pack_bf16x2(d0, d1);
+                    }
                 }
             }
             if (mu_sign) {
