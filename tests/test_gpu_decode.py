@@ -54,10 +54,14 @@ def _random_case(B, Hq, Hkv, W, d, pos, seed):
 
 
 @pytest.mark.parametrize("d", [64, 128])
-@pytest.mark.parametrize("heads", [(1, 1), (4, 1), (8, 2), (6, 2), (16, 1), (32, 8), (3, 3)])
+@pytest.mark.parametrize("heads", [(1, 1), (2, 1), (4, 1), (8, 2), (6, 2), (7, 1), (8, 1), (16, 1),
+                                   (32, 8), (3, 3)])
 def test_decode_sweep(d, heads):
+    """Every query-head group size the kernels are built for (1, 2, 4, 8, 16, padded from 3,
+    6, 7); W from one slot to nine splits of 128 (the combine takes the splits eight at a
+    time), ragged last splits included."""
     Hq, Hkv = heads
-    for W in (1, 7, 128, 129, 300):
+    for W in (1, 7, 128, 129, 300, 1100):
         pos = [0, max(0, W - 2), W - 1, W, 5 * W + 3]
         q, kc, vc = _random_case(len(pos), Hq, Hkv, W, d, pos, seed=W * 31 + Hq + d)
         scale = 1.0 / np.sqrt(d)
