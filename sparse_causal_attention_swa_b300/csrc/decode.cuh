@@ -35,10 +35,7 @@
 
 namespace swa {
 
-#ifndef SWA_DEC_KS
-#define SWA_DEC_KS 128
-#endif
-constexpr int DEC_KS = SWA_DEC_KS;   // cache slots per split, one thread per slot
+constexpr int DEC_KS = 128;  // cache slots per split, one thread per slot (and MMA row)
 constexpr int DEC_THREADS = DEC_KS;
 constexpr int DEC_WARPS = DEC_KS / 32;
 
