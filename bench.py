@@ -77,7 +77,7 @@ TRAFFIC = {
     "strided_bwd": (482.47e6, "e02ff1c9980b2060"),
     "diff_swa_bwd": (886.65e6, "e02ff1c9980b2060"),
     # both decode kernels of one step
-    "mistral_decode": (500.9e6, "7ee8fc5376977c77"),
+    "mistral_decode": (501.19e6, "795ae1706564fbfa"),
 }
 
 
