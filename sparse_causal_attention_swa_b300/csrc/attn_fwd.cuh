@@ -105,7 +105,7 @@ template <int D, int MODE>
 struct SmemLayout {
     static constexpr int QBYTES = BM * D * 2;
     static constexpr int EBYTES = BN * D * 2;  // one ring entry: a K or V tile
-    static constexpr int STAGES = (D == 128) ? 4 : 10;
+    static constexpr int STAGES = (D == 128) ? 4 : 11;
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_RING = 2 * QBYTES;
     // epilogue staging: one output tile, 128 rows x D bf16 as D/64 boxes of 64 columns
