@@ -64,13 +64,13 @@ PREFILL_CYCLES = 20e6  # about 10 ms of device spin ahead of the timed launches 
 # (KERNEL_SOURCES of its family) when it was taken.  A changed kernel invalidates the figure
 # (reported as null).
 TRAFFIC = {
-    "mistral_swa": (330.08e6, "bab5edd6da3da24c"),
-    "gemma_swa": (858.89e6, "bab5edd6da3da24c"),
-    "strided": (112.66e6, "bab5edd6da3da24c"),
-    "diff": (95.20e6, "bab5edd6da3da24c"),
-    "diff_swa": (190.66e6, "bab5edd6da3da24c"),
-    "global": (114.67e6, "bab5edd6da3da24c"),
-    "swa_small": (0.47e6, "bab5edd6da3da24c"),
+    "mistral_swa": (326.28e6, "b2c86708711f2362"),
+    "gemma_swa": (860.15e6, "b2c86708711f2362"),
+    "strided": (112.13e6, "b2c86708711f2362"),
+    "diff": (94.26e6, "b2c86708711f2362"),
+    "diff_swa": (190.63e6, "b2c86708711f2362"),
+    "global": (113.54e6, "b2c86708711f2362"),
+    "swa_small": (0.48e6, "b2c86708711f2362"),
     # the backward calls: every kernel of one call (delta, dk/dv, dq, and the compact-key and
     # differential extras); Q, dO, K and V are read by both the dk/dv and the dq kernel
     "mistral_swa_bwd": (1121.20e6, "e02ff1c9980b2060"),
