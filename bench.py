@@ -73,9 +73,9 @@ TRAFFIC = {
     "swa_small": (0.48e6, "b2c86708711f2362"),
     # the backward calls: every kernel of one call (delta, dk/dv, dq, and the compact-key and
     # differential extras); Q, dO, K and V are read by both the dk/dv and the dq kernel
-    "mistral_swa_bwd": (1121.20e6, "e02ff1c9980b2060"),
-    "strided_bwd": (482.47e6, "e02ff1c9980b2060"),
-    "diff_swa_bwd": (886.65e6, "e02ff1c9980b2060"),
+    "mistral_swa_bwd": (1124.93e6, "14ee695434112f38"),
+    "strided_bwd": (481.59e6, "14ee695434112f38"),
+    "diff_swa_bwd": (886.35e6, "14ee695434112f38"),
     # both decode kernels of one step
     "mistral_decode": (501.19e6, "795ae1706564fbfa"),
 }
